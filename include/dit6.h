@@ -1,0 +1,214 @@
+/*
+ * dit6.h -- C ABI of libdit6, the GB300 (sm_103a) hot path of the dynamically routed
+ * NVFP4 / INT8 linear layer of a video diffusion transformer block, with its Temporal
+ * Delta Cache.
+ *
+ * Method: "6Bit-Diffusion: Inference-Time Mixed-Precision Quantization for Video Diffusion
+ * Models" (arXiv 2603.18742).  Passages are cited by page and section:
+ *   [EN]  gist.science summary (English)   [IT] gist.science summary (Italian)
+ *   [ZH]  gist.science summary (Chinese)   [ABS] the authors' abstract (chatpaper.ai)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named *_dev or passed as tensors are DEVICE pointers owned by the caller.
+ *   Pointers documented as "host" are read synchronously during the call.
+ * - The library never allocates, frees or synchronises.  Every call only enqueues work on
+ *   `stream` and returns.  The return code covers argument errors found on the host;
+ *   errors found on the device (a bounded wait that ran out) are OR-ed into the status
+ *   word at byte 0 of the workspace (see dit_ws_status_offset), which the caller reads
+ *   after synchronising.
+ * - Workspace: `ws` is a caller-owned device buffer of at least dit_workspace_bytes()
+ *   bytes, zero-filled once by the caller before its first use.  The kernels keep it in a
+ *   reusable state (every counter they bump is reset by the same launch).  Two calls that
+ *   run concurrently on the GPU must not share one workspace.
+ * - Tensors are row-major and contiguous.  Activation and delta tensors are bf16 or fp32
+ *   (dit_dtype).  Device pointers must be 32-byte aligned (256-bit vector loads).
+ * - All entry points are thread-compatible (no global mutable state except a cached
+ *   driver entry point).
+ */
+#ifndef DIT6_H_
+#define DIT6_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dit_stream_t; /* == cudaStream_t; NULL is the legacy stream */
+
+typedef enum {
+  DIT_OK = 0,
+  DIT_ERR_INVALID_ARG = 1, /* a null pointer, a negative or inconsistent size */
+  DIT_ERR_ALIGNMENT = 2,   /* a device pointer is not 32-byte aligned */
+  DIT_ERR_UNSUPPORTED = 3, /* a shape the kernels do not cover (see each call) */
+  DIT_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed at launch */
+  DIT_ERR_TIMEOUT = 5      /* device status bit: a bounded wait inside a kernel ran out */
+} dit_status;
+
+typedef enum { DIT_F32 = 0, DIT_BF16 = 1 } dit_dtype;
+typedef enum { DIT_ROUTE_NVFP4 = 0, DIT_ROUTE_INT8 = 1 } dit_route;
+typedef enum { DIT_TDC_COMMIT = 0, DIT_TDC_SKIP = 1 } dit_tdc_mode;
+
+#define DIT_MAX_LAYERS 16
+
+/* Human-readable name of a status code (static storage). */
+const char* dit_status_str(dit_status s);
+
+/* Library version, "major.minor.patch" (static storage). */
+const char* dit_version(void);
+
+/* Bytes of workspace every call below needs (a constant; it holds a status word, a
+ * completion counter and per-CTA partial sums). */
+size_t dit_workspace_bytes(void);
+
+/* Byte offset, inside the workspace, of the uint32 device status word (bit i set means
+ * status code i was raised on the device since the caller last cleared it). */
+size_t dit_ws_status_offset(void);
+
+/* ------------------------------------------------------------------------------------
+ * (a1 + a2) Gamma predictor and routing.
+ * [EN] 2. Methodology, A. DMPQ, Mechanism 1-3; [IT] 2.A Meccanismo / Routing Dinamico.
+ *
+ * Gamma = sum|x_out - x_in| / sum|x_in| over all n elements (the relative L1 distance of a
+ * block's output and input at the previous step), then for each of n_layers linear layers
+ * E_rel = alpha[l] * Gamma + beta[l] and route[l] = INT8 if E_rel > thr[l] else NVFP4.
+ * Per-thread fp32 partial sums, fp64 across threads and CTAs in a fixed order (the result
+ * is bit-reproducible run to run); E_rel and the comparison in fp64.
+ *
+ * x_in, x_out : device, n elements of dtype dt.
+ * alpha, beta, thr : HOST arrays of n_layers floats (1 <= n_layers <= DIT_MAX_LAYERS).
+ * gamma_dev   : device float, receives Gamma (sum|x_in| = 0: 0 if the numerator is 0 else
+ *               +inf).
+ * routes_dev  : device int32[n_layers], receives dit_route values.
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_gamma_route(const void* x_in, const void* x_out, dit_dtype dt, int64_t n,
+                           const float* alpha, const float* beta, const float* thr,
+                           int n_layers, float* gamma_dev, int32_t* routes_dev, void* ws,
+                           size_t ws_bytes, dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * (a3 + a4) Online block Hadamard transform fused with NVFP4 quantisation.
+ * [EN] 2.A "Outlier Smoothing" (block Hadamard on local activation blocks);
+ * [IT] "3. Contributi Chiave" 4 (NVFP4 = E2M1); [ZH] 2.A (weights quantised offline).
+ *
+ * y = x (H_b / sqrt(b)) on every contiguous block of b elements along K (Sylvester order,
+ * fp32 butterflies in stages h = 1, 2, ..., b/2, then the 1/sqrt(b) scale), then
+ *   s_g = amax|y| / 2688 (whole tensor; or *tensor_scale_in when that is not NULL)
+ *   s_b = E4M3_rne_sat(amax_b / (6 s_g))       per 16 elements
+ *   q   = E2M1_rne_sat(y * rcp(dec(s_b) s_g))  per element
+ *
+ * x      : device [rows x k] of dtype dt; k % 64 == 0; hblock in {16, 32, 64}.
+ * codes  : device [rows x k/2] bytes, element 2i in the low nibble, 2i+1 in the high.
+ * sf     : device, dit_sf_bytes(rows, k) bytes; E4M3 scales in the tile layout of
+ *          dit_sf_index (rows padded to 128 are written with zeros).
+ * tensor_scale_dev : device float, receives s_g.
+ * tensor_scale_in  : device float or NULL.  NULL -> two passes over x (amax, then
+ *          quantise); non-NULL -> one pass with the given s_g (values beyond the range
+ *          saturate).
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_hadamard_quant_nvfp4(const void* x, dit_dtype dt, int64_t rows, int64_t k,
+                                    int hblock, uint8_t* codes, uint8_t* sf,
+                                    float* tensor_scale_dev, const float* tensor_scale_in,
+                                    void* ws, size_t ws_bytes, dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * (a3 + a5) Online block Hadamard transform fused with per-token INT8 quantisation.
+ * [EN] 2.A Mechanism 3 (the INT8 route), "Outlier Smoothing".
+ *
+ * y as above; per row s = amax_row|y| / 127, q = round_half_even(y * rcp(s)) in
+ * [-127, 127]; an all-zero row gives s = 0 and q = 0.  The same call quantises weights
+ * per output channel (rows of W).
+ *
+ * x     : device [rows x k] of dtype dt; k % 64 == 0, k <= 65536; hblock in {16,32,64}.
+ * q     : device int8 [rows x k].     row_scale : device float [rows].
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_hadamard_quant_int8(const void* x, dit_dtype dt, int64_t rows, int64_t k,
+                                   int hblock, int8_t* q, float* row_scale,
+                                   dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * (a6) NVFP4 GEMM on the block-scaled tensor cores (tcgen05 kind::mxf4nvf4).
+ * [EN] 1. Problem Statement "Hardware Gap", 3. Key Contributions 4 (NVFP4 on Blackwell).
+ *
+ * Y[m, n] = (*a_gs) (*b_gs) sum_k dec(A)[m,k] dec(sA)[m,k/16] dec(B)[n,k] dec(sB)[n,k/16]
+ *           (+ bias[n])
+ * a, b   : device packed E2M1, [m x k/2] and [n x k/2] (both K-major, as written by
+ *          dit_hadamard_quant_nvfp4); a_sf, b_sf: tile-layout scales; a_gs, b_gs: device
+ *          floats (the tensor scales).  k % 64 == 0; n % 8 == 0.
+ * bias   : device float [n] or NULL.     y : device [m x n] of dtype y_dt.
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
+                           const uint8_t* b, const uint8_t* b_sf, const float* b_gs,
+                           int64_t m, int64_t n, int64_t k, const float* bias, void* y,
+                           dit_dtype y_dt, void* ws, size_t ws_bytes, dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * (a7) INT8 GEMM: exact int32 accumulation, per-row x per-column dequantisation.
+ * [EN] 2.A Mechanism 3 (INT8 route); [ZH] 2.A weight handling.
+ *
+ * acc[m, n] = sum_k a[m, k] b[n, k] (int32, exact);
+ * Y[m, n]   = (float(acc) * a_scale[m]) * b_scale[n] (+ bias[n]).
+ * a : device int8 [m x k]; b : device int8 [n x k]; k % 16 == 0; n % 8 == 0.
+ * acc_debug : device int32 [m x n] or NULL (writes the raw accumulators as well).
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_qgemm_int8(const int8_t* a, const float* a_scale, const int8_t* b,
+                          const float* b_scale, int64_t m, int64_t n, int64_t k,
+                          const float* bias, void* y, dit_dtype y_dt, int32_t* acc_debug,
+                          void* ws, size_t ws_bytes, dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * (a8 / a10) Temporal Delta Cache device step.
+ * [EN] 2.B (TDC); [IT] 2.B "Riuso" (X_out,t ~= X_in,t + Delta_{t-1}).
+ *
+ * mode DIT_TDC_COMMIT (a compute step just produced x_out):
+ *   delta = store(x_out - x_in) -> d_new        (fp32 difference, then dtype dt)
+ *   *gamma_dev = sum|x_out - x_in| / sum|x_in|  (Gamma_t, fp64 final ratio)
+ *   *sim_dev   = sum|delta - d1| / sum|d1|      (relative L1 of the last two computed
+ *                deltas; d1 may be NULL, then *sim_dev = +inf)
+ * mode DIT_TDC_SKIP: x_out_skip = store(x_in + d1); gamma_dev / sim_dev untouched.
+ * n elements; d_new must not alias d1 (the caller keeps a two-slot ring and swaps).
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_tdc_step(int mode, const void* x_in, const void* x_out, void* x_out_skip,
+                        const void* d1, void* d_new, dit_dtype dt, int64_t n,
+                        float* gamma_dev, float* sim_dev, void* ws, size_t ws_bytes,
+                        dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * (a9 + a11) Host-side delta-cache decision and PDR routing (no device work).
+ * [EN] 2.B "Error Control"; [EN] 2.C second bullet (INT8 after a skip); [ZH] 2.C.
+ *
+ * decide: n_computed < 2 -> COMMIT (compute); e_acc + d <= tau -> SKIP; else compute.
+ * update after a SKIP: e_acc += d, gamma_valid = 0.
+ * update after a compute: e_acc = 0, n_computed++, d = sim (if finite-or-first), gamma =
+ *   the step's Gamma, gamma_valid = 1.
+ * route: gamma_valid ? (alpha*gamma+beta > thr ? INT8 : NVFP4) : INT8 for every layer.
+ * ------------------------------------------------------------------------------------ */
+typedef struct {
+  int64_t n_computed;
+  double e_acc;
+  double d;       /* +inf until two deltas have been computed */
+  double gamma;   /* Gamma of the last step (valid iff gamma_valid) */
+  int gamma_valid;
+} dit_tdc_state;
+
+void dit_tdc_state_init(dit_tdc_state* st);
+int dit_tdc_decide(const dit_tdc_state* st, double tau); /* returns dit_tdc_mode */
+void dit_tdc_update(dit_tdc_state* st, int mode, double gamma, double sim, int has_sim);
+void dit_route_host(const dit_tdc_state* st, const float* alpha, const float* beta,
+                    const float* thr, int n_layers, int32_t* routes);
+
+/* ------------------------------------------------------------------------------------
+ * Block-scale tile layout helpers (host).  The scales of a [rows x k] NVFP4 tensor are
+ * cut into atoms of 128 rows x 4 scale columns (512 bytes), ordered with the scale-column
+ * atom index fastest; inside an atom row r, column c is at (r%32)*16 + ((r%128)/32)*4 +
+ * c%4.  This is the operand layout of the block-scaled tcgen05 MMA.
+ * ------------------------------------------------------------------------------------ */
+int64_t dit_sf_index(int64_t row, int64_t kblock, int64_t rows, int64_t k);
+size_t dit_sf_bytes(int64_t rows, int64_t k);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DIT6_H_ */

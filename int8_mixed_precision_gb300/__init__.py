@@ -1,0 +1,228 @@
+"""Python binding of libdit6: the GB300 routed NVFP4/INT8 linear layer + Temporal Delta Cache.
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+``csrc/`` behind the C ABI declared in ``include/dit6.h``.  PyTorch supplies device memory
+and the current stream.  There is no fallback: if the library is missing, every call
+raises ``LibraryMissing``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from ._lib import LibraryMissing, lib, library_path  # noqa: F401
+
+ROUTE_NVFP4 = 0
+ROUTE_INT8 = 1
+TDC_COMMIT = 0
+TDC_SKIP = 1
+MAX_LAYERS = 16
+
+
+class DitError(RuntimeError):
+    pass
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dt(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise DitError(f"unsupported dtype {t.dtype}")
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise DitError(f"{what}: {lib().dit_status_str(status).decode()}")
+
+
+def status_str(code: int) -> str:
+    return lib().dit_status_str(code).decode()
+
+
+def version() -> str:
+    return lib().dit_version().decode()
+
+
+def workspace_bytes() -> int:
+    return int(lib().dit_workspace_bytes())
+
+
+def workspace(device="cuda"):
+    """A zero-filled workspace buffer (uint8) for one stream of calls."""
+    return _torch().zeros(workspace_bytes(), dtype=_torch().uint8, device=device)
+
+
+def device_status(ws) -> int:
+    """The OR of (1 << status) raised on the device since the workspace was last cleared
+    (synchronises with the device)."""
+    off = int(lib().dit_ws_status_offset())
+    return int(ws[off:off + 4].view(_torch().int32).item())
+
+
+def clear_device_status(ws) -> None:
+    off = int(lib().dit_ws_status_offset())
+    ws[off:off + 4].zero_()
+
+
+def sf_bytes(rows: int, k: int) -> int:
+    return int(lib().dit_sf_bytes(rows, k))
+
+
+def sf_index(row: int, kblock: int, rows: int, k: int) -> int:
+    return int(lib().dit_sf_index(row, kblock, rows, k))
+
+
+# ----------------------------------------------------------------------------------------
+# device entry points
+# ----------------------------------------------------------------------------------------
+
+
+def gamma_route(x_in, x_out, alpha, beta, thr, gamma, routes, ws, stream=None):
+    """Gamma = |x_out - x_in|_1 / |x_in|_1 and per-layer routes (device outputs)."""
+    n = len(alpha)
+    arr = ctypes.c_float * max(n, 1)
+    st = lib().dit_gamma_route(_p(x_in), _p(x_out), _dt(x_in), x_in.numel(), arr(*alpha),
+                               arr(*beta), arr(*thr), n, _p(gamma), _p(routes), _p(ws),
+                               ws.numel(), _stream(stream))
+    _check(st, "dit_gamma_route")
+
+
+def hadamard_quant_nvfp4(x, hblock, codes, sf, tensor_scale, ws, tensor_scale_in=None, stream=None):
+    rows, k = x.shape
+    st = lib().dit_hadamard_quant_nvfp4(_p(x), _dt(x), rows, k, hblock, _p(codes), _p(sf),
+                                        _p(tensor_scale), _p(tensor_scale_in), _p(ws), ws.numel(),
+                                        _stream(stream))
+    _check(st, "dit_hadamard_quant_nvfp4")
+
+
+def hadamard_quant_int8(x, hblock, q, row_scale, stream=None):
+    rows, k = x.shape
+    st = lib().dit_hadamard_quant_int8(_p(x), _dt(x), rows, k, hblock, _p(q), _p(row_scale),
+                                       _stream(stream))
+    _check(st, "dit_hadamard_quant_int8")
+
+
+def qgemm_nvfp4(a, a_sf, a_gs, b, b_sf, b_gs, y, ws, bias=None, stream=None):
+    m, n, k = a.shape[0], b.shape[0], a.shape[1] * 2
+    st = lib().dit_qgemm_nvfp4(_p(a), _p(a_sf), _p(a_gs), _p(b), _p(b_sf), _p(b_gs), m, n, k,
+                               _p(bias), _p(y), _dt(y), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dit_qgemm_nvfp4")
+
+
+def qgemm_int8(a, a_scale, b, b_scale, y, ws, bias=None, acc_debug=None, stream=None):
+    m, n, k = a.shape[0], b.shape[0], a.shape[1]
+    st = lib().dit_qgemm_int8(_p(a), _p(a_scale), _p(b), _p(b_scale), m, n, k, _p(bias), _p(y),
+                              _dt(y), _p(acc_debug), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dit_qgemm_int8")
+
+
+def tdc_step(mode, x_in, ws, x_out=None, x_out_skip=None, d1=None, d_new=None, gamma=None,
+             sim=None, stream=None):
+    st = lib().dit_tdc_step(mode, _p(x_in), _p(x_out), _p(x_out_skip), _p(d1), _p(d_new),
+                            _dt(x_in), x_in.numel(), _p(gamma), _p(sim), _p(ws), ws.numel(),
+                            _stream(stream))
+    _check(st, "dit_tdc_step")
+
+
+# ----------------------------------------------------------------------------------------
+# host-side delta-cache state machine (C implementation, no device work)
+# ----------------------------------------------------------------------------------------
+
+
+class TdcState(ctypes.Structure):
+    _fields_ = [("n_computed", ctypes.c_int64), ("e_acc", ctypes.c_double),
+                ("d", ctypes.c_double), ("gamma", ctypes.c_double), ("gamma_valid", ctypes.c_int)]
+
+    def __init__(self):
+        super().__init__()
+        lib().dit_tdc_state_init(ctypes.byref(self))
+
+    def decide(self, tau: float) -> int:
+        return int(lib().dit_tdc_decide(ctypes.byref(self), tau))
+
+    def update(self, mode: int, gamma: float = 0.0, sim: float | None = None) -> None:
+        has = sim is not None
+        lib().dit_tdc_update(ctypes.byref(self), mode, float(gamma), float(sim if has else math.inf),
+                             int(has))
+
+    def routes(self, alpha, beta, thr) -> list[int]:
+        n = len(alpha)
+        arr = ctypes.c_float * n
+        out = (ctypes.c_int32 * n)()
+        lib().dit_route_host(ctypes.byref(self), arr(*alpha), arr(*beta), arr(*thr), n, out)
+        return list(out)
+
+
+# ----------------------------------------------------------------------------------------
+# buffer helpers (torch device memory) and one routed linear layer
+# ----------------------------------------------------------------------------------------
+
+
+def alloc_nvfp4(rows: int, k: int, device="cuda") -> dict:
+    torch = _torch()
+    return {"codes": torch.empty(rows, k // 2, dtype=torch.uint8, device=device),
+            "sf": torch.empty(sf_bytes(rows, k), dtype=torch.uint8, device=device),
+            "gs": torch.empty(1, dtype=torch.float32, device=device)}
+
+
+def alloc_int8(rows: int, k: int, device="cuda") -> dict:
+    torch = _torch()
+    return {"q": torch.empty(rows, k, dtype=torch.int8, device=device),
+            "scale": torch.empty(rows, dtype=torch.float32, device=device)}
+
+
+class QuantizedWeight:
+    """A weight W [N x K] prepared offline in both formats (block Hadamard along K, then an
+    NVFP4 copy and a per-output-channel INT8 copy), all on the device."""
+
+    def __init__(self, w, hblock: int, ws):
+        n, k = w.shape
+        self.n, self.k, self.hblock = n, k, hblock
+        self.nvfp4 = alloc_nvfp4(n, k, w.device)
+        self.int8 = alloc_int8(n, k, w.device)
+        hadamard_quant_nvfp4(w, hblock, self.nvfp4["codes"], self.nvfp4["sf"], self.nvfp4["gs"], ws)
+        hadamard_quant_int8(w, hblock, self.int8["q"], self.int8["scale"])
+
+
+class RoutedLinear:
+    """Y = quant(X H) quant(W H)^T along a route chosen per call; the activation buffers for
+    both routes are allocated once for a maximum token count."""
+
+    def __init__(self, weight: QuantizedWeight, max_tokens: int, ws, device="cuda"):
+        self.w = weight
+        self.ws = ws
+        self.a4 = alloc_nvfp4(max_tokens, weight.k, device)
+        self.a8 = alloc_int8(max_tokens, weight.k, device)
+
+    def __call__(self, x, route: int, y, bias=None, tensor_scale_in=None, stream=None):
+        m = x.shape[0]
+        w = self.w
+        if route == ROUTE_INT8:
+            q, s = self.a8["q"][:m], self.a8["scale"][:m]
+            hadamard_quant_int8(x, w.hblock, q, s, stream=stream)
+            qgemm_int8(q, s, w.int8["q"], w.int8["scale"], y, self.ws, bias=bias, stream=stream)
+        else:
+            c = self.a4["codes"][:m]
+            hadamard_quant_nvfp4(x, w.hblock, c, self.a4["sf"], self.a4["gs"], self.ws,
+                                 tensor_scale_in=tensor_scale_in, stream=stream)
+            qgemm_nvfp4(c, self.a4["sf"], self.a4["gs"], w.nvfp4["codes"], w.nvfp4["sf"],
+                        w.nvfp4["gs"], y, self.ws, bias=bias, stream=stream)
+        return y

@@ -1,0 +1,262 @@
+// Shared device helpers of libdit6 (sm_103a): vector memory ops, packed fp32x2 math,
+// FP4/FP8 conversions, mbarrier / TMA / bounded waits, and the workspace layout.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dit6.h"
+
+namespace dit6 {
+
+// ---------------------------------------------------------------------------------------
+// Workspace layout (caller-owned, zero-filled once; the kernels keep it reusable)
+// ---------------------------------------------------------------------------------------
+constexpr size_t WS_STATUS = 0;      // uint32: OR of (1 << dit_status) raised on device
+constexpr size_t WS_TICKET = 4;      // uint32: CTA completion counter (reset by last CTA)
+constexpr size_t WS_AMAX = 8;        // uint32: float bits of a running amax (reset)
+constexpr size_t WS_SG = 12;         // float : tensor scale produced by the amax pass
+constexpr size_t WS_PARTIALS = 256;  // double[MAX_RED_CTAS][4]
+constexpr int MAX_RED_CTAS = 1024;
+constexpr size_t WS_BYTES = 65536;
+
+// Device-side bounded waits give up after this many nanoseconds of %globaltimer.
+constexpr uint64_t WAIT_LIMIT_NS = 1000ull * 1000ull * 1000ull;  // 1 s
+
+__device__ __forceinline__ uint32_t* ws_u32(void* ws, size_t off) {
+  return reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(ws) + off);
+}
+__device__ __forceinline__ double* ws_partials(void* ws) {
+  return reinterpret_cast<double*>(reinterpret_cast<char*>(ws) + WS_PARTIALS);
+}
+__device__ __forceinline__ void raise_status(void* ws, int code) {
+  atomicOr(ws_u32(ws, WS_STATUS), 1u << code);
+}
+
+// ---------------------------------------------------------------------------------------
+// 256-bit global memory access (sm_100+), read-only path for streamed inputs
+// ---------------------------------------------------------------------------------------
+struct alignas(32) U8x32 {
+  uint32_t w[8];
+};
+
+__device__ __forceinline__ U8x32 ld256_nc(const void* p) {
+  U8x32 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]),
+                 "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st256(void* p, const U8x32& r) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r.w[0]),
+               "r"(r.w[1]), "r"(r.w[2]), "r"(r.w[3]), "r"(r.w[4]), "r"(r.w[5]), "r"(r.w[6]),
+               "r"(r.w[7])
+               : "memory");
+}
+
+// bf16 pair (element 2i in the low half) -> two floats, exact
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// two floats -> bf16 pair, round to nearest even
+__device__ __forceinline__ uint32_t f2_to_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------------------------------
+// packed fp32x2 arithmetic (one instruction for two lanes, no contraction)
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t r, x, y;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+  float2 o;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+  return o;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  uint64_t r, x, y;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+  float2 o;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+  return o;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t r, x, y;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+  float2 o;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+  return o;
+}
+
+// ---------------------------------------------------------------------------------------
+// In-thread fast Walsh-Hadamard transform of 64 values held as 32 pairs (2p, 2p+1).
+// Stage h = 1, 2, ..., HB/2 turns every pair (i, i+h) with bit h of i clear into
+// (a + b, a - b): the stage order of the Sylvester factorisation, fp32 round-to-nearest.
+// ---------------------------------------------------------------------------------------
+template <int HB>
+__device__ __forceinline__ void fwht64(float2 (&v)[32]) {
+  static_assert(HB == 16 || HB == 32 || HB == 64, "block size");
+#pragma unroll
+  for (int p = 0; p < 32; ++p) {  // h = 1: inside a pair
+    float a = v[p].x, b = v[p].y;
+    v[p].x = __fadd_rn(a, b);
+    v[p].y = __fsub_rn(a, b);
+  }
+#pragma unroll
+  for (int h = 2; h < HB; h <<= 1) {
+    const int hp = h >> 1;  // distance in pairs
+#pragma unroll
+    for (int p = 0; p < 32; ++p) {
+      if (((2 * p) & h) == 0) {
+        float2 a = v[p], b = v[p + hp];
+        v[p] = add2(a, b);
+        v[p + hp] = sub2(a, b);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// FP4 / FP8 conversions (documented PTX cvt instructions)
+// ---------------------------------------------------------------------------------------
+// E2M1 of two floats: `lo` in the low nibble, `hi` in the high nibble; RN-even, saturating
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+// E4M3 code of a float (RN-even, saturating to 448)
+__device__ __forceinline__ uint32_t e4m3_code(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  return r & 0xffu;
+}
+// value of an E4M3 code (exact)
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  uint32_t h2;
+  uint16_t c = (uint16_t)code;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+}
+
+// ---------------------------------------------------------------------------------------
+// warp / block reductions
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ---------------------------------------------------------------------------------------
+// mbarrier, TMA and timing primitives
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, "
+      "p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of `parity` to complete; give up after WAIT_LIMIT_NS (or at once when
+// *abort is set by another role), raising DIT_ERR_TIMEOUT.  Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, void* ws,
+                                          volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+        raise_status(ws, DIT_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 2-D tiled TMA load into shared memory, completion counted on `bar`
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+}  // namespace dit6
+
+// ---------------------------------------------------------------------------------------
+// host-side helpers (defined in api.cu)
+// ---------------------------------------------------------------------------------------
+namespace dit6 {
+int num_sms();  // SM count of the current device (cached per device)
+bool aligned32(const void* p);
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda needed)
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base, uint64_t inner,
+                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                    CUtensorMapSwizzle swz);
+}  // namespace dit6
+
+#define DIT_CHECK_LAUNCH()                                  \
+  do {                                                      \
+    if (cudaGetLastError() != cudaSuccess) return DIT_ERR_CUDA; \
+  } while (0)

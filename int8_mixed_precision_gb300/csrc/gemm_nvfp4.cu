@@ -1,0 +1,342 @@
+// NVFP4 GEMM of the NVFP4 route on the 5th-generation tensor cores.
+//
+// 6Bit-Diffusion (arXiv 2603.18742): [EN] gist.science "1. Problem Statement" (Hardware
+// Gap: Blackwell supports the NVFP4 micro-scaling format), "3. Key Contributions" 4;
+// [IT] "3. Contributi Chiave" 4 (NVFP4 = E2M1).
+//
+// Y[m,n] = s_gA s_gB sum_k dec(A)[m,k] dec(sA)[m,k/16] dec(B)[n,k] dec(sB)[n,k/16]
+//
+// Design (sm_103a): tcgen05.mma kind::mxf4nvf4 block_scale scale_vec::4X (E2M1 operands,
+// UE4M3 scales per 16 elements, fp32 accumulator in tensor memory).  Warp-specialised CTA:
+//   warp 0  : TMA producer -- 2-D tiled loads (128-byte swizzle) of the packed A/B tiles and
+//             1-D bulk copies of the matching 512-byte scale atoms, into a STAGES-deep ring
+//             guarded by full/empty mbarriers;
+//   warp 1  : allocates tensor memory; one lane copies each K=64 step's scales from shared
+//             to tensor memory (tcgen05.cp 32x128b.warpx4) and issues the MMA; a
+//             tcgen05.commit per stage frees the ring slot;
+//   warps 2-5: epilogue -- tcgen05.ld of the accumulator (one TMEM lane quarter each),
+//             global scale (+bias), bf16/fp32 conversion, 256-bit stores.
+// Every mbarrier wait is bounded (%globaltimer); on expiry the CTA records
+// DIT_ERR_TIMEOUT in the workspace, lets in-flight copies and MMAs land, frees its tensor
+// memory and exits.
+#include "common.cuh"
+
+namespace dit6 {
+namespace f4 {
+
+constexpr int BM = 128;
+constexpr int BK = 256;              // E2M1 elements per stage (128 bytes per row)
+constexpr int KSTEP = 64;            // elements per MMA
+constexpr int A_BYTES = BM * BK / 2;  // 16 KB
+constexpr int SF_ATOM = 512;          // 128 rows x 4 scales
+
+template <int BN, int STAGES>
+struct Cfg {
+  static constexpr int NB = BN / 128;                 // 128-row scale atoms of B per stage
+  static constexpr int B_BYTES = BN * BK / 2;
+  static constexpr int SFA_BYTES = 4 * SF_ATOM;       // 4 K-steps
+  static constexpr int SFB_BYTES = NB * 4 * SF_ATOM;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int SF_COLS = 4 + 4 * NB;          // TMEM columns per K-step's scales
+  static constexpr int TMEM_USED = BN + STAGES * 4 * SF_COLS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
+  static_assert(TMEM_USED <= 512, "tensor memory");
+};
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused for SW128 K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128 >> 4) << 32;  // 8 rows x 16 B core matrices, stacked along rows
+  d |= (uint64_t)1 << 46;
+  return d;  // no swizzle
+}
+// instruction descriptor: E2M1 x E2M1, UE4M3 scales, fp32 accumulate, K-major A and B
+__host__ __device__ constexpr uint32_t idesc_nvf4(int m, int n) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
+      "[%5], p; }" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int BN, int STAGES, bool SPLIT_N>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
+                 const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
+                 int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
+                 void* ws) {
+  using C = Cfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t sbase = smem_u32(smem);
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + STAGES + s); };
+  const uint32_t tmem_full = smem_u32(bars + 2 * STAGES);
+  auto a_tile = [&](int s) { return sbase + s * C::STAGE_BYTES; };
+  auto b_tile = [&](int s) { return a_tile(s) + A_BYTES; };
+  auto sfa_tile = [&](int s) { return b_tile(s) + C::B_BYTES; };
+  auto sfb_tile = [&](int s) { return sfa_tile(s) + C::SFA_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int ksteps = K / KSTEP;
+  const int num_kb = (ksteps + 3) / 4;
+  const int k_atoms = K / KSTEP;  // scale atoms per 128-row block along K
+  int nb_valid = (N - n0 + 127) / 128;
+  if (nb_valid > C::NB) nb_valid = C::NB;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(tmem_full, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {  // -------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      int issued = 0;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % STAGES;
+        if (!mbar_wait(empty(s), ((kb / STAGES) & 1) ^ 1, ws, abort_flag)) break;
+        const int nsub = min(4, ksteps - kb * 4);
+        const uint32_t bytes = A_BYTES + C::B_BYTES + nsub * SF_ATOM * (1 + nb_valid);
+        mbar_expect_tx(full(s), bytes);
+        tma_load_2d(a_tile(s), &tmA, full(s), kb * (BK / 2), m0);
+        tma_load_2d(b_tile(s), &tmB, full(s), kb * (BK / 2), n0);
+        bulk_load(sfa_tile(s), a_sf + ((size_t)(m0 / 128) * k_atoms + kb * 4) * SF_ATOM,
+                  nsub * SF_ATOM, full(s));
+        for (int nb = 0; nb < nb_valid; ++nb)
+          bulk_load(sfb_tile(s) + nb * 4 * SF_ATOM,
+                    b_sf + ((size_t)(n0 / 128 + nb) * k_atoms + kb * 4) * SF_ATOM,
+                    nsub * SF_ATOM, full(s));
+        issued = kb + 1;
+      }
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        for (int kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
+          mbar_wait(full(kb % STAGES), (kb / STAGES) & 1, ws, &no_abort);
+      }
+    }
+  } else if (warp == 1) {  // ------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr int MMA_N = SPLIT_N ? 128 : BN;
+      constexpr uint32_t idesc = idesc_nvf4(BM, MMA_N);
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % STAGES;
+        if (!mbar_wait(full(s), (kb / STAGES) & 1, ws, abort_flag)) break;
+        tc_fence_after();
+        const int nsub = min(4, ksteps - kb * 4);
+        for (int j = 0; j < nsub; ++j) {
+          const uint32_t sfa_col = BN + (s * 4 + j) * C::SF_COLS;
+          const uint32_t sfb_col = sfa_col + 4;
+          tc_cp_sf(tmem + sfa_col, desc_sf(sfa_tile(s) + j * SF_ATOM));
+          for (int nb = 0; nb < nb_valid; ++nb)
+            tc_cp_sf(tmem + sfb_col + 4 * nb, desc_sf(sfb_tile(s) + nb * 4 * SF_ATOM + j * SF_ATOM));
+          const uint64_t ad = desc_sw128(a_tile(s) + j * 32);
+          const uint32_t accum = (kb | j) != 0;
+          if (SPLIT_N) {
+#pragma unroll
+            for (int h = 0; h < C::NB; ++h)
+              tc_mma(tmem + h * 128, ad, desc_sw128(b_tile(s) + h * 128 * 128 + j * 32), idesc,
+                     tmem + sfa_col, tmem + sfb_col + 4 * h, accum);
+          } else {
+            tc_mma(tmem, ad, desc_sw128(b_tile(s) + j * 32), idesc, tmem + sfa_col,
+                   tmem + sfb_col, accum);
+          }
+        }
+        tc_commit(empty(s));
+      }
+      tc_commit(tmem_full);
+      if (*abort_flag) {  // make sure issued MMAs have finished before TMEM is freed
+        volatile int no_abort = 0;
+        mbar_wait(tmem_full, 0, ws, &no_abort);
+      }
+    }
+    __syncwarp();
+  } else {  // ----------------------------------------------------- epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = m0 + q * 32 + lane;
+    const bool ok = mbar_wait(tmem_full, 0, ws, abort_flag);
+    tc_fence_after();
+    if (ok) {
+      const float alpha = __fmul_rn(*a_gs, *b_gs);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, r);
+        const int col0 = n0 + c * 32;
+        if (row >= M || col0 >= N) continue;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
+          if (bias && col0 + i < N) v[i] = __fadd_rn(v[i], bias[col0 + i]);
+        }
+        const int64_t off = (int64_t)row * N + col0;
+        if (col0 + 32 <= N && (N % 16) == 0) {
+          if (y_bf16) {
+            U8x32 o0, o1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              o0.w[i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
+              o1.w[i] = f2_to_bf16x2(v[16 + 2 * i], v[16 + 2 * i + 1]);
+            }
+            uint16_t* yp = reinterpret_cast<uint16_t*>(y) + off;
+            st256(yp, o0);
+            st256(yp + 16, o1);
+          } else {
+            float* yp = reinterpret_cast<float*>(y) + off;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              U8x32 o;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o.w[i] = __float_as_uint(v[8 * b + i]);
+              st256(yp + 8 * b, o);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (col0 + i >= N) continue;
+            if (y_bf16)
+              reinterpret_cast<__nv_bfloat16*>(y)[off + i] = __float2bfloat16_rn(v[i]);
+            else
+              reinterpret_cast<float*>(y)[off + i] = v[i];
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+template <int BN, int STAGES, bool SPLIT_N>
+static dit_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf,
+                         const uint8_t* b_sf, const float* a_gs, const float* b_gs, int M, int N,
+                         int K, const float* bias, void* y, int y_bf16, void* ws,
+                         cudaStream_t st) {
+  using C = Cfg<BN, STAGES>;
+  static bool attr_done = false;
+  auto kern = k_gemm_nvfp4<BN, STAGES, SPLIT_N>;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
+      return DIT_ERR_CUDA;
+    attr_done = true;
+  }
+  dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
+  if (grid.y > 65535) return DIT_ERR_UNSUPPORTED;
+  kern<<<grid, 192, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y, y_bf16, ws);
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
+}  // namespace f4
+}  // namespace dit6
+
+using namespace dit6;
+
+// Tile configuration, selectable for experiments through DIT6_NVFP4_TILE (0 = default).
+static int nvfp4_tile_cfg() {
+  const char* e = getenv("DIT6_NVFP4_TILE");
+  return e ? atoi(e) : 0;
+}
+
+extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
+                                      const uint8_t* b, const uint8_t* b_sf, const float* b_gs,
+                                      int64_t m, int64_t n, int64_t k, const float* bias, void* y,
+                                      dit_dtype y_dt, void* ws, size_t ws_bytes,
+                                      dit_stream_t stream) {
+  if (!a || !a_sf || !a_gs || !b || !b_sf || !b_gs || !y || !ws || ws_bytes < WS_BYTES)
+    return DIT_ERR_INVALID_ARG;
+  if (m <= 0 || n <= 0 || k <= 0 || m > 0x7fffffff || n > 0x7fffffff || k > 0x7fffffff)
+    return DIT_ERR_INVALID_ARG;
+  if (y_dt != DIT_F32 && y_dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
+  if (k % 64 || n % 8) return DIT_ERR_UNSUPPORTED;
+  if (!aligned32(a) || !aligned32(b) || !aligned32(a_sf) || !aligned32(b_sf) || !aligned32(y) ||
+      !aligned32(ws))
+    return DIT_ERR_ALIGNMENT;
+  const int cfg = nvfp4_tile_cfg();
+  const uint32_t bn_box = (cfg == 1 || cfg == 2) ? 256 : 128;
+  CUtensorMap ta, tb;
+  if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(k / 2),
+                      (uint64_t)m, (uint64_t)(k / 2), f4::BK / 2, f4::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(b), (uint64_t)(k / 2),
+                      (uint64_t)n, (uint64_t)(k / 2), f4::BK / 2, bn_box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return DIT_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int yb = y_dt == DIT_BF16 ? 1 : 0;
+  switch (cfg) {
+    case 1: return f4::launch<256, 3, true>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 2: return f4::launch<256, 3, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 3: return f4::launch<128, 6, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    default: return f4::launch<128, 3, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+  }
+}

@@ -1,0 +1,318 @@
+// Gamma predictor + routing and the Temporal Delta Cache device steps.
+//
+// 6Bit-Diffusion (arXiv 2603.18742): [EN] gist.science 2.A Mechanism 1-3 (Gamma, E_rel,
+// routing); 2.B (delta cache: residual delta, similarity of the last two computed deltas,
+// skip by reusing the cached delta); [IT] 2.B "Riuso" (X_out ~= X_in + Delta_{t-1}).
+//
+// Design: HBM-bound streaming reductions.  Grid = a fixed multiple of the SM count, each
+// thread walks 32-byte vectors of every input (256-bit loads), keeps fp32 partial sums,
+// the CTA folds them in fp64 and writes one partial per CTA; the last CTA to finish
+// (completion ticket) sums the partials in a fixed order, so results are bit-reproducible
+// for a given device and size, and resets the ticket for the next call.
+#include "common.cuh"
+
+namespace dit6 {
+
+constexpr int RED_THREADS = 256;
+
+struct RouteParams {
+  float alpha[DIT_MAX_LAYERS], beta[DIT_MAX_LAYERS], thr[DIT_MAX_LAYERS];
+  int n_layers;
+};
+
+// 16 elements per vector for bf16 (32 bytes), 8 for fp32
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 16;
+  static __device__ __forceinline__ void load(const void* p, int64_t i, float (&v)[16]) {
+    U8x32 r = ld256_nc(reinterpret_cast<const char*>(p) + i * 32);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float2 f = bf16x2_to_f2(r.w[k]);
+      v[2 * k] = f.x;
+      v[2 * k + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ float scalar(const void* p, int64_t i) {
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+  }
+  static __device__ __forceinline__ void store(void* p, int64_t i, const float (&v)[16]) {
+    U8x32 r;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r.w[k] = f2_to_bf16x2(v[2 * k], v[2 * k + 1]);
+    st256(reinterpret_cast<char*>(p) + i * 32, r);
+  }
+  static __device__ __forceinline__ void store_scalar(void* p, int64_t i, float v) {
+    reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+  }
+  static __device__ __forceinline__ float round_store(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+  }
+};
+template <>
+struct Vec<float> {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void load(const void* p, int64_t i, float (&v)[8]) {
+    U8x32 r = ld256_nc(reinterpret_cast<const char*>(p) + i * 32);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(r.w[k]);
+  }
+  static __device__ __forceinline__ float scalar(const void* p, int64_t i) {
+    return reinterpret_cast<const float*>(p)[i];
+  }
+  static __device__ __forceinline__ void store(void* p, int64_t i, const float (&v)[8]) {
+    U8x32 r;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r.w[k] = __float_as_uint(v[k]);
+    st256(reinterpret_cast<char*>(p) + i * 32, r);
+  }
+  static __device__ __forceinline__ void store_scalar(void* p, int64_t i, float v) {
+    reinterpret_cast<float*>(p)[i] = v;
+  }
+  static __device__ __forceinline__ float round_store(float v) { return v; }
+};
+
+// Fold NS per-thread fp32 sums into fp64 CTA partials; the last CTA reduces all partials
+// in a fixed order into out[0..NS).  Returns true in the thread that holds the result.
+template <int NS>
+__device__ bool reduce_partials(const float (&s)[NS], void* ws, double (&out)[NS]) {
+  __shared__ double sh[RED_THREADS / 32][NS];
+  __shared__ bool last;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  double d[NS];
+#pragma unroll
+  for (int i = 0; i < NS; ++i) d[i] = warp_sum_d((double)s[i]);
+  if (lane == 0)
+#pragma unroll
+    for (int i = 0; i < NS; ++i) sh[wid][i] = d[i];
+  __syncthreads();
+  double* part = ws_partials(ws);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      double b = 0.0;
+      for (int w = 0; w < RED_THREADS / 32; ++w) b += sh[w][i];
+      part[blockIdx.x * 4 + i] = b;
+    }
+    __threadfence();
+    last = atomicAdd(ws_u32(ws, WS_TICKET), 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last) return false;
+  __threadfence();
+  // fixed-order: thread t sums partials t, t+256, ...; then a fixed tree
+  double acc[NS];
+#pragma unroll
+  for (int i = 0; i < NS; ++i) acc[i] = 0.0;
+  for (int b = threadIdx.x; b < (int)gridDim.x; b += RED_THREADS)
+#pragma unroll
+    for (int i = 0; i < NS; ++i) acc[i] += __ldcg(part + b * 4 + i);
+#pragma unroll
+  for (int i = 0; i < NS; ++i) acc[i] = warp_sum_d(acc[i]);
+  __syncthreads();
+  if (lane == 0)
+#pragma unroll
+    for (int i = 0; i < NS; ++i) sh[wid][i] = acc[i];
+  __syncthreads();
+  if (threadIdx.x != 0) return false;
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    double b = 0.0;
+    for (int w = 0; w < RED_THREADS / 32; ++w) b += sh[w][i];
+    out[i] = b;
+  }
+  *ws_u32(ws, WS_TICKET) = 0u;
+  return true;
+}
+
+__device__ __forceinline__ double ratio(double num, double den) {
+  if (den == 0.0) return num == 0.0 ? 0.0 : __longlong_as_double(0x7ff0000000000000ll);
+  return num / den;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(RED_THREADS) k_gamma_route(const void* __restrict__ xi,
+                                                             const void* __restrict__ xo,
+                                                             int64_t n, RouteParams rp,
+                                                             float* gamma_out,
+                                                             int32_t* routes, void* ws) {
+  constexpr int N = Vec<T>::N;
+  const int64_t nv = n / N;
+  float s[2] = {0.f, 0.f};
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+    float a[N], b[N];
+    Vec<T>::load(xi, i, a);
+    Vec<T>::load(xo, i, b);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      s[0] += fabsf(__fsub_rn(b[k], a[k]));
+      s[1] += fabsf(a[k]);
+    }
+  }
+  for (int64_t i = nv * N + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float a = Vec<T>::scalar(xi, i), b = Vec<T>::scalar(xo, i);
+    s[0] += fabsf(__fsub_rn(b, a));
+    s[1] += fabsf(a);
+  }
+  double r[2];
+  if (!reduce_partials<2>(s, ws, r)) return;
+  const double g = ratio(r[0], r[1]);
+  *gamma_out = (float)g;
+  for (int l = 0; l < rp.n_layers; ++l) {
+    const double e = (double)rp.alpha[l] * g + (double)rp.beta[l];
+    routes[l] = e > (double)rp.thr[l] ? DIT_ROUTE_INT8 : DIT_ROUTE_NVFP4;
+  }
+}
+
+// COMMIT: delta = store(xo - xi) -> dnew; sums |xo-xi|, |xi|, |delta - d1|, |d1|
+template <typename T>
+__global__ void __launch_bounds__(RED_THREADS) k_tdc_commit(const void* __restrict__ xi,
+                                                            const void* __restrict__ xo,
+                                                            const void* __restrict__ d1,
+                                                            void* __restrict__ dnew, int64_t n,
+                                                            float* gamma_out, float* sim_out,
+                                                            void* ws) {
+  constexpr int N = Vec<T>::N;
+  const int64_t nv = n / N;
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+    float a[N], b[N], c[N], dl[N];
+    Vec<T>::load(xi, i, a);
+    Vec<T>::load(xo, i, b);
+    if (d1) Vec<T>::load(d1, i, c);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const float df = __fsub_rn(b[k], a[k]);
+      dl[k] = Vec<T>::round_store(df);
+      s[0] += fabsf(df);
+      s[1] += fabsf(a[k]);
+      if (d1) {
+        s[2] += fabsf(__fsub_rn(dl[k], c[k]));
+        s[3] += fabsf(c[k]);
+      }
+    }
+    Vec<T>::store(dnew, i, dl);
+  }
+  for (int64_t i = nv * N + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float a = Vec<T>::scalar(xi, i), b = Vec<T>::scalar(xo, i);
+    const float df = __fsub_rn(b, a);
+    const float dl = Vec<T>::round_store(df);
+    s[0] += fabsf(df);
+    s[1] += fabsf(a);
+    if (d1) {
+      const float c = Vec<T>::scalar(d1, i);
+      s[2] += fabsf(__fsub_rn(dl, c));
+      s[3] += fabsf(c);
+    }
+    Vec<T>::store_scalar(dnew, i, dl);
+  }
+  double r[4];
+  if (!reduce_partials<4>(s, ws, r)) return;
+  *gamma_out = (float)ratio(r[0], r[1]);
+  *sim_out = d1 ? (float)ratio(r[2], r[3]) : __int_as_float(0x7f800000);
+}
+
+// SKIP: out = store(xi + d1)
+template <typename T>
+__global__ void __launch_bounds__(RED_THREADS) k_tdc_skip(const void* __restrict__ xi,
+                                                          const void* __restrict__ d1,
+                                                          void* __restrict__ out, int64_t n) {
+  constexpr int N = Vec<T>::N;
+  const int64_t nv = n / N;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+    float a[N], c[N];
+    Vec<T>::load(xi, i, a);
+    Vec<T>::load(d1, i, c);
+#pragma unroll
+    for (int k = 0; k < N; ++k) a[k] = __fadd_rn(a[k], c[k]);
+    Vec<T>::store(out, i, a);
+  }
+  for (int64_t i = nv * N + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    Vec<T>::store_scalar(out, i, __fadd_rn(Vec<T>::scalar(xi, i), Vec<T>::scalar(d1, i)));
+}
+
+static unsigned red_grid(int64_t n, int per_vec) {
+  int64_t nv = n / per_vec;
+  int64_t g = (nv + RED_THREADS - 1) / RED_THREADS;
+  const int64_t cap = 4 * (int64_t)num_sms();
+  if (g > cap) g = cap;
+  if (g > MAX_RED_CTAS) g = MAX_RED_CTAS;
+  if (g < 1) g = 1;
+  return (unsigned)g;
+}
+
+}  // namespace dit6
+
+using namespace dit6;
+
+extern "C" dit_status dit_gamma_route(const void* x_in, const void* x_out, dit_dtype dt,
+                                      int64_t n, const float* alpha, const float* beta,
+                                      const float* thr, int n_layers, float* gamma_dev,
+                                      int32_t* routes_dev, void* ws, size_t ws_bytes,
+                                      dit_stream_t stream) {
+  if (!x_in || !x_out || n <= 0 || !gamma_dev || !ws || ws_bytes < WS_BYTES)
+    return DIT_ERR_INVALID_ARG;
+  if (dt != DIT_F32 && dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
+  if (n_layers < 0 || n_layers > DIT_MAX_LAYERS) return DIT_ERR_INVALID_ARG;
+  if (n_layers > 0 && (!alpha || !beta || !thr || !routes_dev)) return DIT_ERR_INVALID_ARG;
+  if (!aligned32(x_in) || !aligned32(x_out) || !aligned32(ws)) return DIT_ERR_ALIGNMENT;
+  RouteParams rp;
+  rp.n_layers = n_layers;
+  for (int l = 0; l < n_layers; ++l) {
+    rp.alpha[l] = alpha[l];
+    rp.beta[l] = beta[l];
+    rp.thr[l] = thr[l];
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == DIT_BF16)
+    k_gamma_route<__nv_bfloat16><<<red_grid(n, 16), RED_THREADS, 0, st>>>(x_in, x_out, n, rp,
+                                                                         gamma_dev, routes_dev, ws);
+  else
+    k_gamma_route<float><<<red_grid(n, 8), RED_THREADS, 0, st>>>(x_in, x_out, n, rp, gamma_dev,
+                                                               routes_dev, ws);
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
+extern "C" dit_status dit_tdc_step(int mode, const void* x_in, const void* x_out,
+                                   void* x_out_skip, const void* d1, void* d_new, dit_dtype dt,
+                                   int64_t n, float* gamma_dev, float* sim_dev, void* ws,
+                                   size_t ws_bytes, dit_stream_t stream) {
+  if (!x_in || n <= 0) return DIT_ERR_INVALID_ARG;
+  if (dt != DIT_F32 && dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int per = dt == DIT_BF16 ? 16 : 8;
+  if (mode == DIT_TDC_SKIP) {
+    if (!d1 || !x_out_skip) return DIT_ERR_INVALID_ARG;
+    if (!aligned32(x_in) || !aligned32(d1) || !aligned32(x_out_skip)) return DIT_ERR_ALIGNMENT;
+    int64_t g = (n / per + RED_THREADS - 1) / RED_THREADS;
+    const int64_t cap = 8 * (int64_t)num_sms();
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    if (dt == DIT_BF16)
+      k_tdc_skip<__nv_bfloat16><<<(unsigned)g, RED_THREADS, 0, st>>>(x_in, d1, x_out_skip, n);
+    else
+      k_tdc_skip<float><<<(unsigned)g, RED_THREADS, 0, st>>>(x_in, d1, x_out_skip, n);
+    DIT_CHECK_LAUNCH();
+    return DIT_OK;
+  }
+  if (mode != DIT_TDC_COMMIT) return DIT_ERR_INVALID_ARG;
+  if (!x_out || !d_new || !gamma_dev || !sim_dev || !ws || ws_bytes < WS_BYTES)
+    return DIT_ERR_INVALID_ARG;
+  if (d1 == d_new) return DIT_ERR_INVALID_ARG;
+  if (!aligned32(x_in) || !aligned32(x_out) || !aligned32(d_new) || (d1 && !aligned32(d1)) ||
+      !aligned32(ws))
+    return DIT_ERR_ALIGNMENT;
+  if (dt == DIT_BF16)
+    k_tdc_commit<__nv_bfloat16><<<red_grid(n, 16), RED_THREADS, 0, st>>>(
+        x_in, x_out, d1, d_new, n, gamma_dev, sim_dev, ws);
+  else
+    k_tdc_commit<float><<<red_grid(n, 8), RED_THREADS, 0, st>>>(x_in, x_out, d1, d_new, n,
+                                                              gamma_dev, sim_dev, ws);
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}

@@ -125,28 +125,32 @@ def run_block_loop(x_in_seq, delta_true_seq, tau, alpha, beta, thr, dtype="bf16"
 
     ``x_in_seq[t]`` is the block input at step t; a computed step's output is
     x_in + delta_true_seq[t] (no trained block exists, the delta is given).  Returns the
-    decision sequence, the routes of every compute step, and per-step outputs.
+    decision sequence, the routes of every compute step, the Gamma each compute step was
+    routed with (None when missing), per-step outputs and decision margins.
     """
     st = TdcState()
     d1 = None
-    decisions, routes, outs, margins = [], [], [], []
+    decisions, routes, outs, margins, gammas = [], [], [], [], []
     for t, (xi, dt) in enumerate(zip(x_in_seq, delta_true_seq)):
         dec = tdc_decide(st, tau)
         margins.append(decision_margin(st, tau))
         decisions.append(dec)
         if dec == SKIP:
             routes.append(None)
+            gammas.append(None)
             outs.append(tdc_skip(xi, d1, dtype))
             tdc_apply(st, SKIP)
             continue
         r = compute_routes(st, alpha, beta, thr)
         routes.append(r)
+        gammas.append(st.gamma_prev)
         xo = _store((_as_f32(xi, dtype) + _as_f32(dt, dtype)).astype(np.float32), dtype)
         c = tdc_commit(xi, xo, d1, dtype)
         d1 = c["delta"]
         outs.append(xo)
         tdc_apply(st, COMPUTE, c)
-    return {"decisions": decisions, "routes": routes, "outs": outs, "margins": margins}
+    return {"decisions": decisions, "routes": routes, "outs": outs, "margins": margins,
+            "gammas": gammas}
 
 
 __all__ = [

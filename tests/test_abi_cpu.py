@@ -1,0 +1,139 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every symbol that
+include/dit6.h declares, validates arguments on the host, and its host-side delta-cache and
+routing logic agrees with the oracle."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from conftest import ROOT
+from oracle import dmpq as D
+from oracle import formats as F
+from oracle import tdc as T
+
+
+@pytest.fixture(scope="module")
+def L():
+    from int8_mixed_precision_gb300 import _lib, build
+    if not os.path.exists(_lib.library_path()):
+        try:
+            build.build_library()
+        except RuntimeError as e:          # no nvcc on this machine
+            pytest.skip(str(e))
+    return _lib.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "dit6.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dit_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["dit_gamma_route", "dit_hadamard_quant_nvfp4", "dit_hadamard_quant_int8",
+              "dit_qgemm_nvfp4", "dit_qgemm_int8", "dit_tdc_step", "dit_sf_index", "dit_status_str"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings(L):
+    for code, name in enumerate(["DIT_OK", "DIT_ERR_INVALID_ARG", "DIT_ERR_ALIGNMENT", "DIT_ERR_UNSUPPORTED",
+                                 "DIT_ERR_CUDA", "DIT_ERR_TIMEOUT"]):
+        assert L.dit_status_str(code).decode() == name
+
+
+def test_sf_index_matches_oracle_layout(L):
+    for rows, k in [(256, 128), (300, 1920), (17, 64), (129, 7680)]:
+        rp, cp = F.sf_padded_shape(rows, k)
+        assert L.dit_sf_bytes(rows, k) == rp * cp
+        rr, cc = np.meshgrid(np.arange(0, rp, 7), np.arange(cp), indexing="ij")
+        want = F.sf_tiled_offset(rr, cc, rows, k)
+        got = np.vectorize(lambda r, c: L.dit_sf_index(int(r), int(c), rows, k))(rr, cc)
+        assert np.array_equal(got, want)
+    assert L.dit_sf_index(0, 0, 10, 24) == -1       # k not a multiple of 16
+
+
+def test_host_argument_validation_without_device_work(L):
+    nul = None
+    fake_misaligned = ctypes.c_void_p(0x1001)
+    ws = ctypes.c_void_p(0x2000)
+    # null pointers, bad sizes, unsupported shapes and misalignment are rejected on the host
+    assert L.dit_hadamard_quant_int8(nul, 1, 4, 128, 64, nul, nul, nul) == 1
+    assert L.dit_hadamard_quant_int8(fake_misaligned, 1, 4, 100, 64, fake_misaligned, fake_misaligned, nul) == 3
+    assert L.dit_hadamard_quant_int8(fake_misaligned, 1, 4, 128, 48, fake_misaligned, fake_misaligned, nul) == 3
+    assert L.dit_hadamard_quant_int8(fake_misaligned, 1, 4, 128, 64, fake_misaligned, fake_misaligned, nul) == 2
+    assert L.dit_hadamard_quant_nvfp4(ws, 1, 4, 128, 64, nul, nul, nul, nul, ws, 65536, nul) == 1
+    f = ctypes.c_float * 17
+    assert L.dit_gamma_route(fake_misaligned, fake_misaligned, 1, 10, f(), f(), f(), 17, ws, ws, ws, 65536, nul) == 1
+    assert L.dit_gamma_route(fake_misaligned, fake_misaligned, 1, 10, f(), f(), f(), 1, ws, ws, ws, 65536, nul) == 2
+    assert L.dit_qgemm_int8(fake_misaligned, ws, fake_misaligned, ws, 4, 8, 100, nul, ws, 1, nul, ws, 65536, nul) == 3
+    assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 96, nul, ws, 1, ws, 65536, nul) == 3
+    assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 128, nul, ws, 1, ws, 100, nul) == 1
+    ws2 = ctypes.c_void_p(0x4000)
+    assert L.dit_tdc_step(0, fake_misaligned, fake_misaligned, nul, ws, ws2, 1, 64, ws, ws, ws, 65536, nul) == 2
+    assert L.dit_tdc_step(0, ws, ws, nul, ws, ws, 1, 64, ws, ws, ws, 65536, nul) == 1   # d1 == d_new
+    assert L.dit_tdc_step(7, ws, ws, nul, ws, ws, 1, 64, ws, ws, ws, 65536, nul) == 1
+
+
+def test_host_tdc_state_machine_matches_oracle(L):
+    import int8_mixed_precision_gb300 as dit
+    g = synth.rng(12)
+    for trial in range(20):
+        tau = float(g.choice([0.02, 0.05, 0.1]))
+        st_c, st_o = dit.TdcState(), T.TdcState()
+        for step in range(40):
+            dc = st_c.decide(tau)
+            do = T.tdc_decide(st_o, tau)
+            assert (dc == dit.TDC_SKIP) == (do == T.SKIP)
+            if do == T.SKIP:
+                st_c.update(dit.TDC_SKIP)
+                T.tdc_apply(st_o, T.SKIP)
+                continue
+            alpha, beta, thr = [1.0, 2.0], [0.0, 0.01], [0.05, 0.05]
+            assert st_c.routes(alpha, beta, thr) == T.compute_routes(
+                st_o, alpha, beta, np.float32(thr).astype(np.float64))
+            gam = float(np.float32(g.uniform(0, 0.2)))
+            d = float(np.float32(g.exponential(0.03))) if st_o.n_computed > 0 else None
+            st_c.update(dit.TDC_COMMIT, gam, d)
+            T.tdc_apply(st_o, T.COMPUTE, {"gamma": gam, "d": d})
+            assert st_c.e_acc == st_o.e_acc and st_c.n_computed == st_o.n_computed
+
+
+def test_host_tdc_golden_sequence(L):
+    """The hand-worked sequence of tests/golden/tdc_sequence.txt through the C state machine,
+    with Gamma and d taken from the oracle's commits."""
+    import int8_mixed_precision_gb300 as dit
+    from conftest import load_golden
+    kv, _ = load_golden("tdc_sequence.txt")
+    base = np.array([1, -1, 2, -2, 1, -1, 2, -2], np.float32) / 64
+    x = np.ones(8, np.float32)
+    st = dit.TdcState()
+    d1 = None
+    decisions, routes = [], []
+    for c in [float(v) for v in kv["c"]]:
+        if st.decide(0.05) == dit.TDC_SKIP:
+            decisions.append("skip")
+            routes.append("-")
+            st.update(dit.TDC_SKIP)
+            continue
+        decisions.append("compute")
+        routes.append("int8" if st.routes([1.0], [0.0], [0.05])[0] == dit.ROUTE_INT8 else "nvfp4")
+        cm = T.tdc_commit(x, x + np.float32(c) * base, d1, "f32")
+        st.update(dit.TDC_COMMIT, cm["gamma"], cm["d"])
+        d1 = cm["delta"]
+    assert decisions == kv["decisions"] and routes == kv["routes"]
+
+
+def test_workspace_and_version(L):
+    assert L.dit_workspace_bytes() >= 33 * 1024
+    assert L.dit_ws_status_offset() == 0
+    assert L.dit_version().decode().count(".") == 2

@@ -1,0 +1,362 @@
+"""GPU parity: every kernel of libdit6 against the CPU oracle on the same seeded inputs.
+
+Stage-wise: each oracle stage consumes the GPU's own input to that stage.  Codes, scales,
+int32 accumulators, deltas and decisions are bit-exact (codes and scales up to elements
+within 1e-5 relative of a rounding boundary); fp outputs of the NVFP4 GEMM within 1e-3
+relative Frobenius of the float64 oracle.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_helpers import (as_f32, check_int8, check_nvfp4, dev_bf16, dev_f32, host, make_x,
+                         rel_fro)
+from oracle import dmpq as D
+from oracle import formats as F
+from oracle import tdc as T
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import int8_mixed_precision_gb300 as dit  # noqa: E402
+
+GEMM_TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def ws():
+    return dit.workspace()
+
+
+def _status_clean(ws):
+    torch.cuda.synchronize()
+    assert dit.device_status(ws) == 0
+
+
+# ------------------------------------------------------------------------------ quantisers
+
+
+@pytest.mark.parametrize("rows,k,dtype,hb", [
+    (256, 128, "f32", 16),        # the single-linear workload
+    (300, 1920, "bf16", 64),      # ragged rows, CogVideoX-2B hidden
+    (129, 7680, "bf16", 64),      # FFN-down width
+    (7, 3072, "bf16", 32),
+    (1, 12288, "bf16", 64),
+])
+def test_int8_quant_parity(rows, k, dtype, hb):
+    x, xd = make_x(rows, k, dtype, seed=rows + k)
+    q = torch.empty(rows, k, dtype=torch.int8, device="cuda")
+    s = torch.empty(rows, dtype=torch.float32, device="cuda")
+    dit.hadamard_quant_int8(xd, hb, q, s)
+    n_ex, _ = check_int8(host(q), host(s), x, dtype, hb)
+    assert n_ex <= max(2, q.numel() // 10000)
+
+
+def test_int8_quant_zero_and_constant_rows():
+    x = np.zeros((5, 128), np.float32)
+    x[1] = 3.0
+    x[2, 7] = -1e-3
+    x[4] = np.linspace(-2, 2, 128, dtype=np.float32)
+    q = torch.empty(5, 128, dtype=torch.int8, device="cuda")
+    s = torch.empty(5, dtype=torch.float32, device="cuda")
+    dit.hadamard_quant_int8(dev_f32(x), 16, q, s)
+    check_int8(host(q), host(s), x, "f32", 16)
+    assert host(s)[0] == 0 and not host(q)[0].any()
+
+
+@pytest.mark.parametrize("rows,k,dtype,hb", [
+    (256, 128, "f32", 16),
+    (300, 1920, "bf16", 64),
+    (129, 7680, "bf16", 64),
+    (7, 3072, "bf16", 32),
+    (1000, 3072, "bf16", 64),
+])
+def test_nvfp4_quant_parity(rows, k, dtype, hb, ws):
+    x, xd = make_x(rows, k, dtype, seed=3 * rows + k, dist="laplace" if k == 3072 else "normal")
+    buf = dit.alloc_nvfp4(rows, k)
+    buf["sf"].fill_(0xAB)     # padding must be overwritten with zeros
+    dit.hadamard_quant_nvfp4(xd, hb, buf["codes"], buf["sf"], buf["gs"], ws)
+    _status_clean(ws)
+    _, n_ex = check_nvfp4(host(buf["codes"]), host(buf["sf"]), host(buf["gs"])[0], x, dtype, hb, rows, k)
+    assert n_ex <= max(2, rows * k // 10000)
+
+
+def test_nvfp4_quant_given_tensor_scale_and_repeat(ws):
+    rows, k = 200, 1920
+    x, xd = make_x(rows, k, "bf16", seed=77)
+    buf = dit.alloc_nvfp4(rows, k)
+    sg_in = torch.tensor([0.004], dtype=torch.float32, device="cuda")   # small: forces saturation
+    dit.hadamard_quant_nvfp4(xd, 64, buf["codes"], buf["sf"], buf["gs"], ws, tensor_scale_in=sg_in)
+    check_nvfp4(host(buf["codes"]), host(buf["sf"]), host(buf["gs"])[0], x, "bf16", 64, rows, k,
+                s_g=np.float32(0.004))
+    # the dynamic path twice in a row (the workspace must come back to its reusable state)
+    for _ in range(2):
+        dit.hadamard_quant_nvfp4(xd, 64, buf["codes"], buf["sf"], buf["gs"], ws)
+        check_nvfp4(host(buf["codes"]), host(buf["sf"]), host(buf["gs"])[0], x, "bf16", 64, rows, k)
+    _status_clean(ws)
+
+
+def test_nvfp4_quant_zero_tensor(ws):
+    x = np.zeros((130, 128), np.float32)
+    buf = dit.alloc_nvfp4(130, 128)
+    dit.hadamard_quant_nvfp4(dev_f32(x), 16, buf["codes"], buf["sf"], buf["gs"], ws)
+    assert host(buf["gs"])[0] == 0 and not host(buf["codes"]).any() and not host(buf["sf"]).any()
+
+
+def test_e2m1_negative_zero_convention(ws):
+    """Tiny negative values in a block with a large element: the hardware convert and the
+    oracle agree on the sign of the zero code."""
+    x = np.zeros((1, 64), np.float32)
+    x[0, :16] = [6.0, -0.01, 0.01, -0.2, 0.2, -0.26, 0.26, -0.0, 0.0, -1e-30, 3, -3, 0.74, -0.76, 5, -5]
+    sg = torch.tensor([1.0], dtype=torch.float32, device="cuda")
+    buf = dit.alloc_nvfp4(1, 64)
+    # hblock 16 on a one-hot pattern would mix values; quantise the raw row by undoing the
+    # transform: H(H x)/16 = x, so feeding H x / 4 gives back x after the block transform
+    xh = D.block_fwht_f32(x, 16).astype(np.float32)
+    dit.hadamard_quant_nvfp4(dev_f32(xh), 16, buf["codes"], buf["sf"], buf["gs"], ws, tensor_scale_in=sg)
+    check_nvfp4(host(buf["codes"]), host(buf["sf"]), 1.0, xh, "f32", 16, 1, 64, s_g=np.float32(1.0))
+
+
+# ------------------------------------------------------------------------------ Gamma / TDC
+
+
+@pytest.mark.parametrize("n,dtype", [(256 * 128, "f32"), (17776 * 64 + 5, "bf16"), (33, "bf16")])
+def test_gamma_route_parity(n, dtype, ws):
+    g = synth.rng(n)
+    xi = g.standard_normal(n).astype(np.float32)
+    xo = (xi + g.standard_normal(n).astype(np.float32) * 0.07).astype(np.float32)
+    if dtype == "bf16":
+        xi, xo = synth.to_bf16_bits(xi), synth.to_bf16_bits(xo)
+        di, do = dev_bf16(xi), dev_bf16(xo)
+    else:
+        di, do = dev_f32(xi), dev_f32(xo)
+    alpha, beta, thr = [1.0, 0.5, 2.0, 1.0], [0.0, 0.0, 0.0, 0.02], [0.05, 0.05, 0.05, 0.05]
+    gam = torch.empty(1, dtype=torch.float32, device="cuda")
+    routes = torch.empty(4, dtype=torch.int32, device="cuda")
+    dit.gamma_route(di, do, alpha, beta, thr, gam, routes, ws)
+    ref = D.gamma_rel_l1(as_f32(xi, dtype), as_f32(xo, dtype))
+    got = float(host(gam)[0])
+    assert got == pytest.approx(ref, rel=1e-5)
+    want = D.route_layers(ref, alpha, beta, np.float32(thr).astype(np.float64))
+    margins = [D.route_margin(ref, a, b, t) for a, b, t in zip(alpha, beta, thr)]
+    for r, w, m in zip(host(routes).tolist(), want, margins):
+        assert r == w or m <= 1e-5
+    # deterministic across runs
+    dit.gamma_route(di, do, alpha, beta, thr, gam, routes, ws)
+    assert float(host(gam)[0]) == got
+    _status_clean(ws)
+
+
+def test_gamma_single_linear_routes_int8(ws):
+    c = synth.single_linear()
+    gam = torch.empty(1, dtype=torch.float32, device="cuda")
+    routes = torch.empty(1, dtype=torch.int32, device="cuda")
+    dit.gamma_route(dev_f32(c["x"]), dev_f32(c["x_out"]), [1.0], [0.0], [0.05], gam, routes, ws)
+    assert float(host(gam)[0]) == pytest.approx(D.gamma_rel_l1(c["x"], c["x_out"]), rel=1e-5)
+    assert host(routes).tolist() == [dit.ROUTE_INT8]
+
+
+@pytest.mark.parametrize("n,dtype", [(17776 * 16 + 3, "bf16"), (4096 + 5, "f32")])
+def test_tdc_commit_and_skip_parity(n, dtype, ws):
+    g = synth.rng(n + 1)
+    xi32 = g.standard_normal(n).astype(np.float32)
+    d_prev32 = (g.standard_normal(n) * 0.1).astype(np.float32)
+    xo32 = (xi32 + d_prev32 * (1 + g.standard_normal(n).astype(np.float32) * 0.01)).astype(np.float32)
+    conv = synth.to_bf16_bits if dtype == "bf16" else (lambda a: a)
+    dev = dev_bf16 if dtype == "bf16" else dev_f32
+    xi, xo, dp = conv(xi32), conv(xo32), conv(d_prev32)
+    di, do, ddp = dev(xi), dev(xo), dev(dp)
+    dnew = torch.empty_like(di)
+    gam = torch.empty(1, dtype=torch.float32, device="cuda")
+    sim = torch.empty(1, dtype=torch.float32, device="cuda")
+    dit.tdc_step(dit.TDC_COMMIT, di, ws, x_out=do, d1=ddp, d_new=dnew, gamma=gam, sim=sim)
+    ref = T.tdc_commit(xi, xo, dp, dtype)
+    assert np.array_equal(host(dnew), ref["delta"])
+    assert float(host(gam)[0]) == pytest.approx(ref["gamma"], rel=1e-5)
+    assert float(host(sim)[0]) == pytest.approx(ref["d"], rel=1e-5)
+    # no previous delta: similarity is +inf
+    dit.tdc_step(dit.TDC_COMMIT, di, ws, x_out=do, d1=None, d_new=dnew, gamma=gam, sim=sim)
+    assert math.isinf(float(host(sim)[0]))
+    # skip: x_in + cached delta, bit-exact
+    out = torch.empty_like(di)
+    dit.tdc_step(dit.TDC_SKIP, di, ws, x_out_skip=out, d1=dnew)
+    assert np.array_equal(host(out), T.tdc_skip(xi, ref["delta"], dtype))
+    _status_clean(ws)
+
+
+def test_tdc_loop_decisions_match_oracle(ws):
+    """A 12-step, 3-block delta-cache loop: decisions and routes identical to the oracle."""
+    rows, k, steps, tau = 64, 256, 12, 0.05
+    alpha, beta, thr = [1.0] * 4, [0.0] * 4, [0.05] * 4
+    for b in range(3):
+        deltas, _ = synth.tdc_deltas(steps, rows, k, seed=100 + b, jump_every=5.0)
+        xs = [synth.activations(rows, k, seed=1000 * b + t, outlier_frac=0.0) for t in range(steps)]
+        ref = T.run_block_loop(xs, deltas, tau, alpha, beta, np.float32(thr).astype(np.float64))
+        st = dit.TdcState()
+        d1 = torch.empty(rows * k, dtype=torch.bfloat16, device="cuda")
+        d2 = torch.empty_like(d1)
+        gam = torch.empty(1, dtype=torch.float32, device="cuda")
+        sim = torch.empty(1, dtype=torch.float32, device="cuda")
+        decisions, routes = [], []
+        for t in range(steps):
+            mode = st.decide(tau)
+            xi = dev_bf16(xs[t]).reshape(-1)
+            if mode == dit.TDC_SKIP:
+                out = torch.empty_like(xi)
+                dit.tdc_step(dit.TDC_SKIP, xi, ws, x_out_skip=out, d1=d1)
+                assert np.array_equal(host(out), ref["outs"][t].reshape(-1))
+                decisions.append("skip")
+                routes.append(None)
+                st.update(dit.TDC_SKIP)
+                continue
+            routes.append(st.routes(alpha, beta, thr))
+            xo32 = (F.bf16_bits_to_f32(xs[t]) + F.bf16_bits_to_f32(deltas[t])).astype(np.float32)
+            xo = dev_bf16(F.f32_to_bf16_bits(xo32)).reshape(-1)
+            has_prev = st.n_computed > 0
+            dit.tdc_step(dit.TDC_COMMIT, xi, ws, x_out=xo, d1=d1 if has_prev else None, d_new=d2,
+                         gamma=gam, sim=sim)
+            torch.cuda.synchronize()
+            st.update(dit.TDC_COMMIT, float(host(gam)[0]), float(host(sim)[0]) if has_prev else None)
+            d1, d2 = d2, d1
+            decisions.append("compute")
+        for t in range(steps):
+            if ref["margins"][t] > 1e-5:
+                assert decisions[t] == ref["decisions"][t], (b, t, decisions, ref["decisions"])
+        for t in range(steps):
+            if ref["margins"][t] <= 1e-5 or decisions[t] != ref["decisions"][t]:
+                continue
+            g_ref = ref["gammas"][t]
+            if g_ref is not None and abs(g_ref - 0.05) <= 1e-5 * 0.05:
+                continue        # borderline route
+            assert routes[t] == ref["routes"][t], (b, t, routes[t], ref["routes"][t])
+
+
+# ------------------------------------------------------------------------------ GEMMs
+
+
+@pytest.mark.parametrize("m,n,k", [(256, 512, 128), (300, 384, 1920), (129, 256, 7680), (1, 8, 16),
+                                   (200, 136, 208)])
+def test_int8_gemm_exact_accumulators(m, n, k, ws):
+    g = synth.rng(m * n + k)
+    a = g.integers(-127, 128, (m, k)).astype(np.int8)
+    b = g.integers(-127, 128, (n, k)).astype(np.int8)
+    sa = g.random(m).astype(np.float32) * 0.01
+    sb = g.random(n).astype(np.float32) * 0.01
+    bias = g.standard_normal(n).astype(np.float32)
+    ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    acc = torch.empty(m, n, dtype=torch.int32, device="cuda")
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws, bias=dev_f32(bias), acc_debug=acc)
+    ref_acc = D.gemm_int8_acc(a, b)
+    assert np.array_equal(host(acc).astype(np.int64), ref_acc)
+    ref = D.gemm_int8(a, sa, b, sb, bias)
+    assert rel_fro(host(y), ref) <= 1e-6
+    yb = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), yb, ws, bias=dev_f32(bias))
+    assert rel_fro(F.bf16_bits_to_f32(host(yb)), F.bf16_bits_to_f32(F.f32_to_bf16_bits(ref.astype(np.float32)))) <= GEMM_TOL
+    _status_clean(ws)
+
+
+def _nvfp4_operands(m, n, k, seed):
+    g = synth.rng(seed)
+    ya = (g.standard_normal((m, k)) * np.exp(g.standard_normal((m, 1)) * 0.5)).astype(np.float32)
+    yb = (g.standard_normal((n, k)) * 0.02).astype(np.float32)
+    qa, qb = D.quant_nvfp4(ya), D.quant_nvfp4(yb)
+    out = []
+    for q, rows in ((qa, m), (qb, n)):
+        out.append({"codes": torch.from_numpy(D.pack_e2m1(q["codes"])).cuda(),
+                    "sf": torch.from_numpy(F.sf_to_tiled(q["sf"], rows, k)).cuda(),
+                    "gs": torch.tensor([float(q["s_g"])], dtype=torch.float32, device="cuda")})
+    return qa, qb, out[0], out[1]
+
+
+@pytest.mark.parametrize("cfg", ["0", "1", "2", "3"])
+@pytest.mark.parametrize("m,n,k", [(256, 512, 128), (300, 384, 1920), (129, 256, 7680), (128, 128, 64),
+                                   (77, 136, 320)])
+def test_nvfp4_gemm_parity(m, n, k, cfg, ws, monkeypatch):
+    monkeypatch.setenv("DIT6_NVFP4_TILE", cfg)
+    qa, qb, A, B = _nvfp4_operands(m, n, k, seed=m + n + k)
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], y, ws)
+    _status_clean(ws)
+    ref = D.gemm_nvfp4(qa["codes"], qa["sf"], qa["s_g"], qb["codes"], qb["sf"], qb["s_g"])
+    err = rel_fro(host(y), ref)
+    assert err <= GEMM_TOL, f"rel Frobenius {err:.3e}"
+    yb = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    bias = torch.linspace(-1, 1, n, device="cuda", dtype=torch.float32)
+    dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], yb, ws, bias=bias)
+    refb = F.bf16_bits_to_f32(F.f32_to_bf16_bits((ref + host(bias)[None, :]).astype(np.float32)))
+    assert rel_fro(F.bf16_bits_to_f32(host(yb)), refb) <= GEMM_TOL
+
+
+# ------------------------------------------------------------------------------ routed linear
+
+
+@pytest.mark.parametrize("route", [dit.ROUTE_NVFP4, dit.ROUTE_INT8])
+def test_single_linear_end_to_end(route, ws):
+    """The 256x128 single linear (Hadamard block 16) along both routes, stage by stage."""
+    c = synth.single_linear()
+    wq = dit.QuantizedWeight(dev_f32(c["w"]), 16, ws)
+    lin = dit.RoutedLinear(wq, 256, ws)
+    y = torch.empty(256, 512, dtype=torch.float32, device="cuda")
+    lin(dev_f32(c["x"]), route, y)
+    _status_clean(ws)
+    wp = D.prepare_weight(c["w"], 16)
+    if route == dit.ROUTE_INT8:
+        check_int8(host(wq.int8["q"]), host(wq.int8["scale"]), c["w"], "f32", 16)
+        check_int8(host(lin.a8["q"]), host(lin.a8["scale"]), c["x"], "f32", 16)
+        ref = D.gemm_int8(host(lin.a8["q"]), host(lin.a8["scale"]), host(wq.int8["q"]), host(wq.int8["scale"]))
+    else:
+        check_nvfp4(host(wq.nvfp4["codes"]), host(wq.nvfp4["sf"]), host(wq.nvfp4["gs"])[0], c["w"], "f32", 16, 512, 128)
+        check_nvfp4(host(lin.a4["codes"]), host(lin.a4["sf"]), host(lin.a4["gs"])[0], c["x"], "f32", 16, 256, 128)
+        ref = D.gemm_nvfp4(D.unpack_e2m1(host(lin.a4["codes"])), F.sf_from_tiled(host(lin.a4["sf"]), 256, 128),
+                           host(lin.a4["gs"])[0], D.unpack_e2m1(host(wq.nvfp4["codes"])),
+                           F.sf_from_tiled(host(wq.nvfp4["sf"]), 512, 128), host(wq.nvfp4["gs"])[0])
+    assert rel_fro(host(y), ref) <= GEMM_TOL
+    # and the whole path against the all-oracle routed linear
+    assert rel_fro(host(y), D.routed_linear(c["x"], wp, 16, route)) <= GEMM_TOL
+
+
+# ------------------------------------------------------------------------------ full size
+
+
+def test_full_size_cogvideox_2b_sampled(ws):
+    """Full CogVideoX-2B QKV shape (17776 x 1920 -> 5760): quantisers checked on sampled rows
+    (with the whole-tensor scale from the oracle), GEMM outputs on sampled rows."""
+    m, k, n = synth.TOKENS_2B, 1920, 5760
+    x, xd = make_x(m, k, "bf16", seed=2024)
+    w = synth.weights(n, k, seed=2025)
+    wq = dit.QuantizedWeight(dev_f32(w), 64, ws)
+    lin = dit.RoutedLinear(wq, m, ws)
+    y = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    rows = np.unique(np.concatenate([synth.rng(5).choice(m, 48, replace=False), np.arange(m - 16, m)]))
+    for route in (dit.ROUTE_NVFP4, dit.ROUTE_INT8):
+        lin(xd, route, y)
+        torch.cuda.synchronize()
+        yh = F.bf16_bits_to_f32(host(y))[rows]
+        if route == dit.ROUTE_NVFP4:
+            yfull = D.block_fwht_f32(F.bf16_bits_to_f32(x), 64)
+            sg = D.nvfp4_tensor_scale(yfull)
+            assert np.float32(host(lin.a4["gs"])[0]) == sg
+            codes = D.unpack_e2m1(host(lin.a4["codes"]))[rows]
+            sf = F.sf_from_tiled(host(lin.a4["sf"]), m, k)[rows]
+            r = D.quant_nvfp4(yfull[rows], s_g=sg)
+            ex = (F.e2m1_rounding_margin(r["v"]) <= 1e-5) | (F.e4m3_rounding_margin(r["sbf"]) <= 1e-5).repeat(16, axis=1)
+            assert not ((codes != r["codes"]) & ~ex).any()
+            ref = D.gemm_nvfp4(codes, sf, sg, D.unpack_e2m1(host(wq.nvfp4["codes"])),
+                               F.sf_from_tiled(host(wq.nvfp4["sf"]), n, k), host(wq.nvfp4["gs"])[0])
+        else:
+            q = host(lin.a8["q"])[rows]
+            s = host(lin.a8["scale"])[rows]
+            xr = x[rows]
+            check_int8(q, s, xr, "bf16", 64)
+            ref = D.gemm_int8(q, s, host(wq.int8["q"]), host(wq.int8["scale"]))
+        refb = F.bf16_bits_to_f32(F.f32_to_bf16_bits(ref.astype(np.float32)))
+        assert rel_fro(yh, refb) <= GEMM_TOL
+    _status_clean(ws)
