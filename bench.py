@@ -1,0 +1,471 @@
+"""Benchmark of the routed NVFP4/INT8 linear layer + Temporal Delta Cache on GB300.
+
+Workload (default): CogVideoX-2B-shaped DiT block linears, bf16, hidden 1920, 17776 tokens
+(13x30x45 video + 226 text), QKV 1920->5760, out 1920->1920, FFN 1920->7680->1920,
+Hadamard block 64, 1% outlier channels x50, 30 blocks whose Gamma ~ U(0, 0.2) routes each
+block to INT8 (Gamma > 0.05) or NVFP4.  Synthetic, seeded inputs (no trained weights exist).
+
+One step = one pass over the 30 blocks: for each block its four routed linears (online
+block Hadamard + activation quantisation + quantised GEMM) and the delta-cache commit
+(residual delta, Gamma_t for the next step's routing, similarity of the last two deltas).
+value = algorithmic GEMM FLOPs of the step / step time (TFLOP/s).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own 30-block replica (independent problems, no data-path
+collective: weak scaling); value = FLOPs of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized-linear TFLOPS (NVFP4 / INT8) & HBM GB/s of quant+TDC, 1 GB300"
+UNIT = "TFLOP/s"
+WORKLOAD = "cogvideox_2b_block_linears"
+TOKENS = 13 * 30 * 45 + 226
+HIDDEN, FFN, HBLOCK, NBLOCKS = 1920, 7680, 64, 30
+THR, ALPHA, BETA = 0.05, 1.0, 0.0
+LINEARS = [("qkv", HIDDEN, 3 * HIDDEN), ("out", HIDDEN, HIDDEN), ("ffn_up", HIDDEN, FFN),
+           ("ffn_down", FFN, HIDDEN)]
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------
+# our implementation
+# ----------------------------------------------------------------------------------------
+
+
+class Workload:
+    """Device-resident synthetic workload: 30 blocks of routed linears + delta-cache state."""
+
+    def __init__(self, dev, seed: int):
+        import torch
+        import int8_mixed_precision_gb300 as dit
+        self.dit, self.torch, self.dev = dit, torch, dev
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.ws = dit.workspace(dev)
+        M = TOKENS
+
+        def act(k, s):
+            g.manual_seed(seed * 1000 + s)
+            x = torch.randn(M, k, device=dev, generator=g)
+            ch = torch.randperm(k, device=dev, generator=g)[: max(1, k // 100)]
+            x[:, ch] *= 50.0
+            return x.to(torch.bfloat16)
+
+        # two alternating activation sets (consecutive blocks never share an input tensor)
+        self.inputs = [{name: act(k, 10 * s + i) for i, (name, k, _) in enumerate(LINEARS)} for s in range(2)]
+        self.x_in = act(HIDDEN, 99)
+        # per-block Gamma pairs: X_out = X_in + gamma_b * S * X_in, gamma_b ~ U(0, 0.2)
+        g.manual_seed(seed + 7)
+        self.gammas_true = (torch.rand(NBLOCKS, generator=g, device=dev) * 0.2).tolist()
+        self.x_out, self.blocks = [], []
+        for b in range(NBLOCKS):
+            g.manual_seed(seed * 31 + b)
+            sgn = torch.randint(0, 2, self.x_in.shape, generator=g, device=dev).to(torch.float32) * 2 - 1
+            self.x_out.append((self.x_in.float() * (1 + self.gammas_true[b] * sgn)).to(torch.bfloat16))
+            lins = {}
+            for name, k, n in LINEARS:
+                g.manual_seed(seed * 7919 + b * 17 + n + k)
+                w = torch.randn(n, k, device=dev, generator=g) * 0.02
+                lins[name] = dit.RoutedLinear(dit.QuantizedWeight(w, HBLOCK, self.ws), M, self.ws, dev)
+                del w
+            self.blocks.append({"lin": lins, "d": [torch.empty_like(self.x_in), torch.empty_like(self.x_in)],
+                                "has_delta": False})
+        self.y = {name: torch.empty(M, n, dtype=torch.bfloat16, device=dev) for name, _, n in LINEARS}
+        self.gamma = torch.empty(NBLOCKS, dtype=torch.float32, device=dev)
+        self.sim = torch.empty(NBLOCKS, dtype=torch.float32, device=dev)
+        # routing from the predictor (one Gamma per block; the commit of every step
+        # recomputes it, and with fixed pairs the routes stay the same)
+        r = torch.empty(4, dtype=torch.int32, device=dev)
+        self.routes = []
+        for b in range(NBLOCKS):
+            dit.gamma_route(self.x_in, self.x_out[b], [ALPHA] * 4, [BETA] * 4, [THR] * 4,
+                            self.gamma[b:b + 1], r, self.ws)
+            self.routes.append(r.tolist())
+        torch.cuda.synchronize()
+        self.flops_step = NBLOCKS * sum(2 * M * n * k for _, k, n in LINEARS)
+        self.timers = None   # {kernel type: [event pairs]} when per-kernel timing is on
+
+    def launches_per_step(self):
+        n = 0
+        for b in range(NBLOCKS):
+            for r in self.routes[b]:
+                n += 2 if r == self.dit.ROUTE_INT8 else 3
+            n += 1
+        return n
+
+    def _timed(self, kind, fn):
+        if self.timers is None or kind not in self.timers:
+            return fn()
+        a = self.torch.cuda.Event(enable_timing=True)
+        z = self.torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        z.record()
+        self.timers[kind].append((a, z))
+
+    def step(self):
+        dit = self.dit
+        for b, blk in enumerate(self.blocks):
+            xs = self.inputs[b % 2]
+            for li, (name, k, n) in enumerate(LINEARS):
+                lin = blk["lin"][name]
+                route = self.routes[b][li]
+                x, y = xs[name], self.y[name]
+                if route == dit.ROUTE_INT8:
+                    self._timed("quant_int8", lambda: dit.hadamard_quant_int8(x, HBLOCK, lin.a8["q"], lin.a8["scale"]))
+                    self._timed("gemm_int8", lambda: dit.qgemm_int8(lin.a8["q"], lin.a8["scale"], lin.w.int8["q"],
+                                                                    lin.w.int8["scale"], y, self.ws))
+                else:
+                    self._timed("quant_nvfp4", lambda: dit.hadamard_quant_nvfp4(
+                        x, HBLOCK, lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], self.ws))
+                    self._timed("gemm_nvfp4", lambda: dit.qgemm_nvfp4(
+                        lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], lin.w.nvfp4["codes"], lin.w.nvfp4["sf"],
+                        lin.w.nvfp4["gs"], y, self.ws))
+            d_new, d_old = blk["d"][0], blk["d"][1]
+            self._timed("tdc_commit", lambda: dit.tdc_step(
+                dit.TDC_COMMIT, self.x_in, self.ws, x_out=self.x_out[b], d1=d_old if blk["has_delta"] else None,
+                d_new=d_new, gamma=self.gamma[b:b + 1], sim=self.sim[b:b + 1]))
+            blk["d"].reverse()
+            blk["has_delta"] = True
+
+    # algorithmic units per kernel launch type (FLOPs for GEMMs, bytes otherwise)
+    def kernel_units(self):
+        M = TOKENS
+        u = {"gemm_int8": 0, "gemm_nvfp4": 0, "quant_int8": 0, "quant_nvfp4": 0, "tdc_commit": 0}
+        for b in range(NBLOCKS):
+            for li, (name, k, n) in enumerate(LINEARS):
+                if self.routes[b][li] == self.dit.ROUTE_INT8:
+                    u["gemm_int8"] += 2 * M * n * k
+                    u["quant_int8"] += M * k * 3 + 4 * M
+                else:
+                    u["gemm_nvfp4"] += 2 * M * n * k
+                    u["quant_nvfp4"] += M * k * 2 + M * k // 2 + M * k // 16
+            u["tdc_commit"] += M * HIDDEN * 8
+        return u
+
+
+def int8_ceiling(torch, dev):
+    """cuBLASLt INT8 GEMM throughput (torch._int_mm, 8192^3) measured in this run."""
+    a = torch.randint(-127, 127, (8192, 8192), device=dev, dtype=torch.int8)
+    b = torch.randint(-127, 127, (8192, 8192), device=dev, dtype=torch.int8)
+    for _ in range(2):
+        torch._int_mm(a, b.t())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(5):
+        torch._int_mm(a, b.t())
+    e1.record()
+    e1.synchronize()
+    return 5 * 2 * 8192 ** 3 / (e0.elapsed_time(e1) * 1e-3) / 1e12
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as tdist
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = Workload(dev, seed=1234 + rank)
+    stream = torch.cuda.current_stream()
+
+    # one instrumented warm-up step: which kernel type dominates
+    wl.timers = {k: [] for k in ("gemm_int8", "gemm_nvfp4", "quant_int8", "quant_nvfp4", "tdc_commit")}
+    wl.step()
+    torch.cuda.synchronize()
+    tot = {k: sum(a.elapsed_time(z) for a, z in v) for k, v in wl.timers.items()}
+    dominant = max(tot, key=tot.get)
+    wl.timers = None
+    for _ in range(max(0, args.warmup - 1)):
+        wl.step()
+
+    def barrier():
+        if world > 1:
+            tdist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-timed region (inputs resident in HBM) ----
+    wl.timers = {dominant: []}
+    barrier()
+    with Clocks(local_rank) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push("timed")
+        e0.record(stream)
+        for _ in range(args.steps):
+            wl.step()
+        e1.record(stream)
+        torch.cuda.nvtx.range_pop()
+        e1.synchronize()
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    dom_ms = [a.elapsed_time(z) for a, z in wl.timers[dominant]]
+    wl.timers = None
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the public API: host inputs in, results out ----
+    host_in = {}
+    for s in range(2):
+        for name, t in wl.inputs[s].items():
+            host_in[(s, name)] = t.cpu().pin_memory()
+    host_pairs = [t.cpu().pin_memory() for t in wl.x_out] + [wl.x_in.cpu().pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
+        sum(t.numel() * t.element_size() for t in host_pairs)
+    out_host = torch.empty_like(wl.y["ffn_down"], device="cpu").pin_memory()
+    g_host = torch.empty(2 * NBLOCKS, dtype=torch.float32).pin_memory()
+    d2h = out_host.numel() * out_host.element_size() + g_host.numel() * 4
+
+    def e2e_step():
+        for (s, name), t in host_in.items():
+            wl.inputs[s][name].copy_(t, non_blocking=True)
+        for b in range(NBLOCKS):
+            wl.x_out[b].copy_(host_pairs[b], non_blocking=True)
+        wl.x_in.copy_(host_pairs[-1], non_blocking=True)
+        wl.step()
+        out_host.copy_(wl.y["ffn_down"], non_blocking=True)
+        g_host[:NBLOCKS].copy_(wl.gamma, non_blocking=True)
+        g_host[NBLOCKS:].copy_(wl.sim, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    e_steps = max(1, min(args.steps, 3))
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return
+    pk, src = peaks()
+    units = wl.kernel_units()
+    avg_ms = sum(dom_ms) / len(dom_ms)
+    n_launch_step = len(dom_ms) / args.steps
+    unit_per_launch = units[dominant] / n_launch_step
+    if dominant.startswith("gemm"):
+        achieved = unit_per_launch / (avg_ms * 1e-3) / 1e12
+        if dominant == "gemm_int8":
+            peak = int8_ceiling(torch, dev)
+            peak_note = "measured cuBLASLt INT8 GEMM (torch._int_mm 8192^3) in this run"
+        else:
+            peak = pk["bf16_tflops_sustained"] * 6.0
+            peak_note = f"{src} bf16 sustained x 6 (nominal dense fp4/bf16 ratio)"
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "kernel": dominant, "peak_source": peak_note}
+    else:
+        achieved = unit_per_launch / (avg_ms * 1e-3) / 1e9
+        peak = pk["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "kernel": dominant,
+                "peak_source": f"{src} HBM copy"}
+    kern_times = {k: round(v, 3) for k, v in tot.items()}
+    hbm = {k: round(units[k] / (tot[k] * 1e-3) / 1e9, 1) for k in ("quant_int8", "quant_nvfp4", "tdc_commit")
+           if tot.get(k)}
+    value = wl.flops_step * world / (ms * 1e-3) / 1e12
+    e2e_val = wl.flops_step * world / (e2e_ms * 1e-3) / 1e12
+    routes_flat = [r for rr in wl.routes for r in rr]
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4/int8 operands, fp32 accumulate, bf16 activations",
+        "data": "synthetic (seeded; CogVideoX-2B-shaped activations with outlier channels, N(0,0.02) weights)",
+        "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN, "blocks": NBLOCKS,
+                   "hadamard_block": HBLOCK, "gamma": "U(0,0.2)", "thr": THR,
+                   "int8_layers": routes_flat.count(1), "nvfp4_layers": routes_flat.count(0),
+                   "l2": "inputs larger than L2 (68-273 MB per tensor, two alternating sets)",
+                   "parallelism": f"replicas{world}"},
+        "roofline": roof,
+        "kernel_ms_per_step": kern_times,
+        "hbm_gbs_algorithmic": hbm,
+        "e2e": {"value": round(e2e_val, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(wl.launches_per_step() * args.steps),
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------
+# CPU oracle baselines (the one place besides the tests that runs the oracle)
+# ----------------------------------------------------------------------------------------
+
+
+_PREP = {}
+
+
+def _oracle_weights():
+    """Both routes' weights of one block, prepared once by the oracle (untimed)."""
+    if not _PREP:
+        import synth
+        from oracle import dmpq as D
+        for name, k, n in LINEARS:
+            _PREP[name] = D.prepare_weight(synth.weights(n, k, seed=5000 + n + k), HBLOCK)
+    return _PREP
+
+
+def oracle_sample(tokens: int, seed: int):
+    """The oracle on a token sample of one block: the four routed linears (alternating
+    routes) + the delta commit.  Returns (seconds, flops)."""
+    import synth
+    from oracle import dmpq as D
+    from oracle import tdc as T
+    preps = _oracle_weights()
+    xs = [synth.activations(tokens, k, seed=seed + i, dtype="f32") for i, (_, k, _) in enumerate(LINEARS)]
+    xi = synth.activations(tokens, HIDDEN, seed=seed + 9)
+    xo = synth.gamma_pair(xi, 0.1, seed + 10)
+    flops = 0
+    t0 = time.perf_counter()
+    for i, (name, k, n) in enumerate(LINEARS):
+        route = D.ROUTE_INT8 if i % 2 == 0 else D.ROUTE_NVFP4
+        D.routed_linear(xs[i], preps[name], HBLOCK, route)
+        flops += 2 * tokens * n * k
+    T.tdc_commit(xi, xo, None, "bf16")
+    return time.perf_counter() - t0, flops
+
+
+def cpu_baseline(seconds_budget: float = 15.0):
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    tokens, total_t, total_f, reps = 64, 0.0, 0, 0
+    while total_t < seconds_budget and reps < 50:
+        t, f = oracle_sample(tokens, seed=reps)
+        total_t += t
+        total_f += f
+        reps += 1
+        if t < 1.0 and tokens < 2048:
+            tokens *= 2
+    return {"value": round(total_f / total_t / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{reps} oracle passes over one CogVideoX-2B block (4 routed linears, both routes, "
+                      f"+ delta commit) on token samples up to {tokens} tokens; weight preparation untimed; "
+                      f"{total_t:.1f} s of CPU work (numpy float64 BLAS on all cores)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    tokens = 128
+    for _ in range(max(0, args.warmup)):
+        oracle_sample(32, seed=1)
+    total_t, total_f = 0.0, 0
+    for s in range(args.steps):
+        t, f = oracle_sample(tokens, seed=100 + s)
+        total_t += t
+        total_f += f
+    v = total_f / total_t / 1e12
+    sample = (f"each step: the oracle over one CogVideoX-2B block (4 routed linears, both routes, + delta "
+              f"commit) on a {tokens}-token sample; weight preparation untimed")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_t * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/int64 (CPU oracle)",
+        "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "tokens_sample": tokens},
+        "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
