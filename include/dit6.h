@@ -89,6 +89,33 @@ dit_status dit_gamma_route(const void* x_in, const void* x_out, dit_dtype dt, in
                            size_t ws_bytes, dit_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * dit_gamma_route without a workspace argument.  The paper has no counterpart: this is a
+ * convenience of this library for callers that cannot allocate device memory -- e.g. an
+ * inference-engine plugin whose memory is planned by the engine ahead of time and which may
+ * not allocate while enqueueing, or a latency-critical loop that cannot afford cudaMalloc
+ * (it may synchronise the device).
+ *
+ * Same arguments and results as dit_gamma_route, minus ws / ws_bytes.  The reduction's
+ * scratch (a status word, a completion counter and per-CTA partial sums) lives in a fixed
+ * device array of 20,736 bytes inside the library, holding partials for at most 640 CTAs;
+ * every GPU that loads the library keeps it until the process exits.  The launch uses
+ * min(ceil(n / 4096), 4 x SM count) CTAs for bf16 (n / 2048 for fp32); a request that needs
+ * more than 640 returns DIT_ERR_UNSUPPORTED.  Nothing is allocated: no cudaMalloc, cudaFree
+ * or allocating library routine is called.
+ *
+ * The first call on a device sets the scratch up (looks up its device address with
+ * cudaGetSymbolAddress and zero-fills it once, synchronously, with that device current);
+ * make that first call before any stream capture.  Every call then clears the status word
+ * and counter asynchronously on `stream`.  All calls share the one array and it keeps the
+ * last call's contents: calls whose kernels overlap on the GPU (different streams, no
+ * ordering between them) race on it and give wrong results.
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_gamma_route_noalloc(const void* x_in, const void* x_out, dit_dtype dt,
+                                   int64_t n, const float* alpha, const float* beta,
+                                   const float* thr, int n_layers, float* gamma_dev,
+                                   int32_t* routes_dev, dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * (a3 + a4) Online block Hadamard transform fused with NVFP4 quantisation.
  * [EN] 2.A "Outlier Smoothing" (block Hadamard on local activation blocks);
  * [IT] "3. Contributi Chiave" 4 (NVFP4 = E2M1); [ZH] 2.A (weights quantised offline).

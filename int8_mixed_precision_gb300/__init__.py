@@ -105,6 +105,17 @@ def gamma_route(x_in, x_out, alpha, beta, thr, gamma, routes, ws, stream=None):
     _check(st, "dit_gamma_route")
 
 
+def gamma_route_noalloc(x_in, x_out, alpha, beta, thr, gamma, routes, stream=None):
+    """Same as gamma_route, with the reduction scratch held inside the library (a fixed
+    device array) instead of a caller workspace; for callers that cannot allocate.  Calls
+    share that array, so calls running concurrently on different streams race."""
+    n = len(alpha)
+    arr = ctypes.c_float * max(n, 1)
+    st = lib().dit_gamma_route_noalloc(_p(x_in), _p(x_out), _dt(x_in), x_in.numel(), arr(*alpha),
+                                       arr(*beta), arr(*thr), n, _p(gamma), _p(routes), _stream(stream))
+    _check(st, "dit_gamma_route_noalloc")
+
+
 def hadamard_quant_nvfp4(x, hblock, codes, sf, tensor_scale, ws, tensor_scale_in=None, stream=None):
     rows, k = x.shape
     st = lib().dit_hadamard_quant_nvfp4(_p(x), _dt(x), rows, k, hblock, _p(codes), _p(sf),

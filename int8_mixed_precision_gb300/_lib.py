@@ -26,6 +26,7 @@ SIGNATURES = {
     "dit_workspace_bytes": (_sz, []),
     "dit_ws_status_offset": (_sz, []),
     "dit_gamma_route": (_i32, [_vp, _vp, _i32, _i64, _f, _f, _f, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "dit_gamma_route_noalloc": (_i32, [_vp, _vp, _i32, _i64, _f, _f, _f, _i32, _vp, _vp, _vp]),
     "dit_hadamard_quant_nvfp4": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dit_hadamard_quant_int8": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp]),
     "dit_qgemm_nvfp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _i32, _vp, _sz, _vp]),

@@ -316,3 +316,79 @@ extern "C" dit_status dit_tdc_step(int mode, const void* x_in, const void* x_out
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
+
+// ---------------------------------------------------------------------------------------
+// Gamma + routing without a caller-supplied workspace.
+//
+// Some callers cannot hand this library a device buffer: an inference-engine plugin whose
+// memory is planned by the engine before execution and which may not allocate while it
+// enqueues work, or a latency-critical loop that cannot pay for cudaMalloc (which may
+// synchronise the whole device).  For them the per-CTA partial sums and the completion
+// counter of the Gamma reduction live in the fixed device array below instead of a
+// workspace.  It holds a 256-byte header (status word, completion counter) and partial
+// sums for at most NOALLOC_MAX_CTAS CTAs: 20,736 bytes that every GPU which loads the
+// library keeps until the process exits.  All calls share it.
+// ---------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace dit6 {
+constexpr int NOALLOC_MAX_CTAS = 640;
+constexpr size_t NOALLOC_SCRATCH_BYTES = WS_PARTIALS + (size_t)NOALLOC_MAX_CTAS * 4 * sizeof(double);
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+static void* g_noalloc_ptr[NOALLOC_MAX_DEVICES];
+static std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device.  The first call on a device
+// looks the address up (cudaGetSymbolAddress) and zero-fills the array once, synchronously.
+static dit_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DIT_ERR_CUDA;
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return DIT_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return DIT_ERR_CUDA;
+    if (cudaMemset(p, 0, NOALLOC_SCRATCH_BYTES) != cudaSuccess) return DIT_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DIT_OK;
+}
+}  // namespace dit6
+
+extern "C" dit_status dit_gamma_route_noalloc(const void* x_in, const void* x_out, dit_dtype dt,
+                                              int64_t n, const float* alpha, const float* beta,
+                                              const float* thr, int n_layers, float* gamma_dev,
+                                              int32_t* routes_dev, dit_stream_t stream) {
+  if (!x_in || !x_out || n <= 0 || !gamma_dev) return DIT_ERR_INVALID_ARG;
+  if (dt != DIT_F32 && dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
+  if (n_layers < 0 || n_layers > DIT_MAX_LAYERS) return DIT_ERR_INVALID_ARG;
+  if (n_layers > 0 && (!alpha || !beta || !thr || !routes_dev)) return DIT_ERR_INVALID_ARG;
+  if (!aligned32(x_in) || !aligned32(x_out)) return DIT_ERR_ALIGNMENT;
+  const unsigned grid = red_grid(n, dt == DIT_BF16 ? 16 : 8);
+  if (grid > (unsigned)NOALLOC_MAX_CTAS) return DIT_ERR_UNSUPPORTED;  // scratch too small
+  void* scratch = nullptr;
+  dit_status s = noalloc_scratch(&scratch);
+  if (s != DIT_OK) return s;
+  RouteParams rp;
+  rp.n_layers = n_layers;
+  for (int l = 0; l < n_layers; ++l) {
+    rp.alpha[l] = alpha[l];
+    rp.beta[l] = beta[l];
+    rp.thr[l] = thr[l];
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the status word and completion counter must start at zero for every call
+  if (cudaMemsetAsync(scratch, 0, 8, st) != cudaSuccess) return DIT_ERR_CUDA;
+  if (dt == DIT_BF16)
+    k_gamma_route<__nv_bfloat16><<<grid, RED_THREADS, 0, st>>>(x_in, x_out, n, rp, gamma_dev,
+                                                               routes_dev, scratch);
+  else
+    k_gamma_route<float><<<grid, RED_THREADS, 0, st>>>(x_in, x_out, n, rp, gamma_dev,
+                                                       routes_dev, scratch);
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
