@@ -1,0 +1,115 @@
+"""Time one libdit6 kernel on one shape (CUDA events, L2 flushed between repetitions).
+
+  python -m int8_mixed_precision_gb300.kernel_bench --case gemm_nvfp4 --m 17776 --n 5760 --k 1920
+
+Cases: quant_int8, quant_nvfp4 (two passes), quant_nvfp4_given (one pass, tensor scale
+given), gamma, tdc_commit, tdc_skip, gemm_int8, gemm_nvfp4.  Inputs are synthetic bf16
+activations (N(0,1), 1% outlier channels x50) and N(0,0.02) weights.  Prints one JSON line
+with the median time and the algorithmic rate (GB/s for streaming kernels, TFLOP/s for
+GEMMs).  Also the small cases used for ncu captures.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import statistics
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", required=True)
+    ap.add_argument("--m", type=int, default=17776)
+    ap.add_argument("--n", type=int, default=5760)
+    ap.add_argument("--k", type=int, default=1920)
+    ap.add_argument("--hblock", type=int, default=64)
+    ap.add_argument("--reps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--no-flush", action="store_true")
+    a = ap.parse_args(argv)
+
+    import torch
+
+    import int8_mixed_precision_gb300 as dit
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    ws = dit.workspace(dev)
+    m, n, k = a.m, a.n, a.k
+
+    def act(rows, cols):
+        x = torch.randn(rows, cols, device=dev, generator=g)
+        x[:, torch.randperm(cols, device=dev, generator=g)[: max(1, cols // 100)]] *= 50.0
+        return x.to(torch.bfloat16)
+
+    case = a.case
+    if case in ("quant_int8", "quant_nvfp4", "quant_nvfp4_given"):
+        x = act(m, k)
+        if case == "quant_int8":
+            q = torch.empty(m, k, dtype=torch.int8, device=dev)
+            s = torch.empty(m, device=dev)
+            fn = lambda: dit.hadamard_quant_int8(x, a.hblock, q, s)
+            units, unit = m * k * 3 + 4 * m, "GB/s"
+        else:
+            b = dit.alloc_nvfp4(m, k, dev)
+            dit.hadamard_quant_nvfp4(x, a.hblock, b["codes"], b["sf"], b["gs"], ws)
+            sg = b["gs"].clone() if case == "quant_nvfp4_given" else None
+            fn = lambda: dit.hadamard_quant_nvfp4(x, a.hblock, b["codes"], b["sf"], b["gs"], ws, tensor_scale_in=sg)
+            units, unit = m * k * 2 + m * k // 2 + m * k // 16, "GB/s"
+    elif case in ("gamma", "tdc_commit", "tdc_skip"):
+        xi = act(m, k)
+        xo = (xi.float() * 1.05).to(torch.bfloat16)
+        gam = torch.empty(1, device=dev)
+        sim = torch.empty(1, device=dev)
+        if case == "gamma":
+            r = torch.empty(4, dtype=torch.int32, device=dev)
+            fn = lambda: dit.gamma_route(xi, xo, [1.0] * 4, [0.0] * 4, [0.05] * 4, gam, r, ws)
+            units = m * k * 4
+        elif case == "tdc_commit":
+            d1, d2 = torch.zeros_like(xi), torch.empty_like(xi)
+            fn = lambda: dit.tdc_step(dit.TDC_COMMIT, xi, ws, x_out=xo, d1=d1, d_new=d2, gamma=gam, sim=sim)
+            units = m * k * 8
+        else:
+            d1, out = torch.zeros_like(xi), torch.empty_like(xi)
+            fn = lambda: dit.tdc_step(dit.TDC_SKIP, xi, ws, x_out_skip=out, d1=d1)
+            units = m * k * 6
+        unit = "GB/s"
+    elif case in ("gemm_int8", "gemm_nvfp4"):
+        x = act(m, k)
+        w = torch.randn(n, k, device=dev, generator=g) * 0.02
+        lin = dit.RoutedLinear(dit.QuantizedWeight(w, a.hblock, ws), m, ws, dev)
+        y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        if case == "gemm_int8":
+            lin(x, dit.ROUTE_INT8, y)
+            fn = lambda: dit.qgemm_int8(lin.a8["q"], lin.a8["scale"], lin.w.int8["q"], lin.w.int8["scale"], y, ws)
+        else:
+            lin(x, dit.ROUTE_NVFP4, y)
+            fn = lambda: dit.qgemm_nvfp4(lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], lin.w.nvfp4["codes"],
+                                         lin.w.nvfp4["sf"], lin.w.nvfp4["gs"], y, ws)
+        units, unit = 2 * m * n * k, "TFLOP/s"
+    else:
+        raise SystemExit(f"unknown case {case}")
+
+    flush = None if a.no_flush else torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(a.warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(a.reps):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize()
+    assert dit.device_status(ws) == 0, "device status raised"
+    t = statistics.median(times)
+    rate = units / (t * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
+    print(json.dumps({"case": case, "m": m, "n": n, "k": k, "median_us": round(t * 1e3, 2),
+                      "min_us": round(min(times) * 1e3, 2), "rate": round(rate, 2), "unit": unit}))
+
+
+if __name__ == "__main__":
+    main()
