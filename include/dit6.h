@@ -47,7 +47,7 @@ typedef enum {
   DIT_ERR_TIMEOUT = 5      /* device status bit: a bounded wait inside a kernel ran out */
 } dit_status;
 
-typedef enum { DIT_F32 = 0, DIT_BF16 = 1 } dit_dtype;
+typedef enum { DIT_F32 = 0, DIT_BF16 = 1, DIT_I8 = 2 } dit_dtype;
 typedef enum { DIT_ROUTE_NVFP4 = 0, DIT_ROUTE_INT8 = 1 } dit_route;
 typedef enum { DIT_TDC_COMMIT = 0, DIT_TDC_SKIP = 1 } dit_tdc_mode;
 
@@ -148,11 +148,14 @@ dit_status dit_hadamard_quant_nvfp4(const void* x, dit_dtype dt, int64_t rows, i
  * [-127, 127]; an all-zero row gives s = 0 and q = 0.  The same call quantises weights
  * per output channel (rows of W).
  *
- * x     : device [rows x k] of dtype dt; k % 64 == 0, k <= 65536; hblock in {16,32,64}.
- * q     : device int8 [rows x k].     row_scale : device float [rows].
+ * x     : device [rows x k] of dtype dt; k % 64 == 0, k <= 16384; hblock in {16,32,64}.
+ * q     : device [rows x k] codes in container q_dt: DIT_I8 (int8) or DIT_BF16 (the same
+ *         integers stored as bf16, exact; the operand format of the INT8 GEMM on the bf16
+ *         tensor pipe).
+ * row_scale : device float [rows].
  * ------------------------------------------------------------------------------------ */
 dit_status dit_hadamard_quant_int8(const void* x, dit_dtype dt, int64_t rows, int64_t k,
-                                   int hblock, int8_t* q, float* row_scale,
+                                   int hblock, void* q, dit_dtype q_dt, float* row_scale,
                                    dit_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
@@ -177,11 +180,17 @@ dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a
  *
  * acc[m, n] = sum_k a[m, k] b[n, k] (int32, exact);
  * Y[m, n]   = (float(acc) * a_scale[m]) * b_scale[n] (+ bias[n]).
- * a : device int8 [m x k]; b : device int8 [n x k]; k % 16 == 0; n % 8 == 0.
+ * a, b : device codes [m x k] and [n x k] in container ab_dt:
+ *        DIT_I8   -> warp-level IMMA (mma.sync s8) path;
+ *        DIT_BF16 -> tcgen05 bf16 path: the integer codes are exact in bf16, products exact
+ *                    in fp32, and K is accumulated in chunks of <= 1024 so every partial sum
+ *                    stays below 2^24 (exact), then summed in int32.  Same results, bit for
+ *                    bit, as the IMMA path; ~10x its throughput on sm_103a.
+ * k % 16 == 0; n % 8 == 0.
  * acc_debug : device int32 [m x n] or NULL (writes the raw accumulators as well).
  * ------------------------------------------------------------------------------------ */
-dit_status dit_qgemm_int8(const int8_t* a, const float* a_scale, const int8_t* b,
-                          const float* b_scale, int64_t m, int64_t n, int64_t k,
+dit_status dit_qgemm_int8(const void* a, const float* a_scale, const void* b,
+                          const float* b_scale, dit_dtype ab_dt, int64_t m, int64_t n, int64_t k,
                           const float* bias, void* y, dit_dtype y_dt, int32_t* acc_debug,
                           void* ws, size_t ws_bytes, dit_stream_t stream);
 

@@ -35,6 +35,8 @@ def _dt(t) -> int:
         return 0
     if t.dtype == torch.bfloat16:
         return 1
+    if t.dtype == torch.int8:
+        return 2
     raise DitError(f"unsupported dtype {t.dtype}")
 
 
@@ -125,8 +127,9 @@ def hadamard_quant_nvfp4(x, hblock, codes, sf, tensor_scale, ws, tensor_scale_in
 
 
 def hadamard_quant_int8(x, hblock, q, row_scale, stream=None):
+    """q: int8 codes, or the same integers in a bf16 tensor (operands of the bf16-pipe GEMM)."""
     rows, k = x.shape
-    st = lib().dit_hadamard_quant_int8(_p(x), _dt(x), rows, k, hblock, _p(q), _p(row_scale),
+    st = lib().dit_hadamard_quant_int8(_p(x), _dt(x), rows, k, hblock, _p(q), _dt(q), _p(row_scale),
                                        _stream(stream))
     _check(st, "dit_hadamard_quant_int8")
 
@@ -139,8 +142,11 @@ def qgemm_nvfp4(a, a_sf, a_gs, b, b_sf, b_gs, y, ws, bias=None, stream=None):
 
 
 def qgemm_int8(a, a_scale, b, b_scale, y, ws, bias=None, acc_debug=None, stream=None):
+    """a, b: int8 codes (IMMA path) or bf16-held integer codes (tcgen05 bf16 path)."""
+    if a.dtype != b.dtype:
+        raise DitError("qgemm_int8: a and b must use the same code container")
     m, n, k = a.shape[0], b.shape[0], a.shape[1]
-    st = lib().dit_qgemm_int8(_p(a), _p(a_scale), _p(b), _p(b_scale), m, n, k, _p(bias), _p(y),
+    st = lib().dit_qgemm_int8(_p(a), _p(a_scale), _p(b), _p(b_scale), _dt(a), m, n, k, _p(bias), _p(y),
                               _dt(y), _p(acc_debug), _p(ws), ws.numel(), _stream(stream))
     _check(st, "dit_qgemm_int8")
 
@@ -194,9 +200,11 @@ def alloc_nvfp4(rows: int, k: int, device="cuda") -> dict:
             "gs": torch.empty(1, dtype=torch.float32, device=device)}
 
 
-def alloc_int8(rows: int, k: int, device="cuda") -> dict:
+def alloc_int8(rows: int, k: int, device="cuda", container: str = "bf16") -> dict:
+    """INT8 codes in an int8 tensor, or in a bf16 tensor ("bf16": the fast GEMM path)."""
     torch = _torch()
-    return {"q": torch.empty(rows, k, dtype=torch.int8, device=device),
+    dt = torch.bfloat16 if container == "bf16" else torch.int8
+    return {"q": torch.empty(rows, k, dtype=dt, device=device),
             "scale": torch.empty(rows, dtype=torch.float32, device=device)}
 
 
@@ -204,11 +212,11 @@ class QuantizedWeight:
     """A weight W [N x K] prepared offline in both formats (block Hadamard along K, then an
     NVFP4 copy and a per-output-channel INT8 copy), all on the device."""
 
-    def __init__(self, w, hblock: int, ws):
+    def __init__(self, w, hblock: int, ws, int8_container: str = "bf16"):
         n, k = w.shape
         self.n, self.k, self.hblock = n, k, hblock
         self.nvfp4 = alloc_nvfp4(n, k, w.device)
-        self.int8 = alloc_int8(n, k, w.device)
+        self.int8 = alloc_int8(n, k, w.device, int8_container)
         hadamard_quant_nvfp4(w, hblock, self.nvfp4["codes"], self.nvfp4["sf"], self.nvfp4["gs"], ws)
         hadamard_quant_int8(w, hblock, self.int8["q"], self.int8["scale"])
 
@@ -221,7 +229,8 @@ class RoutedLinear:
         self.w = weight
         self.ws = ws
         self.a4 = alloc_nvfp4(max_tokens, weight.k, device)
-        self.a8 = alloc_int8(max_tokens, weight.k, device)
+        container = "bf16" if weight.int8["q"].dtype == _torch().bfloat16 else "int8"
+        self.a8 = alloc_int8(max_tokens, weight.k, device, container)
 
     def __call__(self, x, route: int, y, bias=None, tensor_scale_in=None, stream=None):
         m = x.shape[0]

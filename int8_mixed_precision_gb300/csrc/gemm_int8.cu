@@ -157,23 +157,33 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 using namespace dit6;
 
-extern "C" dit_status dit_qgemm_int8(const int8_t* a, const float* a_scale, const int8_t* b,
-                                     const float* b_scale, int64_t m, int64_t n, int64_t k,
-                                     const float* bias, void* y, dit_dtype y_dt,
+namespace dit6 {
+dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
+                        int64_t n, int64_t k, const float* bias, void* y, int y_bf16, int32_t* acc_out,
+                        void* ws, cudaStream_t st);
+}
+
+extern "C" dit_status dit_qgemm_int8(const void* a, const float* a_scale, const void* b,
+                                     const float* b_scale, dit_dtype ab_dt, int64_t m, int64_t n,
+                                     int64_t k, const float* bias, void* y, dit_dtype y_dt,
                                      int32_t* acc_debug, void* ws, size_t ws_bytes,
                                      dit_stream_t stream) {
   if (!a || !b || !a_scale || !b_scale || !y || !ws || ws_bytes < WS_BYTES) return DIT_ERR_INVALID_ARG;
   if (m <= 0 || n <= 0 || k <= 0 || m > 0x7fffffff || n > 0x7fffffff || k > 0x7fffffff)
     return DIT_ERR_INVALID_ARG;
   if (y_dt != DIT_F32 && y_dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
+  if (ab_dt != DIT_I8 && ab_dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
   if (k % 16 || n % 8) return DIT_ERR_UNSUPPORTED;
   if (!aligned32(a) || !aligned32(b) || !aligned32(y) || !aligned32(ws) ||
       (acc_debug && !aligned32(acc_debug)))
     return DIT_ERR_ALIGNMENT;
+  if (ab_dt == DIT_BF16)
+    return gemm_int8_tc(a, a_scale, b, b_scale, m, n, k, bias, y, y_dt == DIT_BF16 ? 1 : 0, acc_debug,
+                        ws, reinterpret_cast<cudaStream_t>(stream));
   CUtensorMap ta, tb;
-  if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<int8_t*>(a), (uint64_t)k,
+  if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(a), (uint64_t)k,
                       (uint64_t)m, (uint64_t)k, i8::BK, i8::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<int8_t*>(b), (uint64_t)k,
+      !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(b), (uint64_t)k,
                       (uint64_t)n, (uint64_t)k, i8::BK, i8::BN, CU_TENSOR_MAP_SWIZZLE_128B))
     return DIT_ERR_CUDA;
   static bool attr_done = false;

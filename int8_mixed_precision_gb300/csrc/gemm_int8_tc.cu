@@ -1,0 +1,341 @@
+// INT8 route GEMM on the bf16 tcgen05 tensor pipe, with exact int32 accumulators.
+//
+// 6Bit-Diffusion (arXiv 2603.18742): [EN] gist.science 2.A Mechanism 3 (volatile layers go to
+// INT8).  sm_103a has no tcgen05 integer MMA and its IMMA path peaks near 151 TOPS, 13x below
+// the bf16 tensor rate.  The INT8 codes (integers in [-127, 127]) are exact in bf16 and their
+// products (|p| <= 16129) exact in fp32, so this kernel runs the INT8 contraction on
+// tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in tensor memory) and keeps it exact by
+// accumulating K in chunks of at most 1024: every partial sum of a chunk is an integer of
+// magnitude <= 1024 * 16129 < 2^24, hence exactly representable in fp32 whatever the order of
+// the additions.  Each finished chunk is drained from tensor memory, converted to int32
+// (exact) and added to int32 running sums in the epilogue warps' registers.
+//
+// Persistent CTAs (one per SM) walk output tiles of 128 x BN.  Warp 0: TMA producer (128-byte
+// swizzled A/B tiles, STAGES-deep ring).  Warp 1: tensor-memory allocation and the MMA issuer;
+// chunk accumulators alternate between two tensor-memory buffers, so the MMAs of chunk c+1
+// (also of the next tile) overlap the drain of chunk c.  Warps 2..: epilogue, two warps per
+// tensor-memory lane quarter when BN > 128.  Every wait is bounded.
+#include "common.cuh"
+
+namespace dit6 {
+namespace i8tc {
+
+constexpr int BM = 128, BK = 64;  // BK bf16 elements = 128 bytes per row
+constexpr int KCHUNK_BLOCKS = 16;  // 16 x 64 = 1024 elements per exact chunk
+constexpr int A_BYTES = BM * BK * 2;
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN == 128 ? 3 : (BN == 192 ? 5 : 4);
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int EPI_WARPS = BN <= 128 ? 4 : 8;         // 4 lane quarters x (1 or 2)
+  static constexpr int CW = BN / (EPI_WARPS / 4);             // columns per epilogue thread
+  static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+  static_assert(CW % 16 == 0 && CW <= 128, "epilogue split");
+};
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// kind::f16 instruction descriptor: bf16 x bf16 -> fp32, K-major A and B
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int BN>
+__global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
+    k_gemm_int8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N,
+                   int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
+                   int32_t* __restrict__ acc_out, void* ws) {
+  using C = Cfg<BN>;
+  constexpr int S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
+  // bars: full[S], empty[S], chunk_full[2], chunk_empty[2], mma_done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t sbase = smem_u32(smem);
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + S + s); };
+  auto cfull = [&](int b) { return smem_u32(bars + 2 * S + b); };
+  auto cempty = [&](int b) { return smem_u32(bars + 2 * S + 2 + b); };
+  const uint32_t mma_done = smem_u32(bars + 2 * S + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles_n = (N + BN - 1) / BN;
+  const int n_tiles = ((M + BM - 1) / BM) * n_tiles_n;
+  const int nkb = (K + BK - 1) / BK;
+  const int nchunks = (nkb + KCHUNK_BLOCKS - 1) / KCHUNK_BLOCKS;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(cfull(b), 1);
+      mbar_init(cempty(b), C::EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {  // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      uint32_t kc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full(s), C::STAGE_BYTES);
+          tma_load_2d(sbase + s * C::STAGE_BYTES, &tmA, full(s), kb * BK, m0);
+          tma_load_2d(sbase + s * C::STAGE_BYTES + A_BYTES, &tmB, full(s), kb * BK, n0);
+        }
+      }
+      if (!ok) {  // let copies still in flight land before the CTA exits
+        volatile int no_abort = 0;
+        const uint32_t first = kc > (uint32_t)S ? kc - S : 0;
+        for (uint32_t c = first; c < kc; ++c) mbar_wait(full(c % S), (c / S) & 1, ws, &no_abort);
+      }
+    }
+  } else if (warp == 1) {  // --------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      uint32_t kc = 0, cc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        for (int ch = 0; ch < nchunks && ok; ++ch, ++cc) {
+          const int buf = cc & 1;
+          if (!mbar_wait(cempty(buf), ((cc >> 1) & 1) ^ 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + buf * BN;
+          const int kb0 = ch * KCHUNK_BLOCKS;
+          const int kb1 = min(nkb, kb0 + KCHUNK_BLOCKS);
+          for (int kb = kb0; kb < kb1; ++kb, ++kc) {
+            const int s = kc % S;
+            if (!mbar_wait(full(s), (kc / S) & 1, ws, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_s = sbase + s * C::STAGE_BYTES, b_s = a_s + A_BYTES;
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j)
+              tc_mma(d, desc_sw128(a_s + j * 32), desc_sw128(b_s + j * 32), idesc,
+                     (kb > kb0 || j > 0) ? 1u : 0u);
+            tc_commit(empty(s));
+          }
+          if (ok) tc_commit(cfull(buf));
+        }
+      }
+      tc_commit(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait(mma_done, 0, ws, &no_abort);  // every issued MMA has completed
+    }
+    __syncwarp();
+  } else {  // ------------------------------------------------------------- epilogue warps
+    const int e = warp - 2;
+    const int q = warp & 3;        // tensor-memory lane quarter of this warp
+    const int half = e >> 2;       // which CW-column part of the tile
+    uint32_t cc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
+      constexpr int CW = C::CW;
+      int acc[CW];
+#pragma unroll
+      for (int i = 0; i < CW; ++i) acc[i] = 0;
+      for (int ch = 0; ch < nchunks; ++ch, ++cc) {
+        const int buf = cc & 1;
+        if (!mbar_wait(cfull(buf), (cc >> 1) & 1, ws, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + buf * BN + half * CW;
+#pragma unroll
+        for (int c = 0; c < CW / 16; ++c) {
+          uint32_t r[16];
+          tc_ld16(base + c * 16, r);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[c * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cempty(buf));
+      }
+      if (!ok) break;
+      const int row = m0 + q * 32 + lane;
+      const int col0 = n0 + half * CW;
+      if (row < M && col0 < N) {
+        const float sa = a_scale[row];
+        const int64_t off = (int64_t)row * N + col0;
+#pragma unroll
+        for (int c = 0; c < CW / 16; ++c) {  // 16 columns per step
+          const int cb = col0 + c * 16;
+          if (cb >= N) break;
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = cb + i < N ? cb + i : N - 1;
+            v[i] = __fmul_rn(__fmul_rn((float)acc[c * 16 + i], sa), b_scale[col]);
+            if (bias) v[i] = __fadd_rn(v[i], bias[col]);
+          }
+          if (cb + 16 <= N && (N % 16) == 0) {
+            if (y_bf16) {
+              uint32_t w[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) w[i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
+              U8x32 o;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o.w[i] = w[i];
+              st256(reinterpret_cast<uint16_t*>(y) + off + c * 16, o);
+            } else {
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                U8x32 o;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o.w[i] = __float_as_uint(v[8 * b + i]);
+                st256(reinterpret_cast<float*>(y) + off + c * 16 + 8 * b, o);
+              }
+            }
+            if (acc_out) {
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                U8x32 o;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o.w[i] = (uint32_t)acc[c * 16 + 8 * b + i];
+                st256(acc_out + off + c * 16 + 8 * b, o);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              if (cb + i >= N) continue;
+              if (y_bf16)
+                reinterpret_cast<__nv_bfloat16*>(y)[off + c * 16 + i] = __float2bfloat16_rn(v[i]);
+              else
+                reinterpret_cast<float*>(y)[off + c * 16 + i] = v[i];
+              if (acc_out) acc_out[off + c * 16 + i] = acc[c * 16 + i];
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+template <int BN>
+dit_status launch(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
+                  int64_t n, int64_t k, const float* bias, void* y, int y_bf16, int32_t* acc_out,
+                  void* ws, cudaStream_t st) {
+  using C = Cfg<BN>;
+  CUtensorMap ta, tb;
+  if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(a), (uint64_t)k, (uint64_t)m,
+                      (uint64_t)k * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(b), (uint64_t)k, (uint64_t)n,
+                      (uint64_t)k * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return DIT_ERR_CUDA;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(k_gemm_int8_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
+      return DIT_ERR_CUDA;
+    attr_done = true;
+  }
+  const int64_t tiles = ((m + BM - 1) / BM) * ((n + BN - 1) / BN);
+  int64_t grid = num_sms();
+  if (grid > tiles) grid = tiles;
+  k_gemm_int8_tc<BN><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(
+      ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, y_bf16, acc_out, ws);
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
+}  // namespace i8tc
+
+dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
+                        int64_t n, int64_t k, const float* bias, void* y, int y_bf16, int32_t* acc_out,
+                        void* ws, cudaStream_t st) {
+  const char* e = getenv("DIT6_INT8_TC_BN");
+  const int bn = e ? atoi(e) : 256;
+  if (bn == 128) return i8tc::launch<128>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
+  if (bn == 256) return i8tc::launch<256>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
+  return i8tc::launch<192>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
+}
+
+}  // namespace dit6

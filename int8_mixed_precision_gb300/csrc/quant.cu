@@ -67,10 +67,12 @@ __device__ __forceinline__ float amax_range(const float2 (&v)[32], int p0, int n
 // ---------------------------------------------------------------------------------------
 // INT8: CTA = `tr` whole rows x `upr` units per row; row amax through shared memory.
 // ---------------------------------------------------------------------------------------
-template <typename T, int HB>
+// OUT_BF16: the integer codes are written as bf16 values (exact for |q| <= 127), the
+// operand format of the INT8 GEMM that runs on the bf16 tensor pipe.
+template <typename T, int HB, bool OUT_BF16>
 __global__ void __launch_bounds__(256) k_quant_int8(const void* __restrict__ x, int64_t rows,
                                                     int upr, int tr, float inv_sqrt_b,
-                                                    int8_t* __restrict__ q,
+                                                    void* __restrict__ q,
                                                     float* __restrict__ row_scale) {
   __shared__ unsigned row_amax[256];
   const int t = threadIdx.x;
@@ -91,20 +93,33 @@ __global__ void __launch_bounds__(256) k_quant_int8(const void* __restrict__ x, 
   const float s = __fdiv_rn(amax, 127.0f);
   const float inv = s == 0.f ? 0.f : __frcp_rn(s);
   const float2 iv = make_float2(inv, inv);
-  U8x32 out[2];
+  if (OUT_BF16) {
+    U8x32 out[4];
 #pragma unroll
-  for (int p = 0; p < 32; p += 2) {
-    const float2 a = mul2(v[p], iv), b = mul2(v[p + 1], iv);
-    // |a|,|b| <= 127 * (1 + 3 * 2^-24): round-to-nearest-even never leaves [-127, 127]
-    const int q0 = __float2int_rn(a.x), q1 = __float2int_rn(a.y);
-    const int q2 = __float2int_rn(b.x), q3 = __float2int_rn(b.y);
-    const uint32_t w = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) |
-                       ((uint32_t)(q2 & 0xff) << 16) | ((uint32_t)(q3 & 0xff) << 24);
-    out[p / 16].w[(p % 16) / 2] = w;
+    for (int p = 0; p < 32; ++p) {
+      const float2 a = mul2(v[p], iv);
+      // |a| <= 127 * (1 + 3 * 2^-24): round-to-nearest-even never leaves [-127, 127]
+      out[p / 8].w[p % 8] = f2_to_bf16x2(rintf(a.x), rintf(a.y));
+    }
+    char* dst = reinterpret_cast<char*>(q) + unit * (UNIT * 2);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) st256(dst + 32 * c, out[c]);
+  } else {
+    U8x32 out[2];
+#pragma unroll
+    for (int p = 0; p < 32; p += 2) {
+      const float2 a = mul2(v[p], iv), b = mul2(v[p + 1], iv);
+      // |a|,|b| <= 127 * (1 + 3 * 2^-24): round-to-nearest-even never leaves [-127, 127]
+      const int q0 = __float2int_rn(a.x), q1 = __float2int_rn(a.y);
+      const int q2 = __float2int_rn(b.x), q3 = __float2int_rn(b.y);
+      const uint32_t w = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) |
+                         ((uint32_t)(q2 & 0xff) << 16) | ((uint32_t)(q3 & 0xff) << 24);
+      out[p / 16].w[(p % 16) / 2] = w;
+    }
+    int8_t* dst = reinterpret_cast<int8_t*>(q) + unit * UNIT;
+    st256(dst, out[0]);
+    st256(dst + 32, out[1]);
   }
-  int8_t* dst = q + unit * UNIT;
-  st256(dst, out[0]);
-  st256(dst + 32, out[1]);
   if (j == 0) row_scale[row] = s;
 }
 
@@ -205,8 +220,8 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const void* __restrict__ x,
   }
 }
 
-template <typename T>
-static dit_status launch_int8(const void* x, int64_t rows, int64_t k, int hb, int8_t* q,
+template <typename T, bool OB>
+static dit_status launch_int8(const void* x, int64_t rows, int64_t k, int hb, void* q,
                               float* rs, cudaStream_t st) {
   const int upr = (int)(k / UNIT);
   const int tr = upr >= 256 ? 1 : 256 / upr;
@@ -215,9 +230,9 @@ static dit_status launch_int8(const void* x, int64_t rows, int64_t k, int hb, in
   if (grid > 0x7fffffff) return DIT_ERR_UNSUPPORTED;
   const float isb = (float)(1.0 / sqrt((double)hb));
   switch (hb) {
-    case 16: k_quant_int8<T, 16><<<(unsigned)grid, threads, 0, st>>>(x, rows, upr, tr, isb, q, rs); break;
-    case 32: k_quant_int8<T, 32><<<(unsigned)grid, threads, 0, st>>>(x, rows, upr, tr, isb, q, rs); break;
-    default: k_quant_int8<T, 64><<<(unsigned)grid, threads, 0, st>>>(x, rows, upr, tr, isb, q, rs); break;
+    case 16: k_quant_int8<T, 16, OB><<<(unsigned)grid, threads, 0, st>>>(x, rows, upr, tr, isb, q, rs); break;
+    case 32: k_quant_int8<T, 32, OB><<<(unsigned)grid, threads, 0, st>>>(x, rows, upr, tr, isb, q, rs); break;
+    default: k_quant_int8<T, 64, OB><<<(unsigned)grid, threads, 0, st>>>(x, rows, upr, tr, isb, q, rs); break;
   }
   DIT_CHECK_LAUNCH();
   return DIT_OK;
@@ -260,16 +275,20 @@ static dit_status check_quant_args(const void* x, dit_dtype dt, int64_t rows, in
 }
 
 extern "C" dit_status dit_hadamard_quant_int8(const void* x, dit_dtype dt, int64_t rows,
-                                              int64_t k, int hblock, int8_t* q,
+                                              int64_t k, int hblock, void* q, dit_dtype q_dt,
                                               float* row_scale, dit_stream_t stream) {
   dit_status s = check_quant_args(x, dt, rows, k, hblock);
   if (s != DIT_OK) return s;
   if (!q || !row_scale) return DIT_ERR_INVALID_ARG;
+  if (q_dt != DIT_I8 && q_dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
   if (k > 256 * UNIT) return DIT_ERR_UNSUPPORTED;
   if (!aligned32(q)) return DIT_ERR_ALIGNMENT;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return dt == DIT_BF16 ? launch_int8<__nv_bfloat16>(x, rows, k, hblock, q, row_scale, st)
-                        : launch_int8<float>(x, rows, k, hblock, q, row_scale, st);
+  if (q_dt == DIT_BF16)
+    return dt == DIT_BF16 ? launch_int8<__nv_bfloat16, true>(x, rows, k, hblock, q, row_scale, st)
+                          : launch_int8<float, true>(x, rows, k, hblock, q, row_scale, st);
+  return dt == DIT_BF16 ? launch_int8<__nv_bfloat16, false>(x, rows, k, hblock, q, row_scale, st)
+                        : launch_int8<float, false>(x, rows, k, hblock, q, row_scale, st);
 }
 
 extern "C" dit_status dit_hadamard_quant_nvfp4(const void* x, dit_dtype dt, int64_t rows,

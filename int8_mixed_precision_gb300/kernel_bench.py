@@ -25,6 +25,7 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--int8-container", choices=["bf16", "int8"], default="bf16")
     a = ap.parse_args(argv)
 
     import torch
@@ -45,10 +46,10 @@ def main(argv=None):
     if case in ("quant_int8", "quant_nvfp4", "quant_nvfp4_given"):
         x = act(m, k)
         if case == "quant_int8":
-            q = torch.empty(m, k, dtype=torch.int8, device=dev)
+            q = torch.empty(m, k, dtype=torch.int8 if a.int8_container == "int8" else torch.bfloat16, device=dev)
             s = torch.empty(m, device=dev)
             fn = lambda: dit.hadamard_quant_int8(x, a.hblock, q, s)
-            units, unit = m * k * 3 + 4 * m, "GB/s"
+            units, unit = m * k * (2 + q.element_size()) + 4 * m, "GB/s"
         else:
             b = dit.alloc_nvfp4(m, k, dev)
             dit.hadamard_quant_nvfp4(x, a.hblock, b["codes"], b["sf"], b["gs"], ws)
@@ -76,7 +77,7 @@ def main(argv=None):
     elif case in ("gemm_int8", "gemm_nvfp4"):
         x = act(m, k)
         w = torch.randn(n, k, device=dev, generator=g) * 0.02
-        lin = dit.RoutedLinear(dit.QuantizedWeight(w, a.hblock, ws), m, ws, dev)
+        lin = dit.RoutedLinear(dit.QuantizedWeight(w, a.hblock, ws, int8_container=a.int8_container), m, ws, dev)
         y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
         if case == "gemm_int8":
             lin(x, dit.ROUTE_INT8, y)

@@ -49,12 +49,17 @@ def _status_clean(ws):
     (7, 3072, "bf16", 32),
     (1, 12288, "bf16", 64),
 ])
-def test_int8_quant_parity(rows, k, dtype, hb):
+@pytest.mark.parametrize("container", [torch.int8, torch.bfloat16])
+def test_int8_quant_parity(rows, k, dtype, hb, container):
     x, xd = make_x(rows, k, dtype, seed=rows + k)
-    q = torch.empty(rows, k, dtype=torch.int8, device="cuda")
+    q = torch.empty(rows, k, dtype=container, device="cuda")
     s = torch.empty(rows, dtype=torch.float32, device="cuda")
     dit.hadamard_quant_int8(xd, hb, q, s)
-    n_ex, _ = check_int8(host(q), host(s), x, dtype, hb)
+    qh = host(q) if container == torch.int8 else F.bf16_bits_to_f32(host(q))
+    if container == torch.bfloat16:
+        assert np.array_equal(qh, np.rint(qh)) and np.abs(qh).max() <= 127
+        qh = qh.astype(np.int8)
+    n_ex, _ = check_int8(qh, host(s), x, dtype, hb)
     assert n_ex <= max(2, q.numel() // 10000)
 
 
@@ -240,16 +245,25 @@ def test_tdc_loop_decisions_match_oracle(ws):
 # ------------------------------------------------------------------------------ GEMMs
 
 
+def _int8_dev(a, container):
+    t = torch.from_numpy(a).cuda()
+    return t if container == torch.int8 else t.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("container,bn", [(torch.int8, None), (torch.bfloat16, "192"), (torch.bfloat16, "128"),
+                                          (torch.bfloat16, "256")])
 @pytest.mark.parametrize("m,n,k", [(256, 512, 128), (300, 384, 1920), (129, 256, 7680), (1, 8, 16),
-                                   (200, 136, 208)])
-def test_int8_gemm_exact_accumulators(m, n, k, ws):
+                                   (200, 136, 208), (700, 5760 // 10, 2112)])
+def test_int8_gemm_exact_accumulators(m, n, k, container, bn, ws, monkeypatch):
+    if bn:
+        monkeypatch.setenv("DIT6_INT8_TC_BN", bn)
     g = synth.rng(m * n + k)
     a = g.integers(-127, 128, (m, k)).astype(np.int8)
     b = g.integers(-127, 128, (n, k)).astype(np.int8)
     sa = g.random(m).astype(np.float32) * 0.01
     sb = g.random(n).astype(np.float32) * 0.01
     bias = g.standard_normal(n).astype(np.float32)
-    ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    ta, tb = _int8_dev(a, container), _int8_dev(b, container)
     acc = torch.empty(m, n, dtype=torch.int32, device="cuda")
     y = torch.empty(m, n, dtype=torch.float32, device="cuda")
     dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws, bias=dev_f32(bias), acc_debug=acc)
@@ -260,6 +274,36 @@ def test_int8_gemm_exact_accumulators(m, n, k, ws):
     yb = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
     dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), yb, ws, bias=dev_f32(bias))
     assert rel_fro(F.bf16_bits_to_f32(host(yb)), F.bf16_bits_to_f32(F.f32_to_bf16_bits(ref.astype(np.float32)))) <= GEMM_TOL
+    _status_clean(ws)
+
+
+def _adversarial_int8(m, n, k, seed):
+    """Operands that push every exact-chunk partial sum towards its 2^24 bound, mix huge and
+    unit products after a large running sum, and cancel."""
+    g = synth.rng(seed)
+    a = np.full((m, k), 127, np.int8)
+    b = np.full((n, k), 127, np.int8)
+    b[1::2] = -127                                     # all-negative rows
+    a[2, :] = g.choice([-127, 127], size=k)            # random signs: cancellation
+    b[3, k // 2:] = 1                                  # unit products after a large sum
+    a[4, ::7] = -1
+    a[5] = g.integers(-127, 128, k)
+    b[5] = g.integers(-127, 128, k)
+    return a, b
+
+
+@pytest.mark.parametrize("k", [1024, 1040, 2048, 7680, 12288])
+def test_int8_gemm_bf16_pipe_exact_at_the_bound(k, ws):
+    """Extreme codes (+-127 everywhere, totals up to 12288 * 127^2 ~ 2^27.6): the chunked fp32
+    accumulation on the bf16 tensor pipe still gives the exact int32 accumulators."""
+    m, n = 200, 392
+    a, b = _adversarial_int8(m, n, k, seed=k)
+    acc = torch.empty(m, n, dtype=torch.int32, device="cuda")
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    ones_m = torch.ones(m, dtype=torch.float32, device="cuda")
+    ones_n = torch.ones(n, dtype=torch.float32, device="cuda")
+    dit.qgemm_int8(_int8_dev(a, torch.bfloat16), ones_m, _int8_dev(b, torch.bfloat16), ones_n, y, ws, acc_debug=acc)
+    assert np.array_equal(host(acc).astype(np.int64), D.gemm_int8_acc(a, b))
     _status_clean(ws)
 
 
@@ -298,20 +342,27 @@ def test_nvfp4_gemm_parity(m, n, k, cfg, ws, monkeypatch):
 # ------------------------------------------------------------------------------ routed linear
 
 
-@pytest.mark.parametrize("route", [dit.ROUTE_NVFP4, dit.ROUTE_INT8])
-def test_single_linear_end_to_end(route, ws):
+def _codes(t):
+    """INT8 codes on the host from either container."""
+    return host(t) if t.dtype == torch.int8 else F.bf16_bits_to_f32(host(t)).astype(np.int8)
+
+
+@pytest.mark.parametrize("route,container", [(dit.ROUTE_NVFP4, "bf16"), (dit.ROUTE_INT8, "bf16"),
+                                             (dit.ROUTE_INT8, "int8")])
+def test_single_linear_end_to_end(route, container, ws):
     """The 256x128 single linear (Hadamard block 16) along both routes, stage by stage."""
     c = synth.single_linear()
-    wq = dit.QuantizedWeight(dev_f32(c["w"]), 16, ws)
+    wq = dit.QuantizedWeight(dev_f32(c["w"]), 16, ws, int8_container=container)
     lin = dit.RoutedLinear(wq, 256, ws)
     y = torch.empty(256, 512, dtype=torch.float32, device="cuda")
     lin(dev_f32(c["x"]), route, y)
     _status_clean(ws)
     wp = D.prepare_weight(c["w"], 16)
     if route == dit.ROUTE_INT8:
-        check_int8(host(wq.int8["q"]), host(wq.int8["scale"]), c["w"], "f32", 16)
-        check_int8(host(lin.a8["q"]), host(lin.a8["scale"]), c["x"], "f32", 16)
-        ref = D.gemm_int8(host(lin.a8["q"]), host(lin.a8["scale"]), host(wq.int8["q"]), host(wq.int8["scale"]))
+        wqh, aqh = _codes(wq.int8["q"]), _codes(lin.a8["q"])
+        check_int8(wqh, host(wq.int8["scale"]), c["w"], "f32", 16)
+        check_int8(aqh, host(lin.a8["scale"]), c["x"], "f32", 16)
+        ref = D.gemm_int8(aqh, host(lin.a8["scale"]), wqh, host(wq.int8["scale"]))
     else:
         check_nvfp4(host(wq.nvfp4["codes"]), host(wq.nvfp4["sf"]), host(wq.nvfp4["gs"])[0], c["w"], "f32", 16, 512, 128)
         check_nvfp4(host(lin.a4["codes"]), host(lin.a4["sf"]), host(lin.a4["gs"])[0], c["x"], "f32", 16, 256, 128)
@@ -352,11 +403,11 @@ def test_full_size_cogvideox_2b_sampled(ws):
             ref = D.gemm_nvfp4(codes, sf, sg, D.unpack_e2m1(host(wq.nvfp4["codes"])),
                                F.sf_from_tiled(host(wq.nvfp4["sf"]), n, k), host(wq.nvfp4["gs"])[0])
         else:
-            q = host(lin.a8["q"])[rows]
+            q = _codes(lin.a8["q"])[rows]
             s = host(lin.a8["scale"])[rows]
             xr = x[rows]
             check_int8(q, s, xr, "bf16", 64)
-            ref = D.gemm_int8(q, s, host(wq.int8["q"]), host(wq.int8["scale"]))
+            ref = D.gemm_int8(q, s, _codes(wq.int8["q"]), host(wq.int8["scale"]))
         refb = F.bf16_bits_to_f32(F.f32_to_bf16_bits(ref.astype(np.float32)))
         assert rel_fro(yh, refb) <= GEMM_TOL
     _status_clean(ws)
