@@ -277,6 +277,526 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Persistent variant: one CTA per SM walks 128 x BN output tiles; the accumulator is
+// ACC_BUFS-buffered in tensor memory so the epilogue of tile t overlaps the MMAs of tile
+// t+1; scales get one tensor-memory slot per (stage, K step).
+// ---------------------------------------------------------------------------------------
+template <int BN, int STAGES, int ACC_BUFS>
+struct PCfg {
+  static constexpr int NB = BN / 128;
+  static constexpr int B_BYTES = BN * BK / 2;
+  static constexpr int SFA_BYTES = 4 * SF_ATOM;
+  static constexpr int SFB_BYTES = NB * 4 * SF_ATOM;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int SF_COLS = 4 + 4 * NB;
+  static constexpr int SF_BASE = ACC_BUFS * BN;
+  static constexpr int TMEM_USED = SF_BASE + STAGES * 4 * SF_COLS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+  static constexpr int EPI_WARPS = BN / 32;          // 128 columns per epilogue thread
+  static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+  static_assert(TMEM_USED <= 512, "tensor memory");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+template <int BN, int STAGES, int ACC_BUFS>
+__global__ void __launch_bounds__(PCfg<BN, STAGES, ACC_BUFS>::THREADS, 1)
+    k_gemm_nvfp4_p(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
+                   const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
+                   int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
+                   void* ws) {
+  using C = PCfg<BN, STAGES, ACC_BUFS>;
+  constexpr int S = STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
+  // bars: full[S], empty[S], acc_full[ACC_BUFS], acc_empty[ACC_BUFS], mma_done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * ACC_BUFS + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t sbase = smem_u32(smem);
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + S + s); };
+  auto afull = [&](int b) { return smem_u32(bars + 2 * S + b); };
+  auto aempty = [&](int b) { return smem_u32(bars + 2 * S + ACC_BUFS + b); };
+  const uint32_t mma_done = smem_u32(bars + 2 * S + 2 * ACC_BUFS);
+  auto a_tile = [&](int s) { return sbase + s * C::STAGE_BYTES; };
+  auto b_tile = [&](int s) { return a_tile(s) + A_BYTES; };
+  auto sfa_tile = [&](int s) { return b_tile(s) + C::B_BYTES; };
+  auto sfb_tile = [&](int s) { return sfa_tile(s) + C::SFA_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ksteps = K / KSTEP;
+  const int num_kb = (ksteps + 3) / 4;
+  const int k_atoms = K / KSTEP;
+  const int n_tiles_n = (N + BN - 1) / BN;
+  const int n_tiles = ((M + BM - 1) / BM) * n_tiles_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < ACC_BUFS; ++b) {
+      mbar_init(afull(b), 1);
+      mbar_init(aempty(b), C::EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {  // -------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      uint32_t kc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
+        int nb_valid = (N - n0 + 127) / 128;
+        if (nb_valid > C::NB) nb_valid = C::NB;
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int nsub = min(4, ksteps - kb * 4);
+          mbar_expect_tx(full(s), A_BYTES + C::B_BYTES + nsub * SF_ATOM * (1 + nb_valid));
+          tma_load_2d(a_tile(s), &tmA, full(s), kb * (BK / 2), m0);
+          tma_load_2d(b_tile(s), &tmB, full(s), kb * (BK / 2), n0);
+          bulk_load(sfa_tile(s), a_sf + ((size_t)(m0 / 128) * k_atoms + kb * 4) * SF_ATOM, nsub * SF_ATOM,
+                    full(s));
+          for (int nb = 0; nb < nb_valid; ++nb)
+            bulk_load(sfb_tile(s) + nb * 4 * SF_ATOM, b_sf + ((size_t)(n0 / 128 + nb) * k_atoms + kb * 4) * SF_ATOM,
+                      nsub * SF_ATOM, full(s));
+        }
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        const uint32_t first = kc > (uint32_t)S ? kc - S : 0;
+        for (uint32_t c = first; c < kc; ++c) mbar_wait(full(c % S), (c / S) & 1, ws, &no_abort);
+      }
+    }
+  } else if (warp == 1) {  // ------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_nvf4(BM, BN);
+      uint32_t kc = 0, tc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
+        const int n0 = (tile % n_tiles_n) * BN;
+        int nb_valid = (N - n0 + 127) / 128;
+        if (nb_valid > C::NB) nb_valid = C::NB;
+        const int buf = tc % ACC_BUFS;
+        if (!mbar_wait(aempty(buf), ((tc / ACC_BUFS) & 1) ^ 1, ws, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * BN;
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait(full(s), (kc / S) & 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nsub = min(4, ksteps - kb * 4);
+          // all scale copies of the stage first, so the MMAs do not wait on them one by one
+          for (int j = 0; j < nsub; ++j) {
+            const uint32_t sfa_col = C::SF_BASE + (s * 4 + j) * C::SF_COLS;
+            const uint32_t sfb_col = sfa_col + 4;
+            tc_cp_sf(tmem + sfa_col, desc_sf(sfa_tile(s) + j * SF_ATOM));
+            for (int nb = 0; nb < nb_valid; ++nb)
+              tc_cp_sf(tmem + sfb_col + 4 * nb, desc_sf(sfb_tile(s) + nb * 4 * SF_ATOM + j * SF_ATOM));
+          }
+          for (int j = 0; j < nsub; ++j) {
+            const uint32_t sfa_col = C::SF_BASE + (s * 4 + j) * C::SF_COLS;
+            tc_mma(d, desc_sw128(a_tile(s) + j * 32), desc_sw128(b_tile(s) + j * 32), idesc,
+                   tmem + sfa_col, tmem + sfa_col + 4, (kb | j) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty(s));
+        }
+        if (ok) tc_commit(afull(buf));
+      }
+      tc_commit(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait(mma_done, 0, ws, &no_abort);
+    }
+    __syncwarp();
+  } else {  // ----------------------------------------------------- epilogue warps
+    const int e = warp - 2;
+    const int q = warp & 3;
+    const int half = e >> 2;            // 128-column part of the tile
+    const float alpha = __fmul_rn(*a_gs, *b_gs);
+    uint32_t tc = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tc) {
+      const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
+      const int buf = tc % ACC_BUFS;
+      if (!mbar_wait(afull(buf), (tc / ACC_BUFS) & 1, ws, abort_flag)) break;
+      tc_fence_after();
+      const int row = m0 + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * BN + half * 128 + c * 32, r);
+        const int col0 = n0 + half * 128 + c * 32;
+        if (row >= M || col0 >= N) continue;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
+          if (bias) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
+        }
+        const int64_t off = (int64_t)row * N + col0;
+        if (col0 + 32 <= N && (N % 16) == 0) {
+          if (y_bf16) {
+            U8x32 o0, o1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              o0.w[i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
+              o1.w[i] = f2_to_bf16x2(v[16 + 2 * i], v[16 + 2 * i + 1]);
+            }
+            uint16_t* yp = reinterpret_cast<uint16_t*>(y) + off;
+            st256(yp, o0);
+            st256(yp + 16, o1);
+          } else {
+            float* yp = reinterpret_cast<float*>(y) + off;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              U8x32 o;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o.w[i] = __float_as_uint(v[8 * b + i]);
+              st256(yp + 8 * b, o);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (col0 + i >= N) continue;
+            if (y_bf16)
+              reinterpret_cast<__nv_bfloat16*>(y)[off + i] = __float2bfloat16_rn(v[i]);
+            else
+              reinterpret_cast<float*>(y)[off + i] = v[i];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(aempty(buf));
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Band-resident variant (K <= 2048): each persistent CTA walks a contiguous run of 128 x 256
+// tiles in M-major order; the A-side scales of the current 128-row band (all K steps) are
+// copied into tensor memory once per band, so only the B-side scales move per K step.  The
+// scale copies (smem -> tensor memory) have their own limited bandwidth; this halves their
+// bytes per MMA.  Single accumulator buffer.
+// ---------------------------------------------------------------------------------------
+struct RCfg {
+  static constexpr int BN = 256, NB = 2, STAGES = 4;
+  static constexpr int MAX_KSTEPS = 32;                      // K <= 2048
+  static constexpr int B_BYTES = BN * BK / 2;
+  static constexpr int SFB_BYTES = NB * 4 * SF_ATOM;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFB_BYTES;
+  static constexpr int BAND_BYTES = MAX_KSTEPS * SF_ATOM;    // A-side scales of one band
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAND_BYTES + 1024 + 256;
+  static constexpr int SFA_BASE = BN;                        // 4 columns per K step
+  static constexpr int SFB_BASE = SFA_BASE + 4 * MAX_KSTEPS; // 4 K steps x 8 columns per stage
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+  static_assert(SFB_BASE + STAGES * 4 * 4 * NB <= TMEM_COLS, "tensor memory");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+__global__ void __launch_bounds__(RCfg::THREADS, 1)
+    k_gemm_nvfp4_r(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
+                   const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
+                   int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
+                   void* ws) {
+  using C = RCfg;
+  constexpr int S = C::STAGES, BN = C::BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* band = smem + S * C::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(band + C::BAND_BYTES);
+  // bars: full[S], empty[S], acc_full, acc_empty, band_full, band_empty, mma_done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t sbase = smem_u32(smem), band_s = smem_u32(band);
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + S + s); };
+  const uint32_t afull = smem_u32(bars + 2 * S), aempty = smem_u32(bars + 2 * S + 1);
+  const uint32_t bfull = smem_u32(bars + 2 * S + 2), bempty = smem_u32(bars + 2 * S + 3);
+  const uint32_t mma_done = smem_u32(bars + 2 * S + 4);
+  auto a_tile = [&](int s) { return sbase + s * C::STAGE_BYTES; };
+  auto b_tile = [&](int s) { return a_tile(s) + A_BYTES; };
+  auto sfb_tile = [&](int s) { return b_tile(s) + C::B_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ksteps = K / KSTEP;
+  const int num_kb = (ksteps + 3) / 4;
+  const int k_atoms = ksteps;
+  const int n_tiles_n = (N + BN - 1) / BN;
+  const int n_tiles = ((M + BM - 1) / BM) * n_tiles_n;
+  const int per = (n_tiles + gridDim.x - 1) / gridDim.x;
+  const int t_begin = blockIdx.x * per;
+  const int t_end = min(n_tiles, t_begin + per);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(afull, 1);
+    mbar_init(aempty, C::EPI_WARPS);
+    mbar_init(bfull, 1);
+    mbar_init(bempty, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {  // -------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      uint32_t kc = 0, bc = 0;
+      int cur_band = -1;
+      bool ok = true;
+      for (int tile = t_begin; tile < t_end && ok; ++tile) {
+        const int mb = tile / n_tiles_n;
+        const int m0 = mb * BM, n0 = (tile % n_tiles_n) * BN;
+        if (mb != cur_band) {  // A-side scales of the new band, all K steps, one bulk copy
+          if (!mbar_wait(bempty, (bc & 1) ^ 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bfull, k_atoms * SF_ATOM);
+          bulk_load(band_s, a_sf + (size_t)mb * k_atoms * SF_ATOM, k_atoms * SF_ATOM, bfull);
+          cur_band = mb;
+          ++bc;
+        }
+        int nb_valid = (N - n0 + 127) / 128;
+        if (nb_valid > C::NB) nb_valid = C::NB;
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int nsub = min(4, ksteps - kb * 4);
+          mbar_expect_tx(full(s), A_BYTES + C::B_BYTES + nsub * SF_ATOM * nb_valid);
+          tma_load_2d(a_tile(s), &tmA, full(s), kb * (BK / 2), m0);
+          tma_load_2d(b_tile(s), &tmB, full(s), kb * (BK / 2), n0);
+          for (int nb = 0; nb < nb_valid; ++nb)
+            bulk_load(sfb_tile(s) + nb * 4 * SF_ATOM, b_sf + ((size_t)(n0 / 128 + nb) * k_atoms + kb * 4) * SF_ATOM,
+                      nsub * SF_ATOM, full(s));
+        }
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        const uint32_t first = kc > (uint32_t)S ? kc - S : 0;
+        for (uint32_t c = first; c < kc; ++c) mbar_wait(full(c % S), (c / S) & 1, ws, &no_abort);
+        if (bc > 0) mbar_wait(bfull, (bc - 1) & 1, ws, &no_abort);
+      }
+    }
+  } else if (warp == 1) {  // ------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_nvf4(BM, BN);
+      uint32_t kc = 0, bc = 0, tc = 0;
+      int cur_band = -1;
+      bool ok = true;
+      volatile int no_abort = 0;
+      for (int tile = t_begin; tile < t_end && ok; ++tile, ++tc) {
+        const int mb = tile / n_tiles_n;
+        const int n0 = (tile % n_tiles_n) * BN;
+        if (mb != cur_band) {
+          if (cur_band >= 0) {  // every MMA reading the old band's scales has finished
+            tc_commit(mma_done);
+            mbar_wait(mma_done, (bc - 1) & 1, ws, &no_abort);
+          }
+          if (!mbar_wait(bfull, bc & 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int a = 0; a < k_atoms; ++a)
+            tc_cp_sf(tmem + C::SFA_BASE + 4 * a, desc_sf(band_s + a * SF_ATOM));
+          tc_commit(bempty);  // the band buffer may be refilled once these copies are done
+          cur_band = mb;
+          ++bc;
+        }
+        int nb_valid = (N - n0 + 127) / 128;
+        if (nb_valid > C::NB) nb_valid = C::NB;
+        if (!mbar_wait(aempty, (tc & 1) ^ 1, ws, abort_flag)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait(full(s), (kc / S) & 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nsub = min(4, ksteps - kb * 4);
+          for (int j = 0; j < nsub; ++j) {
+            const uint32_t sfb_col = C::SFB_BASE + (s * 4 + j) * 4 * C::NB;
+            for (int nb = 0; nb < nb_valid; ++nb)
+              tc_cp_sf(tmem + sfb_col + 4 * nb, desc_sf(sfb_tile(s) + nb * 4 * SF_ATOM + j * SF_ATOM));
+            tc_mma(tmem, desc_sw128(a_tile(s) + j * 32), desc_sw128(b_tile(s) + j * 32), idesc,
+                   tmem + C::SFA_BASE + 4 * (kb * 4 + j), tmem + sfb_col, (kb | j) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty(s));
+        }
+        if (ok) tc_commit(afull);
+      }
+      tc_commit(mma_done);
+      mbar_wait(mma_done, bc > 0 ? ((bc - 1) & 1) ^ 0 : 0, ws, &no_abort);
+    }
+    __syncwarp();
+  } else {  // ----------------------------------------------------- epilogue warps
+    const int e = warp - 2;
+    const int q = warp & 3;
+    const int half = e >> 2;
+    const float alpha = __fmul_rn(*a_gs, *b_gs);
+    uint32_t tc = 0;
+    for (int tile = t_begin; tile < t_end; ++tile, ++tc) {
+      const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
+      if (!mbar_wait(afull, tc & 1, ws, abort_flag)) break;
+      tc_fence_after();
+      const int row = m0 + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + half * 128 + c * 32, r);
+        const int col0 = n0 + half * 128 + c * 32;
+        if (row >= M || col0 >= N) continue;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
+          if (bias) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
+        }
+        const int64_t off = (int64_t)row * N + col0;
+        if (col0 + 32 <= N && (N % 16) == 0) {
+          if (y_bf16) {
+            U8x32 o0, o1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              o0.w[i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
+              o1.w[i] = f2_to_bf16x2(v[16 + 2 * i], v[16 + 2 * i + 1]);
+            }
+            uint16_t* yp = reinterpret_cast<uint16_t*>(y) + off;
+            st256(yp, o0);
+            st256(yp + 16, o1);
+          } else {
+            float* yp = reinterpret_cast<float*>(y) + off;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              U8x32 o;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o.w[i] = __float_as_uint(v[8 * b + i]);
+              st256(yp + 8 * b, o);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (col0 + i >= N) continue;
+            if (y_bf16)
+              reinterpret_cast<__nv_bfloat16*>(y)[off + i] = __float2bfloat16_rn(v[i]);
+            else
+              reinterpret_cast<float*>(y)[off + i] = v[i];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(aempty);
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+static dit_status launch_r(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf, const uint8_t* b_sf,
+                           const float* a_gs, const float* b_gs, int M, int N, int K, const float* bias, void* y,
+                           int y_bf16, void* ws, cudaStream_t st) {
+  using C = RCfg;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(k_gemm_nvfp4_r, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
+      return DIT_ERR_CUDA;
+    attr_done = true;
+  }
+  const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + C::BN - 1) / C::BN);
+  int64_t grid = num_sms();
+  if (grid > tiles) grid = tiles;
+  k_gemm_nvfp4_r<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias,
+                                                                    y, y_bf16, ws);
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
+template <int BN, int STAGES, int ACC_BUFS, int CTAS_PER_SM = 1>
+static dit_status launch_p(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf,
+                           const uint8_t* b_sf, const float* a_gs, const float* b_gs, int M, int N,
+                           int K, const float* bias, void* y, int y_bf16, void* ws, cudaStream_t st) {
+  using C = PCfg<BN, STAGES, ACC_BUFS>;
+  static bool attr_done = false;
+  auto kern = k_gemm_nvfp4_p<BN, STAGES, ACC_BUFS>;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+      return DIT_ERR_CUDA;
+    attr_done = true;
+  }
+  const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  int64_t grid = (int64_t)num_sms() * CTAS_PER_SM;
+  if (grid > tiles) grid = tiles;
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y,
+                                                         y_bf16, ws);
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
 template <int BN, int STAGES, bool SPLIT_N>
 static dit_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf,
                          const uint8_t* b_sf, const float* a_gs, const float* b_gs, int M, int N,
@@ -304,9 +824,13 @@ static dit_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const uin
 using namespace dit6;
 
 // Tile configuration, selectable for experiments through DIT6_NVFP4_TILE (0 = default).
+// Tile configuration.  The default (9) is the persistent 128 x 128 kernel with two CTAs per
+// SM: the scale copies into tensor memory serialise within a CTA, and two independent
+// copy/MMA streams per SM hide that best (measured on GB300 across the CogVideoX shapes).
+// DIT6_NVFP4_TILE selects another one for experiments and tests.
 static int nvfp4_tile_cfg() {
   const char* e = getenv("DIT6_NVFP4_TILE");
-  return e ? atoi(e) : 0;
+  return e ? atoi(e) : 9;
 }
 
 extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
@@ -324,7 +848,7 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
       !aligned32(ws))
     return DIT_ERR_ALIGNMENT;
   const int cfg = nvfp4_tile_cfg();
-  const uint32_t bn_box = (cfg == 1 || cfg == 2) ? 256 : 128;
+  const uint32_t bn_box = (cfg == 1 || cfg == 2 || cfg == 5 || cfg == 6 || cfg == 8) ? 256 : 128;
   CUtensorMap ta, tb;
   if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(k / 2),
                       (uint64_t)m, (uint64_t)(k / 2), f4::BK / 2, f4::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -337,6 +861,15 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
     case 1: return f4::launch<256, 3, true>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 2: return f4::launch<256, 3, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 3: return f4::launch<128, 6, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
-    default: return f4::launch<128, 3, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 4: return f4::launch_p<128, 4, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 5: return f4::launch_p<256, 3, 1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 6: return f4::launch_p<256, 4, 1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 7: return f4::launch_p<128, 6, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 8:
+      if (k <= 64 * f4::RCfg::MAX_KSTEPS)
+        return f4::launch_r(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+      return f4::launch_p<256, 4, 1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    default: return f4::launch_p<128, 3, 1, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 0: return f4::launch<128, 3, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
   }
 }
