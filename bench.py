@@ -212,6 +212,94 @@ class Workload:
         return u
 
 
+def run_tdc_loop(wl, steps: int = 50, tau: float = 0.05, seed: int = 77):
+    """The full TDC/PDR loop on the same 30 CogVideoX-2B blocks: per denoising step and block,
+    skip (X_out = X_in + cached delta) or compute (four routed linears + delta commit), with
+    the block chain X_in(b+1) = X_out(b).  The synthetic "true" block delta follows
+    Delta_t = Delta_{t-1} (1 + eps), eps ~ N(0, 0.01) elementwise, N(0, 0.5) on jump steps
+    (Bernoulli(1/8) per block-step), Delta_0 ~ N(0, sigma_b), sigma_b ~ U(0.02, 0.15); it is
+    generated on the device between our kernels and is not part of the timed segments."""
+    import torch
+    import int8_mixed_precision_gb300 as dit
+    dev, M = wl.dev, TOKENS
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    gam = torch.zeros(NBLOCKS, dtype=torch.float32, device=dev)
+    sim = torch.zeros(NBLOCKS, dtype=torch.float32, device=dev)
+    blocks = [dit.DeltaCachedBlock(M * HIDDEN, torch.bfloat16, tau, [ALPHA] * 4, [BETA] * 4, [THR] * 4, wl.ws,
+                                   gam[b:b + 1], sim[b:b + 1], dev) for b in range(NBLOCKS)]
+    sig = (torch.rand(NBLOCKS, generator=g, device=dev) * 0.13 + 0.02).tolist()
+    deltas = [torch.randn(M, HIDDEN, generator=g, device=dev) * sig[b] for b in range(NBLOCKS)]
+    x0 = wl.x_in
+    xb = [torch.empty_like(x0), torch.empty_like(x0)]
+    y = wl.y
+    segs, n_skip, n_comp, route_count, launches = [], 0, 0, [0, 0], 0
+    skip_bytes = commit_bytes = 0.0
+    skip_ms = commit_ms = 0.0
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for t in range(steps):
+        x = x0
+        for b, blk in enumerate(blocks):
+            if t > 0:  # advance the true trajectory
+                jump = bool(torch.rand(1, generator=g, device=dev).item() < 1.0 / 8.0)
+                eps = torch.randn(M, HIDDEN, generator=g, device=dev) * (0.5 if jump else 0.01)
+                deltas[b].mul_(1.0 + eps)
+            x_next = xb[1] if x is xb[0] else xb[0]
+            mode = blk.decide()
+            a, z = ev(), ev()
+            if mode == dit.TDC_SKIP:
+                a.record()
+                blk.skip(x, x_next)
+                z.record()
+                segs.append(("skip", a, z))
+                n_skip += 1
+                launches += 1
+            else:
+                routes = blk.routes()
+                lins = wl.blocks[b]["lin"]
+                a.record()
+                for li, (name, k, n) in enumerate(LINEARS):
+                    xin = x if k == HIDDEN else wl.inputs[b % 2]["ffn_down"]
+                    lins[name](xin, routes[li], y[name])
+                    launches += 2 if routes[li] == dit.ROUTE_INT8 else 3
+                    route_count[routes[li]] += 1
+                z.record()
+                segs.append(("linears", a, z))
+                x_next.copy_((x.float() + deltas[b]).to(torch.bfloat16))
+                a2, z2 = ev(), ev()
+                a2.record()
+                blk.commit(x, x_next)
+                z2.record()
+                segs.append(("commit", a2, z2))
+                n_comp += 1
+                launches += 1
+            x = x_next
+        h = torch.stack([gam, sim]).cpu()      # one device-to-host copy per denoising step
+        for b, blk in enumerate(blocks):
+            blk.absorb(float(h[0, b]), float(h[1, b]))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    tot = {"skip": 0.0, "linears": 0.0, "commit": 0.0}
+    for kind, a, z in segs:
+        tot[kind] += a.elapsed_time(z)
+    kernel_ms = sum(tot.values())
+    n_elem = M * HIDDEN
+    total_bits = route_count[1] * 8 + route_count[0] * 4.5
+    return {
+        "workload": "cogvideox_2b_tdc_loop", "denoising_steps": steps, "blocks": NBLOCKS, "tau": tau,
+        "skip_fraction": round(n_skip / (n_skip + n_comp), 4), "computed_block_steps": n_comp,
+        "skipped_block_steps": n_skip, "routes": {"int8": route_count[1], "nvfp4": route_count[0]},
+        "avg_activation_bits": round(total_bits / max(1, sum(route_count)), 3),
+        "kernel_ms_total": round(kernel_ms, 2), "kernel_ms_per_denoising_step": round(kernel_ms / steps, 3),
+        "wall_s_incl_synthetic_delta_generation": round(wall, 2),
+        "tdc_skip_gbs": round(n_skip * n_elem * 6 / (tot["skip"] * 1e-3) / 1e9, 1) if n_skip else None,
+        "tdc_commit_gbs": round(n_comp * n_elem * 8 / (tot["commit"] * 1e-3) / 1e9, 1) if n_comp else None,
+        "gpu_launches": launches,
+    }
+
+
 def int8_ceiling(torch, dev):
     """cuBLASLt INT8 GEMM throughput (torch._int_mm, 8192^3) measured in this run."""
     a = torch.randint(-127, 127, (8192, 8192), device=dev, dtype=torch.int8)
@@ -360,6 +448,8 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": int(wl.launches_per_step() * args.steps),
         "clocks": clk.summary(),
     }
+    if not args.no_tdc_loop:
+        line["tdc_loop"] = run_tdc_loop(wl, steps=args.tdc_steps)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -452,6 +542,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-tdc-loop", action="store_true")
+    ap.add_argument("--tdc-steps", type=int, default=50)
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

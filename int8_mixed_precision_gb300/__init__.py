@@ -246,3 +246,53 @@ class RoutedLinear:
             qgemm_nvfp4(c, self.a4["sf"], self.a4["gs"], w.nvfp4["codes"], w.nvfp4["sf"],
                         w.nvfp4["gs"], y, self.ws, bias=bias, stream=stream)
         return y
+
+
+# ----------------------------------------------------------------------------------------
+# one DiT block under the Temporal Delta Cache with PDR routing (host control, device data)
+# ----------------------------------------------------------------------------------------
+
+
+class DeltaCachedBlock:
+    """Drives one block through denoising steps: skip (X_out = X_in + cached delta) or compute
+    (routed linears + delta commit), with the decision and PDR routing of the C state machine.
+
+    Gamma and the delta similarity come back from the device in bulk: call ``absorb`` with the
+    host copies after the step (``gamma_dev``/``sim_dev`` are slots of caller-owned arrays),
+    so a denoising step needs one device-to-host copy for all blocks.
+    """
+
+    def __init__(self, n_elems: int, dtype, tau: float, alpha, beta, thr, ws, gamma_dev, sim_dev,
+                 device="cuda"):
+        torch = _torch()
+        self.tau, self.alpha, self.beta, self.thr = tau, list(alpha), list(beta), list(thr)
+        self.ws, self.gamma_dev, self.sim_dev = ws, gamma_dev, sim_dev
+        self.d = [torch.empty(n_elems, dtype=dtype, device=device), torch.empty(n_elems, dtype=dtype, device=device)]
+        self.state = TdcState()
+        self.pending = False
+        self.had_delta = False
+
+    def decide(self) -> int:
+        return self.state.decide(self.tau)
+
+    def routes(self) -> list[int]:
+        return self.state.routes(self.alpha, self.beta, self.thr)
+
+    def skip(self, x_in, x_out, stream=None):
+        tdc_step(TDC_SKIP, x_in.reshape(-1), self.ws, x_out_skip=x_out.reshape(-1), d1=self.d[0], stream=stream)
+        self.state.update(TDC_SKIP)
+
+    def commit(self, x_in, x_out, stream=None):
+        tdc_step(TDC_COMMIT, x_in.reshape(-1), self.ws, x_out=x_out.reshape(-1),
+                 d1=self.d[0] if self.had_delta else None, d_new=self.d[1], gamma=self.gamma_dev,
+                 sim=self.sim_dev, stream=stream)
+        self.d.reverse()
+        self.pending = True
+
+    def absorb(self, gamma: float, sim: float) -> None:
+        """Fold a committed step's Gamma and similarity (host values) into the state."""
+        if not self.pending:
+            return
+        self.state.update(TDC_COMMIT, gamma, sim if self.had_delta else None)
+        self.had_delta = True
+        self.pending = False

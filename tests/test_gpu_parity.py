@@ -411,3 +411,44 @@ def test_full_size_cogvideox_2b_sampled(ws):
         refb = F.bf16_bits_to_f32(F.f32_to_bf16_bits(ref.astype(np.float32)))
         assert rel_fro(yh, refb) <= GEMM_TOL
     _status_clean(ws)
+
+
+def test_tdc_chained_blocks_full_size(ws):
+    """Two chained CogVideoX-2B-sized blocks (17776 x 1920 bf16) through 8 denoising steps with
+    DeltaCachedBlock: decisions, PDR routes and every block output identical to the oracle."""
+    rows, k, steps, tau = synth.TOKENS_2B, 1920, 8, 0.05
+    alpha, beta, thr = [1.0] * 4, [0.0] * 4, [0.05] * 4
+    thr64 = np.float32(thr).astype(np.float64)
+    xs = [synth.activations(rows, k, seed=500 + t, outlier_frac=0.0) for t in range(steps)]
+    deltas = [synth.tdc_deltas(steps, rows, k, seed=600 + b, jump_every=4.0)[0] for b in range(2)]
+    ref0 = T.run_block_loop(xs, deltas[0], tau, alpha, beta, thr64)
+    ref1 = T.run_block_loop(ref0["outs"], deltas[1], tau, alpha, beta, thr64)
+    refs = [ref0, ref1]
+    gam = torch.zeros(2, dtype=torch.float32, device="cuda")
+    sim = torch.zeros(2, dtype=torch.float32, device="cuda")
+    blocks = [dit.DeltaCachedBlock(rows * k, torch.bfloat16, tau, alpha, beta, thr, ws, gam[b:b + 1], sim[b:b + 1])
+              for b in range(2)]
+    for t in range(steps):
+        x = dev_bf16(xs[t]).reshape(-1)
+        for b, blk in enumerate(blocks):
+            mode = blk.decide()
+            x_next = torch.empty_like(x)
+            want = refs[b]["decisions"][t]
+            if refs[b]["margins"][t] > 1e-5:
+                assert (mode == dit.TDC_SKIP) == (want == "skip"), (t, b)
+            if mode == dit.TDC_SKIP:
+                blk.skip(x, x_next)
+            else:
+                if refs[b]["routes"][t] is not None:
+                    g_ref = refs[b]["gammas"][t]
+                    if g_ref is None or abs(g_ref - 0.05) > 1e-5 * 0.05:
+                        assert blk.routes() == refs[b]["routes"][t], (t, b)
+                dlt = dev_bf16(deltas[b][t]).reshape(-1)
+                x_next.copy_((x.float() + dlt.float()).to(torch.bfloat16))
+                blk.commit(x, x_next)
+            assert np.array_equal(host(x_next), refs[b]["outs"][t].reshape(-1)), (t, b)
+            x = x_next
+        h = torch.stack([gam, sim]).cpu()
+        for b, blk in enumerate(blocks):
+            blk.absorb(float(h[0, b]), float(h[1, b]))
+    _status_clean(ws)
