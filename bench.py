@@ -300,6 +300,22 @@ def run_tdc_loop(wl, steps: int = 50, tau: float = 0.05, seed: int = 77):
     }
 
 
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """Largest value over all ranks (the step time the job reports); identity at world 1."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / (ms_max * 1e-3) / 1e12
+
+
 def int8_ceiling(torch, dev):
     """cuBLASLt INT8 GEMM throughput (torch._int_mm, 8192^3) measured in this run."""
     a = torch.randint(-127, 127, (8192, 8192), device=dev, dtype=torch.int8)
@@ -355,10 +371,7 @@ def run_ours(args, rank, world, local_rank):
     ms = e0.elapsed_time(e1) / args.steps
     dom_ms = [a.elapsed_time(z) for a, z in wl.timers[dominant]]
     wl.timers = None
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # ---- end to end through the public API: host inputs in, results out ----
     host_in = {}
@@ -392,10 +405,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     if rank != 0:
         return
@@ -427,8 +437,8 @@ def run_ours(args, rank, world, local_rank):
     kern_times = {k: round(v, 3) for k, v in tot.items()}
     hbm = {k: round(units[k] / (tot[k] * 1e-3) / 1e9, 1) for k in ("quant_int8", "quant_nvfp4", "tdc_commit")
            if tot.get(k)}
-    value = wl.flops_step * world / (ms * 1e-3) / 1e12
-    e2e_val = wl.flops_step * world / (e2e_ms * 1e-3) / 1e12
+    value = aggregate_value(wl.flops_step, world, ms)
+    e2e_val = aggregate_value(wl.flops_step, world, e2e_ms)
     routes_flat = [r for rr in wl.routes for r in rr]
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
