@@ -26,14 +26,16 @@ struct Vec;
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int N = 16;
-  static __device__ __forceinline__ void load(const void* p, int64_t i, float (&v)[16]) {
-    U8x32 r = ld256_nc(reinterpret_cast<const char*>(p) + i * 32);
+  static __device__ __forceinline__ void unpack(const U8x32& r, float (&v)[16]) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       float2 f = bf16x2_to_f2(r.w[k]);
       v[2 * k] = f.x;
       v[2 * k + 1] = f.y;
     }
+  }
+  static __device__ __forceinline__ void load(const void* p, int64_t i, float (&v)[16]) {
+    unpack(ld256_nc(reinterpret_cast<const char*>(p) + i * 32), v);
   }
   static __device__ __forceinline__ float scalar(const void* p, int64_t i) {
     return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
@@ -54,10 +56,12 @@ struct Vec<__nv_bfloat16> {
 template <>
 struct Vec<float> {
   static constexpr int N = 8;
-  static __device__ __forceinline__ void load(const void* p, int64_t i, float (&v)[8]) {
-    U8x32 r = ld256_nc(reinterpret_cast<const char*>(p) + i * 32);
+  static __device__ __forceinline__ void unpack(const U8x32& r, float (&v)[8]) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(r.w[k]);
+  }
+  static __device__ __forceinline__ void load(const void* p, int64_t i, float (&v)[8]) {
+    unpack(ld256_nc(reinterpret_cast<const char*>(p) + i * 32), v);
   }
   static __device__ __forceinline__ float scalar(const void* p, int64_t i) {
     return reinterpret_cast<const float*>(p)[i];
@@ -138,10 +142,31 @@ __global__ void __launch_bounds__(RED_THREADS) k_gamma_route(const void* __restr
                                                              float* gamma_out,
                                                              int32_t* routes, void* ws) {
   constexpr int N = Vec<T>::N;
+  constexpr int U = 4;  // vectors in flight per thread
   const int64_t nv = n / N;
   float s[2] = {0.f, 0.f};
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + (U - 1) * stride < nv; i += U * stride) {
+    U8x32 ra[U], rb[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      ra[u] = ld256_nc(reinterpret_cast<const char*>(xi) + (i + u * stride) * 32);
+      rb[u] = ld256_nc(reinterpret_cast<const char*>(xo) + (i + u * stride) * 32);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float a[N], b[N];
+      Vec<T>::unpack(ra[u], a);
+      Vec<T>::unpack(rb[u], b);
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        s[0] += fabsf(__fsub_rn(b[k], a[k]));
+        s[1] += fabsf(a[k]);
+      }
+    }
+  }
+  for (; i < nv; i += stride) {
     float a[N], b[N];
     Vec<T>::load(xi, i, a);
     Vec<T>::load(xo, i, b);
@@ -178,7 +203,36 @@ __global__ void __launch_bounds__(RED_THREADS) k_tdc_commit(const void* __restri
   const int64_t nv = n / N;
   float s[4] = {0.f, 0.f, 0.f, 0.f};
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+  int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i0 + stride < nv; i0 += 2 * stride) {  // two vectors in flight per thread
+    U8x32 ra[2], rb[2], rc[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      ra[u] = ld256_nc(reinterpret_cast<const char*>(xi) + (i0 + u * stride) * 32);
+      rb[u] = ld256_nc(reinterpret_cast<const char*>(xo) + (i0 + u * stride) * 32);
+      if (d1) rc[u] = ld256_nc(reinterpret_cast<const char*>(d1) + (i0 + u * stride) * 32);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float a[N], b[N], c[N], dl[N];
+      Vec<T>::unpack(ra[u], a);
+      Vec<T>::unpack(rb[u], b);
+      if (d1) Vec<T>::unpack(rc[u], c);
+#pragma unroll
+      for (int k = 0; k < N; ++k) {
+        const float df = __fsub_rn(b[k], a[k]);
+        dl[k] = Vec<T>::round_store(df);
+        s[0] += fabsf(df);
+        s[1] += fabsf(a[k]);
+        if (d1) {
+          s[2] += fabsf(__fsub_rn(dl[k], c[k]));
+          s[3] += fabsf(c[k]);
+        }
+      }
+      Vec<T>::store(dnew, i0 + u * stride, dl);
+    }
+  }
+  for (int64_t i = i0; i < nv; i += stride) {
     float a[N], b[N], c[N], dl[N];
     Vec<T>::load(xi, i, a);
     Vec<T>::load(xo, i, b);
@@ -223,7 +277,25 @@ __global__ void __launch_bounds__(RED_THREADS) k_tdc_skip(const void* __restrict
   constexpr int N = Vec<T>::N;
   const int64_t nv = n / N;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+  int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i0 + stride < nv; i0 += 2 * stride) {  // two vectors in flight per thread
+    U8x32 ra[2], rc[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      ra[u] = ld256_nc(reinterpret_cast<const char*>(xi) + (i0 + u * stride) * 32);
+      rc[u] = ld256_nc(reinterpret_cast<const char*>(d1) + (i0 + u * stride) * 32);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float a[N], c[N];
+      Vec<T>::unpack(ra[u], a);
+      Vec<T>::unpack(rc[u], c);
+#pragma unroll
+      for (int k = 0; k < N; ++k) a[k] = __fadd_rn(a[k], c[k]);
+      Vec<T>::store(out, i0 + u * stride, a);
+    }
+  }
+  for (int64_t i = i0; i < nv; i += stride) {
     float a[N], c[N];
     Vec<T>::load(xi, i, a);
     Vec<T>::load(d1, i, c);

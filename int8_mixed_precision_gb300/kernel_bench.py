@@ -1,4 +1,4 @@
-"""Time one libdit6 kernel on one shape (CUDA events, L2 flushed between repetitions).
+"""Time one libdit6 kernel on one shape (CUDA events, L2 cleaned between repetitions).
 
   python -m int8_mixed_precision_gb300.kernel_bench --case gemm_nvfp4 --m 17776 --n 5760 --k 1920
 
@@ -90,14 +90,17 @@ def main(argv=None):
     else:
         raise SystemExit(f"unknown case {case}")
 
-    flush = None if a.no_flush else torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    # L2 flush between repetitions: a read sweep over a buffer larger than L2, so that the
+    # timed kernel starts with neither its inputs nor dirty lines (whose write-back would
+    # otherwise be charged to it) in L2
+    flush = None if a.no_flush else torch.ones(640 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     for _ in range(a.warmup):
         fn()
     torch.cuda.synchronize()
     times = []
     for _ in range(a.reps):
         if flush is not None:
-            flush.zero_()
+            flush.max()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn()
