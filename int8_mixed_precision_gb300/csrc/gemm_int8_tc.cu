@@ -85,7 +85,35 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-template <int BN>
+// TMA load of a box multicast into the same shared-memory offset of every CTA in `mask`
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                               int32_t c1, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+      "[%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
+      : "memory");
+}
+// MMA completion arrives on the barrier at the same offset in every CTA of `mask`
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// MC = 1: independent CTAs.  MC = 2: clusters of two CTAs on adjacent 128-row M blocks and the
+// same N block; each loads half of the shared B tile and multicasts it to both, halving the
+// B traffic from L2; a stage is refilled only after both CTAs' MMAs have consumed it.
+template <int BN, int MC>
 __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     k_gemm_int8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N,
@@ -108,14 +136,20 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles_n = (N + BN - 1) / BN;
-  const int n_tiles = ((M + BM - 1) / BM) * n_tiles_n;
+  const int m_groups = ((M + BM - 1) / BM + MC - 1) / MC;     // groups of MC adjacent M blocks
+  const int n_tiles = m_groups * n_tiles_n;                    // work items (one per CTA group)
+  const int rank = MC > 1 ? (int)cluster_rank() : 0;
+  const int first_item = blockIdx.x / MC, item_step = gridDim.x / MC;
+  auto tile_m0 = [&](int item) { return ((item / n_tiles_n) * MC + rank) * BM; };
+  auto tile_n0 = [&](int item) { return (item % n_tiles_n) * BN; };
   const int nkb = (K + BK - 1) / BK;
   const int nchunks = (nkb + KCHUNK_BLOCKS - 1) / KCHUNK_BLOCKS;
+  constexpr uint16_t PEERS = MC > 1 ? (uint16_t)((1u << MC) - 1) : (uint16_t)1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 1);
+      mbar_init(empty(s), MC);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(cfull(b), 1);
@@ -133,6 +167,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     tc_fence_before();
   }
   __syncthreads();
+  if (MC > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -142,8 +177,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
       prefetch_tmap(&tmB);
       uint32_t kc = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
+      for (int item = first_item; item < n_tiles && ok; item += item_step) {
+        const int m0 = tile_m0(item), n0 = tile_n0(item);
         for (int kb = 0; kb < nkb; ++kb, ++kc) {
           const int s = kc % S;
           if (!mbar_wait(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
@@ -152,7 +187,11 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
           }
           mbar_expect_tx(full(s), C::STAGE_BYTES);
           tma_load_2d(sbase + s * C::STAGE_BYTES, &tmA, full(s), kb * BK, m0);
-          tma_load_2d(sbase + s * C::STAGE_BYTES + A_BYTES, &tmB, full(s), kb * BK, n0);
+          if (MC > 1)
+            tma_load_2d_mc(sbase + s * C::STAGE_BYTES + A_BYTES + rank * (C::B_BYTES / MC), &tmB, full(s), kb * BK,
+                           n0 + rank * (BN / MC), PEERS);
+          else
+            tma_load_2d(sbase + s * C::STAGE_BYTES + A_BYTES, &tmB, full(s), kb * BK, n0);
         }
       }
       if (!ok) {  // let copies still in flight land before the CTA exits
@@ -166,7 +205,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
       constexpr uint32_t idesc = idesc_bf16(BM, BN);
       uint32_t kc = 0, cc = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      for (int item = first_item; item < n_tiles && ok; item += item_step) {
         for (int ch = 0; ch < nchunks && ok; ++ch, ++cc) {
           const int buf = cc & 1;
           if (!mbar_wait(cempty(buf), ((cc >> 1) & 1) ^ 1, ws, abort_flag)) {
@@ -189,7 +228,10 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             for (int j = 0; j < BK / 16; ++j)
               tc_mma(d, desc_sw128(a_s + j * 32), desc_sw128(b_s + j * 32), idesc,
                      (kb > kb0 || j > 0) ? 1u : 0u);
-            tc_commit(empty(s));
+            if (MC > 1)
+              tc_commit_mc(empty(s), PEERS);
+            else
+              tc_commit(empty(s));
           }
           if (ok) tc_commit(cfull(buf));
         }
@@ -205,8 +247,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     const int half = e >> 2;       // which CW-column part of the tile
     uint32_t cc = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
+    for (int item = first_item; item < n_tiles && ok; item += item_step) {
+      const int m0 = tile_m0(item), n0 = tile_n0(item);
       constexpr int CW = C::CW;
       int acc[CW];
 #pragma unroll
@@ -297,9 +339,10 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
                  : "memory");
   }
+  if (MC > 1) cluster_sync();  // no peer may still multicast into, or arrive on, this CTA
 }
 
-template <int BN>
+template <int BN, int MC>
 dit_status launch(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
                   int64_t n, int64_t k, const float* bias, void* y, int y_bf16, int32_t* acc_out,
                   void* ws, cudaStream_t st) {
@@ -308,21 +351,41 @@ dit_status launch(const void* a, const float* a_scale, const void* b, const floa
   if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(a), (uint64_t)k, (uint64_t)m,
                       (uint64_t)k * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(b), (uint64_t)k, (uint64_t)n,
-                      (uint64_t)k * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                      (uint64_t)k * 2, BK, BN / MC, CU_TENSOR_MAP_SWIZZLE_128B))
     return DIT_ERR_CUDA;
+  auto kern = k_gemm_int8_tc<BN, MC>;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(k_gemm_int8_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+      return DIT_ERR_CUDA;
+    if (MC > 1 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
       return DIT_ERR_CUDA;
     attr_done = true;
   }
-  const int64_t tiles = ((m + BM - 1) / BM) * ((n + BN - 1) / BN);
+  const int64_t items = (((m + BM - 1) / BM + MC - 1) / MC) * ((n + BN - 1) / BN);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
   int64_t grid = num_sms();
-  if (grid > tiles) grid = tiles;
-  k_gemm_int8_tc<BN><<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(
-      ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, y_bf16, acc_out, ws);
-  DIT_CHECK_LAUNCH();
+  if (MC > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = MC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)(grid / MC * MC));
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return DIT_ERR_CUDA;
+    grid = (int64_t)clusters * MC;
+  }
+  if (grid > items * MC) grid = items * MC;
+  cfg.gridDim = dim3((unsigned)grid);
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, y_bf16, acc_out,
+                         ws) != cudaSuccess)
+    return DIT_ERR_CUDA;
   return DIT_OK;
 }
 
@@ -332,10 +395,13 @@ dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, cons
                         int64_t n, int64_t k, const float* bias, void* y, int y_bf16, int32_t* acc_out,
                         void* ws, cudaStream_t st) {
   const char* e = getenv("DIT6_INT8_TC_BN");
+  const char* c = getenv("DIT6_INT8_TC_CLUSTER");
   const int bn = e ? atoi(e) : 256;
-  if (bn == 128) return i8tc::launch<128>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
-  if (bn == 256) return i8tc::launch<256>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
-  return i8tc::launch<192>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
+  const int mc = c ? atoi(c) : 1;
+  if (bn == 128) return i8tc::launch<128, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
+  if (bn == 192) return i8tc::launch<192, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
+  if (mc == 2) return i8tc::launch<256, 2>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
+  return i8tc::launch<256, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
 }
 
 }  // namespace dit6

@@ -251,12 +251,13 @@ def _int8_dev(a, container):
 
 
 @pytest.mark.parametrize("container,bn", [(torch.int8, None), (torch.bfloat16, "192"), (torch.bfloat16, "128"),
-                                          (torch.bfloat16, "256")])
+                                          (torch.bfloat16, "256"), (torch.bfloat16, "256c2")])
 @pytest.mark.parametrize("m,n,k", [(256, 512, 128), (300, 384, 1920), (129, 256, 7680), (1, 8, 16),
                                    (200, 136, 208), (700, 5760 // 10, 2112)])
 def test_int8_gemm_exact_accumulators(m, n, k, container, bn, ws, monkeypatch):
     if bn:
-        monkeypatch.setenv("DIT6_INT8_TC_BN", bn)
+        monkeypatch.setenv("DIT6_INT8_TC_BN", bn[:3])
+        monkeypatch.setenv("DIT6_INT8_TC_CLUSTER", "2" if bn.endswith("c2") else "1")
     g = synth.rng(m * n + k)
     a = g.integers(-127, 128, (m, k)).astype(np.int8)
     b = g.integers(-127, 128, (n, k)).astype(np.int8)
@@ -292,8 +293,10 @@ def _adversarial_int8(m, n, k, seed):
     return a, b
 
 
+@pytest.mark.parametrize("cluster", ["1", "2"])
 @pytest.mark.parametrize("k", [1024, 1040, 2048, 7680, 12288])
-def test_int8_gemm_bf16_pipe_exact_at_the_bound(k, ws):
+def test_int8_gemm_bf16_pipe_exact_at_the_bound(k, cluster, ws, monkeypatch):
+    monkeypatch.setenv("DIT6_INT8_TC_CLUSTER", cluster)
     """Extreme codes (+-127 everywhere, totals up to 12288 * 127^2 ~ 2^27.6): the chunked fp32
     accumulation on the bf16 tensor pipe still gives the exact int32 accumulators."""
     m, n = 200, 392
