@@ -776,6 +776,283 @@ static dit_status launch_r(const CUtensorMap& ta, const CUtensorMap& tb, const u
   return DIT_OK;
 }
 
+// ---------------------------------------------------------------------------------------
+// Scale-writer variant: four extra warps move each stage's scale atoms from shared memory into
+// tensor memory with tcgen05.st (each warp writes its own lane quarter, reproducing exactly
+// the layout the 32x128b.warpx4 copy would produce), instead of tcgen05.cp on the tensor-core
+// unit.  The MMA thread waits on a per-stage "scales ready" barrier.
+// ---------------------------------------------------------------------------------------
+template <int BN, int STAGES, int CTAS>
+struct SCfg {
+  static constexpr int NB = BN / 128;
+  static constexpr int B_BYTES = BN * BK / 2;
+  static constexpr int SFA_BYTES = 4 * SF_ATOM;
+  static constexpr int SFB_BYTES = NB * 4 * SF_ATOM;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int SF_COLS = 4 + 4 * NB;
+  static constexpr int SF_BASE = BN;
+  static constexpr int TMEM_USED = SF_BASE + STAGES * 4 * SF_COLS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+  static constexpr int EPI_WARPS = BN / 32;
+  static constexpr int SF_WARP0 = 2 + EPI_WARPS;
+  static constexpr int THREADS = (2 + EPI_WARPS + 4) * 32;
+  static_assert(TMEM_USED <= 512 / CTAS, "tensor memory");
+  static_assert(SMEM_BYTES * CTAS <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ void tc_st4(uint32_t taddr, const uint4& v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+template <int BN, int STAGES, int CTAS>
+__global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
+    k_gemm_nvfp4_s(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
+                   const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
+                   int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
+                   void* ws) {
+  using C = SCfg<BN, STAGES, CTAS>;
+  constexpr int S = STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
+  // bars: full[S], empty[S], sf_ready[S], acc_full, acc_empty, mma_done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t sbase = smem_u32(smem);
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + S + s); };
+  auto sf_ready = [&](int s) { return smem_u32(bars + 2 * S + s); };
+  const uint32_t afull = smem_u32(bars + 3 * S), aempty = smem_u32(bars + 3 * S + 1);
+  const uint32_t mma_done = smem_u32(bars + 3 * S + 2);
+  auto a_tile = [&](int s) { return sbase + s * C::STAGE_BYTES; };
+  auto b_tile = [&](int s) { return a_tile(s) + A_BYTES; };
+  auto sfa_tile = [&](int s) { return smem + s * C::STAGE_BYTES + A_BYTES + C::B_BYTES; };
+  auto sfb_tile = [&](int s) { return sfa_tile(s) + C::SFA_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ksteps = K / KSTEP;
+  const int num_kb = (ksteps + 3) / 4;
+  const int k_atoms = K / KSTEP;
+  const int n_tiles_n = (N + BN - 1) / BN;
+  const int n_tiles = ((M + BM - 1) / BM) * n_tiles_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+      mbar_init(sf_ready(s), 4);
+    }
+    mbar_init(afull, 1);
+    mbar_init(aempty, C::EPI_WARPS);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {  // -------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      uint32_t kc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
+        int nb_valid = (N - n0 + 127) / 128;
+        if (nb_valid > C::NB) nb_valid = C::NB;
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int nsub = min(4, ksteps - kb * 4);
+          mbar_expect_tx(full(s), A_BYTES + C::B_BYTES + nsub * SF_ATOM * (1 + nb_valid));
+          tma_load_2d(a_tile(s), &tmA, full(s), kb * (BK / 2), m0);
+          tma_load_2d(b_tile(s), &tmB, full(s), kb * (BK / 2), n0);
+          bulk_load(smem_u32(sfa_tile(s)), a_sf + ((size_t)(m0 / 128) * k_atoms + kb * 4) * SF_ATOM,
+                    nsub * SF_ATOM, full(s));
+          for (int nb = 0; nb < nb_valid; ++nb)
+            bulk_load(smem_u32(sfb_tile(s)) + nb * 4 * SF_ATOM,
+                      b_sf + ((size_t)(n0 / 128 + nb) * k_atoms + kb * 4) * SF_ATOM, nsub * SF_ATOM, full(s));
+        }
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        const uint32_t first = kc > (uint32_t)S ? kc - S : 0;
+        for (uint32_t c = first; c < kc; ++c) mbar_wait(full(c % S), (c / S) & 1, ws, &no_abort);
+      }
+    }
+  } else if (warp == 1) {  // ------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_nvf4(BM, BN);
+      uint32_t kc = 0, tc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
+        if (!mbar_wait(aempty, (tc & 1) ^ 1, ws, abort_flag)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait(full(s), (kc / S) & 1, ws, abort_flag) ||
+              !mbar_wait(sf_ready(s), (kc / S) & 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nsub = min(4, ksteps - kb * 4);
+          for (int j = 0; j < nsub; ++j) {
+            const uint32_t sfa_col = C::SF_BASE + (s * 4 + j) * C::SF_COLS;
+            tc_mma(tmem, desc_sw128(a_tile(s) + j * 32), desc_sw128(b_tile(s) + j * 32), idesc,
+                   tmem + sfa_col, tmem + sfa_col + 4, (kb | j) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty(s));
+        }
+        if (ok) tc_commit(afull);
+      }
+      tc_commit(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait(mma_done, 0, ws, &no_abort);
+    }
+    __syncwarp();
+  } else if (warp >= C::SF_WARP0) {  // ------------------------------- scale writers
+    const int q = warp & 3;  // the lane quarter this warp may write
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    uint32_t kc = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      const int n0 = (tile % n_tiles_n) * BN;
+      int nb_valid = (N - n0 + 127) / 128;
+      if (nb_valid > C::NB) nb_valid = C::NB;
+      for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+        const int s = kc % S;
+        if (!mbar_wait(full(s), (kc / S) & 1, ws, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int nsub = min(4, ksteps - kb * 4);
+        // lane l gets the 16-byte line l of each 512-byte atom: the four scale words of
+        // rows l, l+32, l+64, l+96 -- the same words the warpx4 copy puts in every quarter
+        for (int j = 0; j < nsub; ++j) {
+          const uint32_t sfa_col = C::SF_BASE + (s * 4 + j) * C::SF_COLS;
+          const uint4 va = *reinterpret_cast<const uint4*>(sfa_tile(s) + j * SF_ATOM + lane * 16);
+          tc_st4(lane_base + sfa_col, va);
+          for (int nb = 0; nb < nb_valid; ++nb) {
+            const uint4 vb =
+                *reinterpret_cast<const uint4*>(sfb_tile(s) + nb * 4 * SF_ATOM + j * SF_ATOM + lane * 16);
+            tc_st4(lane_base + sfa_col + 4 + 4 * nb, vb);
+          }
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sf_ready(s));
+      }
+    }
+  } else {  // ----------------------------------------------------- epilogue warps
+    const int e = warp - 2;
+    const int q = warp & 3;
+    const int half = e >> 2;
+    const float alpha = __fmul_rn(*a_gs, *b_gs);
+    uint32_t tc = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tc) {
+      const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
+      if (!mbar_wait(afull, tc & 1, ws, abort_flag)) break;
+      tc_fence_after();
+      const int row = m0 + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + half * 128 + c * 32, r);
+        const int col0 = n0 + half * 128 + c * 32;
+        if (row >= M || col0 >= N) continue;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
+          if (bias) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
+        }
+        const int64_t off = (int64_t)row * N + col0;
+        if (col0 + 32 <= N && (N % 16) == 0) {
+          if (y_bf16) {
+            U8x32 o0, o1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              o0.w[i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
+              o1.w[i] = f2_to_bf16x2(v[16 + 2 * i], v[16 + 2 * i + 1]);
+            }
+            uint16_t* yp = reinterpret_cast<uint16_t*>(y) + off;
+            st256(yp, o0);
+            st256(yp + 16, o1);
+          } else {
+            float* yp = reinterpret_cast<float*>(y) + off;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              U8x32 o;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o.w[i] = __float_as_uint(v[8 * b + i]);
+              st256(yp + 8 * b, o);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (col0 + i >= N) continue;
+            if (y_bf16)
+              reinterpret_cast<__nv_bfloat16*>(y)[off + i] = __float2bfloat16_rn(v[i]);
+            else
+              reinterpret_cast<float*>(y)[off + i] = v[i];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(aempty);
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+template <int BN, int STAGES, int CTAS>
+static dit_status launch_s(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf, const uint8_t* b_sf,
+                           const float* a_gs, const float* b_gs, int M, int N, int K, const float* bias, void* y,
+                           int y_bf16, void* ws, cudaStream_t st) {
+  using C = SCfg<BN, STAGES, CTAS>;
+  static bool attr_done = false;
+  auto kern = k_gemm_nvfp4_s<BN, STAGES, CTAS>;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+      return DIT_ERR_CUDA;
+    attr_done = true;
+  }
+  const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  int64_t grid = (int64_t)num_sms() * CTAS;
+  if (grid > tiles) grid = tiles;
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y,
+                                                         y_bf16, ws);
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
 template <int BN, int STAGES, int ACC_BUFS, int CTAS_PER_SM = 1>
 static dit_status launch_p(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf,
                            const uint8_t* b_sf, const float* a_gs, const float* b_gs, int M, int N,
@@ -824,13 +1101,14 @@ static dit_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const uin
 using namespace dit6;
 
 // Tile configuration, selectable for experiments through DIT6_NVFP4_TILE (0 = default).
-// Tile configuration.  The default (9) is the persistent 128 x 128 kernel with two CTAs per
-// SM: the scale copies into tensor memory serialise within a CTA, and two independent
-// copy/MMA streams per SM hide that best (measured on GB300 across the CogVideoX shapes).
-// DIT6_NVFP4_TILE selects another one for experiments and tests.
+// Tile configuration.  The default (10) is the persistent 128 x 128 kernel with two CTAs per
+// SM whose scale atoms are written into tensor memory by four dedicated warps (tcgen05.st):
+// scale copies on the tensor-core unit (tcgen05.cp) serialise with the MMAs, and two
+// independent MMA streams per SM hide the pipeline latency best (measured on GB300 across the
+// CogVideoX shapes).  DIT6_NVFP4_TILE selects another one for experiments and tests.
 static int nvfp4_tile_cfg() {
   const char* e = getenv("DIT6_NVFP4_TILE");
-  return e ? atoi(e) : 9;
+  return e ? atoi(e) : 10;
 }
 
 extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
@@ -848,7 +1126,7 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
       !aligned32(ws))
     return DIT_ERR_ALIGNMENT;
   const int cfg = nvfp4_tile_cfg();
-  const uint32_t bn_box = (cfg == 1 || cfg == 2 || cfg == 5 || cfg == 6 || cfg == 8) ? 256 : 128;
+  const uint32_t bn_box = (cfg == 1 || cfg == 2 || cfg == 5 || cfg == 6 || cfg == 8 || cfg == 11) ? 256 : 128;
   CUtensorMap ta, tb;
   if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(k / 2),
                       (uint64_t)m, (uint64_t)(k / 2), f4::BK / 2, f4::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -869,7 +1147,10 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
       if (k <= 64 * f4::RCfg::MAX_KSTEPS)
         return f4::launch_r(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
       return f4::launch_p<256, 4, 1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
-    default: return f4::launch_p<128, 3, 1, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 9: return f4::launch_p<128, 3, 1, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    default: return f4::launch_s<128, 3, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 11: return f4::launch_s<256, 4, 1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 12: return f4::launch_s<128, 6, 1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 0: return f4::launch<128, 3, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
   }
 }

@@ -203,36 +203,7 @@ __global__ void __launch_bounds__(RED_THREADS) k_tdc_commit(const void* __restri
   const int64_t nv = n / N;
   float s[4] = {0.f, 0.f, 0.f, 0.f};
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i0 + stride < nv; i0 += 2 * stride) {  // two vectors in flight per thread
-    U8x32 ra[2], rb[2], rc[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      ra[u] = ld256_nc(reinterpret_cast<const char*>(xi) + (i0 + u * stride) * 32);
-      rb[u] = ld256_nc(reinterpret_cast<const char*>(xo) + (i0 + u * stride) * 32);
-      if (d1) rc[u] = ld256_nc(reinterpret_cast<const char*>(d1) + (i0 + u * stride) * 32);
-    }
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      float a[N], b[N], c[N], dl[N];
-      Vec<T>::unpack(ra[u], a);
-      Vec<T>::unpack(rb[u], b);
-      if (d1) Vec<T>::unpack(rc[u], c);
-#pragma unroll
-      for (int k = 0; k < N; ++k) {
-        const float df = __fsub_rn(b[k], a[k]);
-        dl[k] = Vec<T>::round_store(df);
-        s[0] += fabsf(df);
-        s[1] += fabsf(a[k]);
-        if (d1) {
-          s[2] += fabsf(__fsub_rn(dl[k], c[k]));
-          s[3] += fabsf(c[k]);
-        }
-      }
-      Vec<T>::store(dnew, i0 + u * stride, dl);
-    }
-  }
-  for (int64_t i = i0; i < nv; i += stride) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
     float a[N], b[N], c[N], dl[N];
     Vec<T>::load(xi, i, a);
     Vec<T>::load(xo, i, b);
