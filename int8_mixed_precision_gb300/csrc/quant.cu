@@ -56,6 +56,42 @@ __device__ __forceinline__ void load_transform(const void* x, int64_t unit, floa
   for (int p = 0; p < 32; ++p) v[p] = mul2(v[p], c);
 }
 
+// Raw bytes of one unit, fetched ahead of use so the next unit's loads are in flight while
+// the current unit is transformed (software pipelining of the streaming loops).
+template <typename T>
+struct RawUnit {
+  static constexpr int CHUNKS = UNIT * (int)sizeof(T) / 32;
+  U8x32 r[CHUNKS];
+  __device__ __forceinline__ void fetch(const void* base, int64_t unit) {
+    const char* p = reinterpret_cast<const char*>(base) + unit * (UNIT * (int64_t)sizeof(T));
+#pragma unroll
+    for (int c = 0; c < CHUNKS; ++c) r[c] = ld256_nc(p + 32 * c);
+  }
+  __device__ __forceinline__ void unpack(float2 (&v)[32]) const {
+    if (sizeof(T) == 2) {
+#pragma unroll
+      for (int c = 0; c < CHUNKS; ++c)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[c * 8 + i] = bf16x2_to_f2(r[c].w[i]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < CHUNKS; ++c)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          v[c * 4 + i] = make_float2(__uint_as_float(r[c].w[2 * i]), __uint_as_float(r[c].w[2 * i + 1]));
+    }
+  }
+};
+
+template <typename T, int HB>
+__device__ __forceinline__ void transform_raw(const RawUnit<T>& raw, float2 (&v)[32], float inv_sqrt_b) {
+  raw.unpack(v);
+  fwht64<HB>(v);
+  const float2 c = make_float2(inv_sqrt_b, inv_sqrt_b);
+#pragma unroll
+  for (int p = 0; p < 32; ++p) v[p] = mul2(v[p], c);
+}
+
 __device__ __forceinline__ float amax_range(const float2 (&v)[32], int p0, int np) {
   float m = 0.f;
 #pragma unroll
@@ -133,11 +169,17 @@ __global__ void __launch_bounds__(256) k_nvfp4_amax(const void* __restrict__ x, 
   __shared__ float wmax[8];
   __shared__ bool last;
   float m = 0.f;
-  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units;
-       u += (int64_t)gridDim.x * blockDim.x) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  RawUnit<T> cur;
+  if (u < units) cur.fetch(x, u);
+  for (; u < units; u += stride) {
+    RawUnit<T> nxt;
+    if (u + stride < units) nxt.fetch(x, u + stride);
     float2 v[32];
-    load_transform<T, HB>(x, u, v, inv_sqrt_b);
+    transform_raw<T, HB>(cur, v, inv_sqrt_b);
     m = fmaxf(m, amax_range(v, 0, 32));
+    cur = nxt;
   }
   m = warp_max_f(m);
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
@@ -177,8 +219,11 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const void* __restrict__ x,
   const float six_sg = __fmul_rn(6.0f, s_g);
   const int64_t units = rows * upr;
   const int64_t atoms_per_row = upr;  // 4 scale columns per unit == one atom column
-  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < pad_units;
-       u += (int64_t)gridDim.x * blockDim.x) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  RawUnit<T> cur;
+  if (u < units) cur.fetch(x, u);
+  for (; u < pad_units; u += stride) {
     const int64_t row = u / upr;
     const int64_t j = u - row * upr;
     const int64_t ri = row & 127;
@@ -188,8 +233,11 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const void* __restrict__ x,
       *sfw = 0u;
       continue;
     }
+    RawUnit<T> nxt;
+    if (u + stride < units) nxt.fetch(x, u + stride);
     float2 v[32];
-    load_transform<T, HB>(x, u, v, inv_sqrt_b);
+    transform_raw<T, HB>(cur, v, inv_sqrt_b);
+    cur = nxt;
     U8x32 out;
     uint32_t sfword = 0;
 #pragma unroll
@@ -248,14 +296,13 @@ static void launch_nvfp4_t(const void* x, int64_t rows, int upr, float isb, uint
   const float* sgp = ts_in;
   if (!ts_in) {
     int64_t g1 = (units + 255) / 256;
-    if (g1 > 4 * sms) g1 = 4 * sms;
-    if (g1 > MAX_RED_CTAS) g1 = MAX_RED_CTAS;
+    if (g1 > 6 * sms) g1 = 6 * sms;
     if (g1 < 1) g1 = 1;
     k_nvfp4_amax<T, HB><<<(unsigned)g1, 256, 0, st>>>(x, units, isb, ws, ts_out);
     sgp = reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws) + WS_SG);
   }
   int64_t g2 = (pad_units + 255) / 256;
-  if (g2 > 16 * sms) g2 = 16 * sms;
+  if (g2 > 6 * sms) g2 = 6 * sms;
   if (g2 < 1) g2 = 1;
   k_nvfp4_quant<T, HB><<<(unsigned)g2, 256, 0, st>>>(x, rows, upr, pad_units, isb, sgp, codes,
                                                       sf, ts_out, ts_in ? 1 : 0);
