@@ -2,6 +2,7 @@
 // driver entry points, and the delta-cache decision logic of 6Bit-Diffusion
 // ([EN] gist.science 2.B "Error Control", 2.C second bullet).
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -25,6 +26,11 @@ int num_sms() {
 }
 
 bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+int test_stall() {
+  const char* e = getenv("DIT6_TEST_STALL_PRODUCER");
+  return (e && e[0] == '1') ? 1 : 0;
+}
 
 typedef CUresult (*encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                     const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

@@ -249,6 +249,9 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 // ---------------------------------------------------------------------------------------
 namespace dit6 {
 int num_sms();  // SM count of the current device (cached per device)
+// Failure-path test hook: DIT6_TEST_STALL_PRODUCER=1 makes the GEMMs' producer warp issue no
+// loads, so the consumers' bounded waits run out and the kernels report DIT_ERR_TIMEOUT.
+int test_stall();
 bool aligned32(const void* p);
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda needed)
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base, uint64_t inner,

@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     k_gemm_int8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N,
                    int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
-                   int32_t* __restrict__ acc_out, void* ws) {
+                   int32_t* __restrict__ acc_out, void* ws, int stall) {
   using C = Cfg<BN>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {  // ------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && !stall) {  // stall: a test hook that issues no loads at all
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       uint32_t kc = 0;
@@ -384,7 +384,7 @@ dit_status launch(const void* a, const float* a_scale, const void* b, const floa
   if (grid > items * MC) grid = items * MC;
   cfg.gridDim = dim3((unsigned)grid);
   if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, y_bf16, acc_out,
-                         ws) != cudaSuccess)
+                         ws, MC > 1 ? 0 : test_stall()) != cudaSuccess)
     return DIT_ERR_CUDA;
   return DIT_OK;
 }

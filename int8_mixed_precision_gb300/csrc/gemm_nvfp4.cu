@@ -813,7 +813,7 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
                    const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
                    const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
                    int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
-                   void* ws) {
+                   void* ws, int stall) {
   using C = SCfg<BN, STAGES, CTAS>;
   constexpr int S = STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -864,7 +864,7 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {  // -------------------------------------------------- TMA producer
-    if (lane == 0) {
+    if (lane == 0 && !stall) {  // stall: a test hook that issues no loads at all
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       uint32_t kc = 0;
@@ -1048,7 +1048,7 @@ static dit_status launch_s(const CUtensorMap& ta, const CUtensorMap& tb, const u
   int64_t grid = (int64_t)num_sms() * CTAS;
   if (grid > tiles) grid = tiles;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y,
-                                                         y_bf16, ws);
+                                                         y_bf16, ws, test_stall());
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }

@@ -455,3 +455,39 @@ def test_tdc_chained_blocks_full_size(ws):
         for b, blk in enumerate(blocks):
             blk.absorb(float(h[0, b]), float(h[1, b]))
     _status_clean(ws)
+
+
+@pytest.mark.parametrize("route", ["nvfp4", "int8"])
+def test_gemm_bounded_wait_reports_timeout_and_recovers(route, monkeypatch):
+    """A GEMM whose producer issues no loads (test hook): the consumers' bounded waits run out
+    after ~1 s, the kernel records DIT_ERR_TIMEOUT in the workspace status word, frees its
+    tensor memory and exits; the next normal call on the same context is correct."""
+    import time
+    ws2 = dit.workspace()
+    m, n, k = 256, 256, 128
+    g = synth.rng(55)
+    if route == "nvfp4":
+        qa, qb, A, B = _nvfp4_operands(m, n, k, seed=56)
+        ref = D.gemm_nvfp4(qa["codes"], qa["sf"], qa["s_g"], qb["codes"], qb["sf"], qb["s_g"])
+        call = lambda y: dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], y, ws2)
+    else:
+        a = g.integers(-127, 128, (m, k)).astype(np.int8)
+        b = g.integers(-127, 128, (n, k)).astype(np.int8)
+        sa, sb = np.ones(m, np.float32), np.ones(n, np.float32)
+        ref = D.gemm_int8(a, sa, b, sb)
+        ta, tb = _int8_dev(a, torch.bfloat16), _int8_dev(b, torch.bfloat16)
+        call = lambda y: dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws2)
+    y = torch.zeros(m, n, dtype=torch.float32, device="cuda")
+    monkeypatch.setenv("DIT6_TEST_STALL_PRODUCER", "1")
+    t0 = time.time()
+    call(y)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert dit.device_status(ws2) & (1 << 5), "DIT_ERR_TIMEOUT not raised"
+    assert elapsed < 30.0
+    monkeypatch.delenv("DIT6_TEST_STALL_PRODUCER")
+    dit.clear_device_status(ws2)
+    call(y)
+    torch.cuda.synchronize()
+    assert dit.device_status(ws2) == 0
+    assert rel_fro(host(y), ref) <= GEMM_TOL
