@@ -6,7 +6,8 @@ Hadamard block 64, 1% outlier channels x50, 30 blocks whose Gamma ~ U(0, 0.2) ro
 block to INT8 (Gamma > 0.05) or NVFP4.  Synthetic, seeded inputs (no trained weights exist).
 
 One step = one pass over the 30 blocks: for each block its four routed linears (online
-block Hadamard + activation quantisation + quantised GEMM) and the delta-cache commit
+block Hadamard + activation quantisation + quantised GEMM; GELU (erf form) fused into the
+FFN-up epilogue, whose output is the FFN-down input) and the delta-cache commit
 (residual delta, Gamma_t for the next step's routing, similarity of the last two deltas).
 value = algorithmic GEMM FLOPs of the step / step time (TFLOP/s).
 
@@ -118,8 +119,10 @@ class Workload:
             x[:, ch] *= 50.0
             return x.to(torch.bfloat16)
 
-        # two alternating activation sets (consecutive blocks never share an input tensor)
-        self.inputs = [{name: act(k, 10 * s + i) for i, (name, k, _) in enumerate(LINEARS)} for s in range(2)]
+        # two alternating activation sets (consecutive blocks never share an input tensor); the
+        # FFN-down input is not among them: it is GELU(FFN-up output), produced in the step
+        self.inputs = [{name: act(k, 10 * s + i) for i, (name, k, _) in enumerate(LINEARS) if name != "ffn_down"}
+                       for s in range(2)]
         self.x_in = act(HIDDEN, 99)
         # per-block Gamma pairs: X_out = X_in + gamma_b * S * X_in, gamma_b ~ U(0, 0.2)
         g.manual_seed(seed + 7)
@@ -178,17 +181,19 @@ class Workload:
             for li, (name, k, n) in enumerate(LINEARS):
                 lin = blk["lin"][name]
                 route = self.routes[b][li]
-                x, y = xs[name], self.y[name]
+                x = self.y["ffn_up"] if name == "ffn_down" else xs[name]
+                y = self.y[name]
+                act = dit.ACT_GELU_ERF if name == "ffn_up" else dit.ACT_NONE
                 if route == dit.ROUTE_INT8:
                     self._timed("quant_int8", lambda: dit.hadamard_quant_int8(x, HBLOCK, lin.a8["q"], lin.a8["scale"]))
                     self._timed("gemm_int8", lambda: dit.qgemm_int8(lin.a8["q"], lin.a8["scale"], lin.w.int8["q"],
-                                                                    lin.w.int8["scale"], y, self.ws))
+                                                                    lin.w.int8["scale"], y, self.ws, act=act))
                 else:
                     self._timed("quant_nvfp4", lambda: dit.hadamard_quant_nvfp4(
                         x, HBLOCK, lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], self.ws))
                     self._timed("gemm_nvfp4", lambda: dit.qgemm_nvfp4(
                         lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], lin.w.nvfp4["codes"], lin.w.nvfp4["sf"],
-                        lin.w.nvfp4["gs"], y, self.ws))
+                        lin.w.nvfp4["gs"], y, self.ws, act=act))
             d_new, d_old = blk["d"][0], blk["d"][1]
             self._timed("tdc_commit", lambda: dit.tdc_step(
                 dit.TDC_COMMIT, self.x_in, self.ws, x_out=self.x_out[b], d1=d_old if blk["has_delta"] else None,
@@ -261,8 +266,9 @@ def run_tdc_loop(wl, steps: int = 50, tau: float = 0.05, seed: int = 77):
                 lins = wl.blocks[b]["lin"]
                 a.record()
                 for li, (name, k, n) in enumerate(LINEARS):
-                    xin = x if k == HIDDEN else wl.inputs[b % 2]["ffn_down"]
-                    lins[name](xin, routes[li], y[name])
+                    xin = y["ffn_up"] if name == "ffn_down" else x
+                    lins[name](xin, routes[li], y[name],
+                               act=dit.ACT_GELU_ERF if name == "ffn_up" else dit.ACT_NONE)
                     launches += 2 if routes[li] == dit.ROUTE_INT8 else 3
                     route_count[routes[li]] += 1
                 z.record()
@@ -485,19 +491,25 @@ def _oracle_weights():
 
 def oracle_sample(tokens: int, seed: int):
     """The oracle on a token sample of one block: the four routed linears (alternating
-    routes) + the delta commit.  Returns (seconds, flops)."""
+    routes; the FFN-down input is the bf16 GELU of the FFN-up output) + the delta commit.
+    Returns (seconds, flops)."""
+    import numpy as np
     import synth
     from oracle import dmpq as D
+    from oracle import formats as F
     from oracle import tdc as T
     preps = _oracle_weights()
-    xs = [synth.activations(tokens, k, seed=seed + i, dtype="f32") for i, (_, k, _) in enumerate(LINEARS)]
+    xs = {name: synth.activations(tokens, k, seed=seed + i, dtype="f32")
+          for i, (name, k, _) in enumerate(LINEARS) if name != "ffn_down"}
     xi = synth.activations(tokens, HIDDEN, seed=seed + 9)
     xo = synth.gamma_pair(xi, 0.1, seed + 10)
     flops = 0
     t0 = time.perf_counter()
     for i, (name, k, n) in enumerate(LINEARS):
         route = D.ROUTE_INT8 if i % 2 == 0 else D.ROUTE_NVFP4
-        D.routed_linear(xs[i], preps[name], HBLOCK, route)
+        y = D.routed_linear(xs[name], preps[name], HBLOCK, route)
+        if name == "ffn_up":
+            xs["ffn_down"] = F.bf16_bits_to_f32(F.f32_to_bf16_bits(D.gelu_erf(y).astype(np.float32)))
         flops += 2 * tokens * n * k
     T.tdc_commit(xi, xo, None, "bf16")
     return time.perf_counter() - t0, flops
@@ -514,7 +526,7 @@ def cpu_baseline(seconds_budget: float = 15.0):
         if t < 1.0 and tokens < 2048:
             tokens *= 2
     return {"value": round(total_f / total_t / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{reps} oracle passes over one CogVideoX-2B block (4 routed linears, both routes, "
+            "sample": f"{reps} oracle passes over one CogVideoX-2B block (4 routed linears, both routes, GELU "
                       f"+ delta commit) on token samples up to {tokens} tokens; weight preparation untimed; "
                       f"{total_t:.1f} s of CPU work (numpy float64 BLAS on all cores)"}
 
@@ -532,7 +544,7 @@ def run_reference(args, rank, world):
         total_t += t
         total_f += f
     v = total_f / total_t / 1e12
-    sample = (f"each step: the oracle over one CogVideoX-2B block (4 routed linears, both routes, + delta "
+    sample = (f"each step: the oracle over one CogVideoX-2B block (4 routed linears, both routes, GELU, + delta "
               f"commit) on a {tokens}-token sample; weight preparation untimed")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": world,

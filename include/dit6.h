@@ -50,6 +50,11 @@ typedef enum {
 typedef enum { DIT_F32 = 0, DIT_BF16 = 1, DIT_I8 = 2 } dit_dtype;
 typedef enum { DIT_ROUTE_NVFP4 = 0, DIT_ROUTE_INT8 = 1 } dit_route;
 typedef enum { DIT_TDC_COMMIT = 0, DIT_TDC_SKIP = 1 } dit_tdc_mode;
+/* Activation applied in the GEMM epilogue after the bias: none, or GELU in its erf form
+ * x * Phi(x) (the FFN activation between the up and down projections of the CogVideoX-shaped
+ * block), computed in fp32 before the output is stored, with Phi from the erf approximation
+ * of Abramowitz & Stegun 7.1.26 (absolute error of Phi <= 7.5e-8 + fp32 rounding). */
+typedef enum { DIT_ACT_NONE = 0, DIT_ACT_GELU_ERF = 1 } dit_act;
 
 #define DIT_MAX_LAYERS 16
 
@@ -163,23 +168,25 @@ dit_status dit_hadamard_quant_int8(const void* x, dit_dtype dt, int64_t rows, in
  * [EN] 1. Problem Statement "Hardware Gap", 3. Key Contributions 4 (NVFP4 on Blackwell).
  *
  * Y[m, n] = (*a_gs) (*b_gs) sum_k dec(A)[m,k] dec(sA)[m,k/16] dec(B)[n,k] dec(sB)[n,k/16]
- *           (+ bias[n])
+ *           (+ bias[n]), then act (dit_act) elementwise
  * a, b   : device packed E2M1, [m x k/2] and [n x k/2] (both K-major, as written by
  *          dit_hadamard_quant_nvfp4); a_sf, b_sf: tile-layout scales; a_gs, b_gs: device
  *          floats (the tensor scales).  k % 64 == 0; n % 8 == 0.
- * bias   : device float [n] or NULL.     y : device [m x n] of dtype y_dt.
+ * bias   : device float [n] or NULL.     act : DIT_ACT_NONE or DIT_ACT_GELU_ERF (any other
+ *          value is DIT_ERR_INVALID_ARG).     y : device [m x n] of dtype y_dt.
  * ------------------------------------------------------------------------------------ */
 dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
                            const uint8_t* b, const uint8_t* b_sf, const float* b_gs,
-                           int64_t m, int64_t n, int64_t k, const float* bias, void* y,
-                           dit_dtype y_dt, void* ws, size_t ws_bytes, dit_stream_t stream);
+                           int64_t m, int64_t n, int64_t k, const float* bias, dit_act act,
+                           void* y, dit_dtype y_dt, void* ws, size_t ws_bytes,
+                           dit_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * (a7) INT8 GEMM: exact int32 accumulation, per-row x per-column dequantisation.
  * [EN] 2.A Mechanism 3 (INT8 route); [ZH] 2.A weight handling.
  *
  * acc[m, n] = sum_k a[m, k] b[n, k] (int32, exact);
- * Y[m, n]   = (float(acc) * a_scale[m]) * b_scale[n] (+ bias[n]).
+ * Y[m, n]   = act((float(acc) * a_scale[m]) * b_scale[n] (+ bias[n])), act as in a6.
  * a, b : device codes [m x k] and [n x k] in container ab_dt:
  *        DIT_I8   -> warp-level IMMA (mma.sync s8) path;
  *        DIT_BF16 -> tcgen05 bf16 path: the integer codes are exact in bf16, products exact
@@ -191,8 +198,8 @@ dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a
  * ------------------------------------------------------------------------------------ */
 dit_status dit_qgemm_int8(const void* a, const float* a_scale, const void* b,
                           const float* b_scale, dit_dtype ab_dt, int64_t m, int64_t n, int64_t k,
-                          const float* bias, void* y, dit_dtype y_dt, int32_t* acc_debug,
-                          void* ws, size_t ws_bytes, dit_stream_t stream);
+                          const float* bias, dit_act act, void* y, dit_dtype y_dt,
+                          int32_t* acc_debug, void* ws, size_t ws_bytes, dit_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * (a8 / a10) Temporal Delta Cache device step.

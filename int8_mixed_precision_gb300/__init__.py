@@ -17,6 +17,8 @@ ROUTE_NVFP4 = 0
 ROUTE_INT8 = 1
 TDC_COMMIT = 0
 TDC_SKIP = 1
+ACT_NONE = 0
+ACT_GELU_ERF = 1
 MAX_LAYERS = 16
 
 
@@ -134,20 +136,20 @@ def hadamard_quant_int8(x, hblock, q, row_scale, stream=None):
     _check(st, "dit_hadamard_quant_int8")
 
 
-def qgemm_nvfp4(a, a_sf, a_gs, b, b_sf, b_gs, y, ws, bias=None, stream=None):
+def qgemm_nvfp4(a, a_sf, a_gs, b, b_sf, b_gs, y, ws, bias=None, act=ACT_NONE, stream=None):
     m, n, k = a.shape[0], b.shape[0], a.shape[1] * 2
     st = lib().dit_qgemm_nvfp4(_p(a), _p(a_sf), _p(a_gs), _p(b), _p(b_sf), _p(b_gs), m, n, k,
-                               _p(bias), _p(y), _dt(y), _p(ws), ws.numel(), _stream(stream))
+                               _p(bias), act, _p(y), _dt(y), _p(ws), ws.numel(), _stream(stream))
     _check(st, "dit_qgemm_nvfp4")
 
 
-def qgemm_int8(a, a_scale, b, b_scale, y, ws, bias=None, acc_debug=None, stream=None):
+def qgemm_int8(a, a_scale, b, b_scale, y, ws, bias=None, acc_debug=None, act=ACT_NONE, stream=None):
     """a, b: int8 codes (IMMA path) or bf16-held integer codes (tcgen05 bf16 path)."""
     if a.dtype != b.dtype:
         raise DitError("qgemm_int8: a and b must use the same code container")
     m, n, k = a.shape[0], b.shape[0], a.shape[1]
-    st = lib().dit_qgemm_int8(_p(a), _p(a_scale), _p(b), _p(b_scale), _dt(a), m, n, k, _p(bias), _p(y),
-                              _dt(y), _p(acc_debug), _p(ws), ws.numel(), _stream(stream))
+    st = lib().dit_qgemm_int8(_p(a), _p(a_scale), _p(b), _p(b_scale), _dt(a), m, n, k, _p(bias), act,
+                              _p(y), _dt(y), _p(acc_debug), _p(ws), ws.numel(), _stream(stream))
     _check(st, "dit_qgemm_int8")
 
 
@@ -232,19 +234,19 @@ class RoutedLinear:
         container = "bf16" if weight.int8["q"].dtype == _torch().bfloat16 else "int8"
         self.a8 = alloc_int8(max_tokens, weight.k, device, container)
 
-    def __call__(self, x, route: int, y, bias=None, tensor_scale_in=None, stream=None):
+    def __call__(self, x, route: int, y, bias=None, tensor_scale_in=None, act=ACT_NONE, stream=None):
         m = x.shape[0]
         w = self.w
         if route == ROUTE_INT8:
             q, s = self.a8["q"][:m], self.a8["scale"][:m]
             hadamard_quant_int8(x, w.hblock, q, s, stream=stream)
-            qgemm_int8(q, s, w.int8["q"], w.int8["scale"], y, self.ws, bias=bias, stream=stream)
+            qgemm_int8(q, s, w.int8["q"], w.int8["scale"], y, self.ws, bias=bias, act=act, stream=stream)
         else:
             c = self.a4["codes"][:m]
             hadamard_quant_nvfp4(x, w.hblock, c, self.a4["sf"], self.a4["gs"], self.ws,
                                  tensor_scale_in=tensor_scale_in, stream=stream)
             qgemm_nvfp4(c, self.a4["sf"], self.a4["gs"], w.nvfp4["codes"], w.nvfp4["sf"],
-                        w.nvfp4["gs"], y, self.ws, bias=bias, stream=stream)
+                        w.nvfp4["gs"], y, self.ws, bias=bias, act=act, stream=stream)
         return y
 
 

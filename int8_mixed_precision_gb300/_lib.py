@@ -29,8 +29,10 @@ SIGNATURES = {
     "dit_gamma_route_noalloc": (_i32, [_vp, _vp, _i32, _i64, _f, _f, _f, _i32, _vp, _vp, _vp]),
     "dit_hadamard_quant_nvfp4": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dit_hadamard_quant_int8": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _i32, _vp, _vp]),
-    "dit_qgemm_nvfp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _i32, _vp, _sz, _vp]),
-    "dit_qgemm_int8": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "dit_qgemm_nvfp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _sz,
+                                _vp]),
+    "dit_qgemm_int8": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp, _sz,
+                               _vp]),
     "dit_tdc_step": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _sz, _vp]),
     "dit_tdc_state_init": (None, [_vp]),
     "dit_tdc_decide": (_i32, [_vp, ctypes.c_double]),

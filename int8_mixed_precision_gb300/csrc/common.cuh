@@ -67,6 +67,30 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// GEMM epilogue flags: bit 0 = bf16 output (else fp32), bit 1 = GELU (erf form) after bias
+constexpr int EPI_BF16 = 1, EPI_GELU = 2;
+
+// GELU(x) = x * Phi(x), Phi the standard normal CDF, with Phi from the rational approximation
+// of erf in Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26 (Hastings):
+// for z >= 0, erfc(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2) + e(z),
+// t = 1 / (1 + p z), |e(z)| <= 1.5e-7.  With z = |x| / sqrt 2, Phi(x) = erfc(z) / 2 for x < 0 and
+// 1 - erfc(z) / 2 otherwise, so the negative tail carries no cancellation; the absolute error
+// of Phi is <= 7.5e-8 plus fp32 rounding.  One reciprocal, one exponential and six FMAs: the
+// epilogue warps run it beside the accumulator drain.
+__device__ __forceinline__ float gelu_erf(float x) {
+  const float z = fabsf(x) * 0.70710678118654752f;
+  float t;  // 1 / (1 + p z) to ~1 ulp; the approximation's own error dominates
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, z, 1.0f)));
+  float p = fmaf(1.061405429f, t, -1.453152027f);
+  p = fmaf(p, t, 1.421413741f);
+  p = fmaf(p, t, -0.284496736f);
+  p = fmaf(p, t, 0.254829592f);
+  const float h = 0.5f * (p * t) * __expf(-z * z);   // erfc(z) / 2
+  return x * (x < 0.0f ? h : 1.0f - h);
+}
+
+__device__ __forceinline__ float epi_act(float v, int epi) { return (epi & EPI_GELU) ? gelu_erf(v) : v; }
+
 // ---------------------------------------------------------------------------------------
 // packed fp32x2 arithmetic (one instruction for two lanes, no contraction)
 // ---------------------------------------------------------------------------------------

@@ -40,7 +40,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_int8(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M,
-                int N, int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
+                int N, int K, const float* __restrict__ bias, void* __restrict__ y, int epi,
                 int32_t* __restrict__ acc_out, void* ws) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -141,8 +141,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           v0 = __fadd_rn(v0, bias[col]);
           v1 = __fadd_rn(v1, bias[col + 1]);
         }
+        v0 = epi_act(v0, epi);
+        v1 = epi_act(v1, epi);
         const int64_t off = (int64_t)row * N + col;
-        if (y_bf16)
+        if (epi & EPI_BF16)
           *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(y) + off) = f2_to_bf16x2(v0, v1);
         else
           *reinterpret_cast<float2*>(reinterpret_cast<float*>(y) + off) = make_float2(v0, v1);
@@ -159,26 +161,28 @@ using namespace dit6;
 
 namespace dit6 {
 dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
-                        int64_t n, int64_t k, const float* bias, void* y, int y_bf16, int32_t* acc_out,
+                        int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
                         void* ws, cudaStream_t st);
 }
 
 extern "C" dit_status dit_qgemm_int8(const void* a, const float* a_scale, const void* b,
                                      const float* b_scale, dit_dtype ab_dt, int64_t m, int64_t n,
-                                     int64_t k, const float* bias, void* y, dit_dtype y_dt,
-                                     int32_t* acc_debug, void* ws, size_t ws_bytes,
-                                     dit_stream_t stream) {
+                                     int64_t k, const float* bias, dit_act act, void* y,
+                                     dit_dtype y_dt, int32_t* acc_debug, void* ws,
+                                     size_t ws_bytes, dit_stream_t stream) {
   if (!a || !b || !a_scale || !b_scale || !y || !ws || ws_bytes < WS_BYTES) return DIT_ERR_INVALID_ARG;
   if (m <= 0 || n <= 0 || k <= 0 || m > 0x7fffffff || n > 0x7fffffff || k > 0x7fffffff)
     return DIT_ERR_INVALID_ARG;
   if (y_dt != DIT_F32 && y_dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
   if (ab_dt != DIT_I8 && ab_dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
+  if (act != DIT_ACT_NONE && act != DIT_ACT_GELU_ERF) return DIT_ERR_INVALID_ARG;
+  const int epi = (y_dt == DIT_BF16 ? EPI_BF16 : 0) | (act == DIT_ACT_GELU_ERF ? EPI_GELU : 0);
   if (k % 16 || n % 8) return DIT_ERR_UNSUPPORTED;
   if (!aligned32(a) || !aligned32(b) || !aligned32(y) || !aligned32(ws) ||
       (acc_debug && !aligned32(acc_debug)))
     return DIT_ERR_ALIGNMENT;
   if (ab_dt == DIT_BF16)
-    return gemm_int8_tc(a, a_scale, b, b_scale, m, n, k, bias, y, y_dt == DIT_BF16 ? 1 : 0, acc_debug,
+    return gemm_int8_tc(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_debug,
                         ws, reinterpret_cast<cudaStream_t>(stream));
   CUtensorMap ta, tb;
   if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(a), (uint64_t)k,
@@ -196,7 +200,7 @@ extern "C" dit_status dit_qgemm_int8(const void* a, const float* a_scale, const 
   dim3 grid((unsigned)((n + i8::BN - 1) / i8::BN), (unsigned)((m + i8::BM - 1) / i8::BM));
   if (grid.y > 65535) return DIT_ERR_UNSUPPORTED;
   i8::k_gemm_int8<<<grid, i8::THREADS, i8::SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
-      ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, y_dt == DIT_BF16 ? 1 : 0,
+      ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, epi,
       acc_debug, ws);
   DIT_CHECK_LAUNCH();
   return DIT_OK;

@@ -113,11 +113,14 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 // MC = 1: independent CTAs.  MC = 2: clusters of two CTAs on adjacent 128-row M blocks and the
 // same N block; each loads half of the shared B tile and multicasts it to both, halving the
 // B traffic from L2; a stage is refilled only after both CTAs' MMAs have consumed it.
-template <int BN, int MC>
+// GELU selects the epilogue activation at compile time (erf GELU after the bias): the wide
+// accumulator drain already runs at the register cap, so the plain instantiation carries none
+// of the activation's code.
+template <int BN, int MC, bool GELU>
 __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     k_gemm_int8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N,
-                   int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
+                   int K, const float* __restrict__ bias, void* __restrict__ y, int epi,
                    int32_t* __restrict__ acc_out, void* ws, int stall) {
   using C = Cfg<BN>;
   constexpr int S = C::STAGES;
@@ -288,9 +291,10 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             const int col = cb + i < N ? cb + i : N - 1;
             v[i] = __fmul_rn(__fmul_rn((float)acc[c * 16 + i], sa), b_scale[col]);
             if (bias) v[i] = __fadd_rn(v[i], bias[col]);
+            if (GELU) v[i] = epi_act(v[i], EPI_GELU);
           }
           if (cb + 16 <= N && (N % 16) == 0) {
-            if (y_bf16) {
+            if (epi & EPI_BF16) {
               uint32_t w[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) w[i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               if (cb + i >= N) continue;
-              if (y_bf16)
+              if (epi & EPI_BF16)
                 reinterpret_cast<__nv_bfloat16*>(y)[off + c * 16 + i] = __float2bfloat16_rn(v[i]);
               else
                 reinterpret_cast<float*>(y)[off + c * 16 + i] = v[i];
@@ -342,9 +346,9 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
   if (MC > 1) cluster_sync();  // no peer may still multicast into, or arrive on, this CTA
 }
 
-template <int BN, int MC>
+template <int BN, int MC, bool GELU>
 dit_status launch(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
-                  int64_t n, int64_t k, const float* bias, void* y, int y_bf16, int32_t* acc_out,
+                  int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
                   void* ws, cudaStream_t st) {
   using C = Cfg<BN>;
   CUtensorMap ta, tb;
@@ -353,7 +357,7 @@ dit_status launch(const void* a, const float* a_scale, const void* b, const floa
       !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(b), (uint64_t)k, (uint64_t)n,
                       (uint64_t)k * 2, BK, BN / MC, CU_TENSOR_MAP_SWIZZLE_128B))
     return DIT_ERR_CUDA;
-  auto kern = k_gemm_int8_tc<BN, MC>;
+  auto kern = k_gemm_int8_tc<BN, MC, GELU>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
@@ -383,7 +387,7 @@ dit_status launch(const void* a, const float* a_scale, const void* b, const floa
   }
   if (grid > items * MC) grid = items * MC;
   cfg.gridDim = dim3((unsigned)grid);
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, y_bf16, acc_out,
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, epi, acc_out,
                          ws, MC > 1 ? 0 : test_stall()) != cudaSuccess)
     return DIT_ERR_CUDA;
   return DIT_OK;
@@ -392,16 +396,21 @@ dit_status launch(const void* a, const float* a_scale, const void* b, const floa
 }  // namespace i8tc
 
 dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
-                        int64_t n, int64_t k, const float* bias, void* y, int y_bf16, int32_t* acc_out,
+                        int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
                         void* ws, cudaStream_t st) {
   const char* e = getenv("DIT6_INT8_TC_BN");
   const char* c = getenv("DIT6_INT8_TC_CLUSTER");
   const int bn = e ? atoi(e) : 256;
   const int mc = c ? atoi(c) : 1;
-  if (bn == 128) return i8tc::launch<128, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
-  if (bn == 192) return i8tc::launch<192, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
-  if (mc == 2) return i8tc::launch<256, 2>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
-  return i8tc::launch<256, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, y_bf16, acc_out, ws, st);
+  const bool g = (epi & EPI_GELU) != 0;
+#define DIT6_I8TC(BN_, MC_)                                                                          \
+  return g ? i8tc::launch<BN_, MC_, true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st) \
+           : i8tc::launch<BN_, MC_, false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
+  if (bn == 128) DIT6_I8TC(128, 1);
+  if (bn == 192) DIT6_I8TC(192, 1);
+  if (mc == 2) DIT6_I8TC(256, 2);
+  DIT6_I8TC(256, 1);
+#undef DIT6_I8TC
 }
 
 }  // namespace dit6

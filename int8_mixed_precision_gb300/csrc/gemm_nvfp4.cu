@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(192, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
                  const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
-                 int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
+                 int K, const float* __restrict__ bias, void* __restrict__ y, int epi,
                  void* ws) {
   using C = Cfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
@@ -231,10 +231,11 @@ __global__ void __launch_bounds__(192, 1)
         for (int i = 0; i < 32; ++i) {
           v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
           if (bias && col0 + i < N) v[i] = __fadd_rn(v[i], bias[col0 + i]);
+          v[i] = epi_act(v[i], epi);
         }
         const int64_t off = (int64_t)row * N + col0;
         if (col0 + 32 <= N && (N % 16) == 0) {
-          if (y_bf16) {
+          if (epi & EPI_BF16) {
             U8x32 o0, o1;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             if (col0 + i >= N) continue;
-            if (y_bf16)
+            if (epi & EPI_BF16)
               reinterpret_cast<__nv_bfloat16*>(y)[off + i] = __float2bfloat16_rn(v[i]);
             else
               reinterpret_cast<float*>(y)[off + i] = v[i];
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(PCfg<BN, STAGES, ACC_BUFS>::THREADS, 1)
     k_gemm_nvfp4_p(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
                    const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
-                   int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
+                   int K, const float* __restrict__ bias, void* __restrict__ y, int epi,
                    void* ws) {
   using C = PCfg<BN, STAGES, ACC_BUFS>;
   constexpr int S = STAGES;
@@ -456,10 +457,11 @@ __global__ void __launch_bounds__(PCfg<BN, STAGES, ACC_BUFS>::THREADS, 1)
         for (int i = 0; i < 32; ++i) {
           v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
           if (bias) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
+          v[i] = epi_act(v[i], epi);
         }
         const int64_t off = (int64_t)row * N + col0;
         if (col0 + 32 <= N && (N % 16) == 0) {
-          if (y_bf16) {
+          if (epi & EPI_BF16) {
             U8x32 o0, o1;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -483,7 +485,7 @@ __global__ void __launch_bounds__(PCfg<BN, STAGES, ACC_BUFS>::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             if (col0 + i >= N) continue;
-            if (y_bf16)
+            if (epi & EPI_BF16)
               reinterpret_cast<__nv_bfloat16*>(y)[off + i] = __float2bfloat16_rn(v[i]);
             else
               reinterpret_cast<float*>(y)[off + i] = v[i];
@@ -533,7 +535,7 @@ __global__ void __launch_bounds__(RCfg::THREADS, 1)
     k_gemm_nvfp4_r(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
                    const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
-                   int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
+                   int K, const float* __restrict__ bias, void* __restrict__ y, int epi,
                    void* ws) {
   using C = RCfg;
   constexpr int S = C::STAGES, BN = C::BN;
@@ -707,10 +709,11 @@ __global__ void __launch_bounds__(RCfg::THREADS, 1)
         for (int i = 0; i < 32; ++i) {
           v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
           if (bias) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
+          v[i] = epi_act(v[i], epi);
         }
         const int64_t off = (int64_t)row * N + col0;
         if (col0 + 32 <= N && (N % 16) == 0) {
-          if (y_bf16) {
+          if (epi & EPI_BF16) {
             U8x32 o0, o1;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -734,7 +737,7 @@ __global__ void __launch_bounds__(RCfg::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             if (col0 + i >= N) continue;
-            if (y_bf16)
+            if (epi & EPI_BF16)
               reinterpret_cast<__nv_bfloat16*>(y)[off + i] = __float2bfloat16_rn(v[i]);
             else
               reinterpret_cast<float*>(y)[off + i] = v[i];
@@ -758,7 +761,7 @@ __global__ void __launch_bounds__(RCfg::THREADS, 1)
 
 static dit_status launch_r(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf, const uint8_t* b_sf,
                            const float* a_gs, const float* b_gs, int M, int N, int K, const float* bias, void* y,
-                           int y_bf16, void* ws, cudaStream_t st) {
+                           int epi, void* ws, cudaStream_t st) {
   using C = RCfg;
   static bool attr_done = false;
   if (!attr_done) {
@@ -771,7 +774,7 @@ static dit_status launch_r(const CUtensorMap& ta, const CUtensorMap& tb, const u
   int64_t grid = num_sms();
   if (grid > tiles) grid = tiles;
   k_gemm_nvfp4_r<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias,
-                                                                    y, y_bf16, ws);
+                                                                    y, epi, ws);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -812,7 +815,7 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
     k_gemm_nvfp4_s(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
                    const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
-                   int K, const float* __restrict__ bias, void* __restrict__ y, int y_bf16,
+                   int K, const float* __restrict__ bias, void* __restrict__ y, int epi,
                    void* ws, int stall) {
   using C = SCfg<BN, STAGES, CTAS>;
   constexpr int S = STAGES;
@@ -983,10 +986,11 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
         for (int i = 0; i < 32; ++i) {
           v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
           if (bias) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
+          v[i] = epi_act(v[i], epi);
         }
         const int64_t off = (int64_t)row * N + col0;
         if (col0 + 32 <= N && (N % 16) == 0) {
-          if (y_bf16) {
+          if (epi & EPI_BF16) {
             U8x32 o0, o1;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -1010,7 +1014,7 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             if (col0 + i >= N) continue;
-            if (y_bf16)
+            if (epi & EPI_BF16)
               reinterpret_cast<__nv_bfloat16*>(y)[off + i] = __float2bfloat16_rn(v[i]);
             else
               reinterpret_cast<float*>(y)[off + i] = v[i];
@@ -1035,7 +1039,7 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
 template <int BN, int STAGES, int CTAS>
 static dit_status launch_s(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf, const uint8_t* b_sf,
                            const float* a_gs, const float* b_gs, int M, int N, int K, const float* bias, void* y,
-                           int y_bf16, void* ws, cudaStream_t st) {
+                           int epi, void* ws, cudaStream_t st) {
   using C = SCfg<BN, STAGES, CTAS>;
   static bool attr_done = false;
   auto kern = k_gemm_nvfp4_s<BN, STAGES, CTAS>;
@@ -1048,7 +1052,7 @@ static dit_status launch_s(const CUtensorMap& ta, const CUtensorMap& tb, const u
   int64_t grid = (int64_t)num_sms() * CTAS;
   if (grid > tiles) grid = tiles;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y,
-                                                         y_bf16, ws, test_stall());
+                                                         epi, ws, test_stall());
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -1056,7 +1060,7 @@ static dit_status launch_s(const CUtensorMap& ta, const CUtensorMap& tb, const u
 template <int BN, int STAGES, int ACC_BUFS, int CTAS_PER_SM = 1>
 static dit_status launch_p(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf,
                            const uint8_t* b_sf, const float* a_gs, const float* b_gs, int M, int N,
-                           int K, const float* bias, void* y, int y_bf16, void* ws, cudaStream_t st) {
+                           int K, const float* bias, void* y, int epi, void* ws, cudaStream_t st) {
   using C = PCfg<BN, STAGES, ACC_BUFS>;
   static bool attr_done = false;
   auto kern = k_gemm_nvfp4_p<BN, STAGES, ACC_BUFS>;
@@ -1069,7 +1073,7 @@ static dit_status launch_p(const CUtensorMap& ta, const CUtensorMap& tb, const u
   int64_t grid = (int64_t)num_sms() * CTAS_PER_SM;
   if (grid > tiles) grid = tiles;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y,
-                                                         y_bf16, ws);
+                                                         epi, ws);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -1077,7 +1081,7 @@ static dit_status launch_p(const CUtensorMap& ta, const CUtensorMap& tb, const u
 template <int BN, int STAGES, bool SPLIT_N>
 static dit_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf,
                          const uint8_t* b_sf, const float* a_gs, const float* b_gs, int M, int N,
-                         int K, const float* bias, void* y, int y_bf16, void* ws,
+                         int K, const float* bias, void* y, int epi, void* ws,
                          cudaStream_t st) {
   using C = Cfg<BN, STAGES>;
   static bool attr_done = false;
@@ -1090,7 +1094,7 @@ static dit_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const uin
   }
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
   if (grid.y > 65535) return DIT_ERR_UNSUPPORTED;
-  kern<<<grid, 192, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y, y_bf16, ws);
+  kern<<<grid, 192, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y, epi, ws);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -1113,14 +1117,15 @@ static int nvfp4_tile_cfg() {
 
 extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
                                       const uint8_t* b, const uint8_t* b_sf, const float* b_gs,
-                                      int64_t m, int64_t n, int64_t k, const float* bias, void* y,
-                                      dit_dtype y_dt, void* ws, size_t ws_bytes,
-                                      dit_stream_t stream) {
+                                      int64_t m, int64_t n, int64_t k, const float* bias,
+                                      dit_act act, void* y, dit_dtype y_dt, void* ws,
+                                      size_t ws_bytes, dit_stream_t stream) {
   if (!a || !a_sf || !a_gs || !b || !b_sf || !b_gs || !y || !ws || ws_bytes < WS_BYTES)
     return DIT_ERR_INVALID_ARG;
   if (m <= 0 || n <= 0 || k <= 0 || m > 0x7fffffff || n > 0x7fffffff || k > 0x7fffffff)
     return DIT_ERR_INVALID_ARG;
   if (y_dt != DIT_F32 && y_dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
+  if (act != DIT_ACT_NONE && act != DIT_ACT_GELU_ERF) return DIT_ERR_INVALID_ARG;
   if (k % 64 || n % 8) return DIT_ERR_UNSUPPORTED;
   if (!aligned32(a) || !aligned32(b) || !aligned32(a_sf) || !aligned32(b_sf) || !aligned32(y) ||
       !aligned32(ws))
@@ -1134,7 +1139,7 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
                       (uint64_t)n, (uint64_t)(k / 2), f4::BK / 2, bn_box, CU_TENSOR_MAP_SWIZZLE_128B))
     return DIT_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int yb = y_dt == DIT_BF16 ? 1 : 0;
+  const int yb = (y_dt == DIT_BF16 ? EPI_BF16 : 0) | (act == DIT_ACT_GELU_ERF ? EPI_GELU : 0);
   switch (cfg) {
     case 1: return f4::launch<256, 3, true>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 2: return f4::launch<256, 3, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);

@@ -321,7 +321,10 @@ def routed_linear(x: np.ndarray, wprep: dict, b: int, route: int) -> np.ndarray:
 
 
 def gelu_erf(x: np.ndarray) -> np.ndarray:
-    """x * Phi(x), erf form, float64 (the FFN activation of the CogVideoX-shaped block)."""
-    from scipy.special import erf
+    """x * Phi(x) with Phi the standard normal CDF, float64: the FFN activation of the
+    CogVideoX-shaped block (erf form, not the tanh approximation).  Phi(x) is written as
+    erfc(-x / sqrt 2) / 2, which equals (1 + erf(x / sqrt 2)) / 2 without the cancellation of
+    the latter for large negative x."""
+    from scipy.special import erfc
     x = np.asarray(x, np.float64)
-    return 0.5 * x * (1.0 + erf(x / math.sqrt(2.0)))
+    return 0.5 * x * erfc(-x / math.sqrt(2.0))

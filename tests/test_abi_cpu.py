@@ -76,10 +76,13 @@ def test_host_argument_validation_without_device_work(L):
     f = ctypes.c_float * 17
     assert L.dit_gamma_route(fake_misaligned, fake_misaligned, 1, 10, f(), f(), f(), 17, ws, ws, ws, 65536, nul) == 1
     assert L.dit_gamma_route(fake_misaligned, fake_misaligned, 1, 10, f(), f(), f(), 1, ws, ws, ws, 65536, nul) == 2
-    assert L.dit_qgemm_int8(fake_misaligned, ws, fake_misaligned, ws, 2, 4, 8, 100, nul, ws, 1, nul, ws, 65536, nul) == 3
-    assert L.dit_qgemm_int8(ws, ws, ws, ws, 0, 4, 8, 128, nul, ws, 1, nul, ws, 65536, nul) == 1
-    assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 96, nul, ws, 1, ws, 65536, nul) == 3
-    assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 128, nul, ws, 1, ws, 100, nul) == 1
+    assert L.dit_qgemm_int8(fake_misaligned, ws, fake_misaligned, ws, 2, 4, 8, 100, nul, 0, ws, 1, nul, ws, 65536, nul) == 3
+    assert L.dit_qgemm_int8(ws, ws, ws, ws, 0, 4, 8, 128, nul, 0, ws, 1, nul, ws, 65536, nul) == 1
+    assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 96, nul, 0, ws, 1, ws, 65536, nul) == 3
+    assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 128, nul, 0, ws, 1, ws, 100, nul) == 1
+    # an activation code outside dit_act
+    assert L.dit_qgemm_int8(ws, ws, ws, ws, 2, 4, 8, 128, nul, 5, ws, 1, nul, ws, 65536, nul) == 1
+    assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 128, nul, 2, ws, 1, ws, 65536, nul) == 1
     ws2 = ctypes.c_void_p(0x4000)
     assert L.dit_tdc_step(0, fake_misaligned, fake_misaligned, nul, ws, ws2, 1, 64, ws, ws, ws, 65536, nul) == 2
     assert L.dit_tdc_step(0, ws, ws, nul, ws, ws, 1, 64, ws, ws, ws, 65536, nul) == 1   # d1 == d_new

@@ -60,9 +60,10 @@ def _check_nvfp4_rows(codes_dev, sf_dev, sg, x_rows_f32, rows_idx, m, k):
     return codes, sf
 
 
-def _routed_linear_full(m, k, n, dist, mult, frac, seed, routes, ws, x_bits=None):
+def _routed_linear_full(m, k, n, dist, mult, frac, seed, routes, ws, x_bits=None, act=0, keep=None):
     """Quantise a full [m x k] activation and an [n x k] weight on the GPU along the given
-    routes, run the GEMM, and check sampled rows of every stage against the oracle."""
+    routes, run the GEMM (with the epilogue activation act), and check sampled rows of every
+    stage against the oracle.  keep: route whose full bf16 output is returned (host bits)."""
     if x_bits is None:
         x_bits = synth.activations(m, k, dist=dist, outlier_frac=frac, outlier_mult=mult, seed=seed)
     w = synth.weights(n, k, seed=seed + 1)
@@ -73,8 +74,9 @@ def _routed_linear_full(m, k, n, dist, mult, frac, seed, routes, ws, x_bits=None
     rows = _sample_rows(m, seed)
     wrows = _sample_rows(n, seed + 2, 24)
     xr = F.bf16_bits_to_f32(x_bits[rows])
+    kept = None
     for route in routes:
-        lin(xd, route, y)
+        lin(xd, route, y, act=act)
         torch.cuda.synchronize()
         yh = F.bf16_bits_to_f32(host(y[torch.from_numpy(rows).cuda()]))
         if route == dit.ROUTE_INT8:
@@ -93,10 +95,15 @@ def _routed_linear_full(m, k, n, dist, mult, frac, seed, routes, ws, x_bits=None
             _check_nvfp4_rows(wq.nvfp4["codes"], wq.nvfp4["sf"], wsg, w[wrows], wrows, n, k)
             ref = D.gemm_nvfp4(codes, sf, sg, D.unpack_e2m1(host(wq.nvfp4["codes"])),
                                F.sf_from_tiled(host(wq.nvfp4["sf"]), n, k), wsg)
+        if act == dit.ACT_GELU_ERF:
+            ref = D.gelu_erf(ref)
         refb = F.bf16_bits_to_f32(F.f32_to_bf16_bits(ref.astype(np.float32)))
         assert rel_fro(yh, refb) <= TOL, (route, rel_fro(yh, refb))
+        if route == keep:
+            kept = host(y)
     torch.cuda.synchronize()
     assert dit.device_status(ws) == 0
+    return kept
 
 
 @pytest.mark.parametrize("layer,k,n", [("qkv", 3072, 9216), ("out", 3072, 3072), ("ffn_up", 3072, 12288),
@@ -105,6 +112,19 @@ def test_cogvideox_5b_block_linears(layer, k, n, ws):
     """CogVideoX-5B-shaped linears: 17776 tokens, Laplace(0,1) with 0.5% channels x100."""
     _routed_linear_full(synth.TOKENS_2B, k, n, "laplace", 100.0, 0.005, 3000 + k + n,
                         (dit.ROUTE_NVFP4, dit.ROUTE_INT8), ws)
+
+
+@pytest.mark.parametrize("up_route,down_routes", [(1, (0, 1)), (0, (1,))])
+def test_cogvideox_2b_ffn_chain_with_gelu(up_route, down_routes, ws):
+    """The CogVideoX-2B FFN as one chain: 17776 x 1920 -> 7680 with GELU (erf form) fused in
+    the up projection's epilogue, whose bf16 output is the down projection's input
+    (7680 -> 1920).  Each stage is checked on sampled rows against the oracle, the down
+    projection on the GPU's own GELU output (its NVFP4 tensor scale from that whole tensor)."""
+    m = synth.TOKENS_2B
+    h = _routed_linear_full(m, 1920, 7680, "normal", 50.0, 0.01, 5000, (up_route,), ws, act=dit.ACT_GELU_ERF,
+                            keep=up_route)
+    assert h is not None and h.shape == (m, 7680)
+    _routed_linear_full(m, 7680, 1920, None, None, None, 5100, down_routes, ws, x_bits=h)
 
 
 def test_long_sequence_1080p_ffn_up(ws):

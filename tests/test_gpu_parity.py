@@ -275,7 +275,33 @@ def test_int8_gemm_exact_accumulators(m, n, k, container, bn, ws, monkeypatch):
     yb = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
     dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), yb, ws, bias=dev_f32(bias))
     assert rel_fro(F.bf16_bits_to_f32(host(yb)), F.bf16_bits_to_f32(F.f32_to_bf16_bits(ref.astype(np.float32)))) <= GEMM_TOL
+    # GELU (erf form) in the epilogue: fp32 pre-activation, x * Phi(x) before the store
+    dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws, bias=dev_f32(bias), act=dit.ACT_GELU_ERF)
+    assert rel_fro(host(y), D.gelu_erf(ref)) <= 2e-6
     _status_clean(ws)
+
+
+@pytest.mark.parametrize("container", [torch.int8, torch.bfloat16])
+def test_gelu_epilogue_elementwise_error_bound(container, ws):
+    """GELU in the epilogue over pre-activations spread across [-9, 9] (tails included):
+    every output within |x| * 4e-7 of x * Phi(x) in float64, x being the kernel's own fp32
+    pre-activation (acc * row scale) * column scale."""
+    m, n, k = 384, 256, 16
+    a = np.zeros((m, k), np.int8)
+    a[:, 0] = 1
+    b = np.zeros((n, k), np.int8)
+    b[:, 0] = np.linspace(-127, 127, n).round().astype(np.int8)
+    sa = np.linspace(1e-3, 1.0, m).astype(np.float32)
+    sb = np.full(n, 9.0 / 127.0, np.float32)
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    dit.qgemm_int8(_int8_dev(a, container), dev_f32(sa), _int8_dev(b, container), dev_f32(sb), y, ws,
+                   act=dit.ACT_GELU_ERF)
+    _status_clean(ws)
+    x = (D.gemm_int8_acc(a, b).astype(np.float32) * sa[:, None]).astype(np.float32) * sb[None, :]
+    x = x.astype(np.float32)
+    err = np.abs(host(y).astype(np.float64) - D.gelu_erf(x))
+    assert (err <= 4e-7 * np.abs(x) + 1e-37).all(), float(np.max(err / np.maximum(np.abs(x), 1e-30)))
+    assert host(y)[x == 0].tolist() == [0.0] * int((x == 0).sum())
 
 
 def _adversarial_int8(m, n, k, seed):
@@ -340,6 +366,10 @@ def test_nvfp4_gemm_parity(m, n, k, cfg, ws, monkeypatch):
     dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], yb, ws, bias=bias)
     refb = F.bf16_bits_to_f32(F.f32_to_bf16_bits((ref + host(bias)[None, :]).astype(np.float32)))
     assert rel_fro(F.bf16_bits_to_f32(host(yb)), refb) <= GEMM_TOL
+    dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], y, ws, bias=bias,
+                    act=dit.ACT_GELU_ERF)
+    _status_clean(ws)
+    assert rel_fro(host(y), D.gelu_erf(ref + host(bias)[None, :])) <= GEMM_TOL
 
 
 # ------------------------------------------------------------------------------ routed linear

@@ -511,3 +511,39 @@ def test_planted_transposed_operand_is_caught():
     naive = np.array([[sum(int(a[m, k]) * int(b[n, k]) for k in range(4)) for n in range(4)] for m in range(4)])
     assert np.array_equal(D.gemm_int8_acc(a, b), naive)
     assert not np.array_equal(acc_bad, naive)
+
+
+# ----------------------------------------------------------------------------------------
+# GELU (erf form) of the FFN between the up and down projections
+# ----------------------------------------------------------------------------------------
+
+
+def test_gelu_erf_matches_integrated_normal_density():
+    """x * Phi(x) with Phi obtained by quadrature of the standard normal density (no erf)."""
+    from scipy.integrate import quad
+    xs = np.array([-6.0, -3.0, -1.5, -0.7, -0.1, 0.0, 0.05, 0.3, 1.0, 2.2, 4.0])
+    pdf = lambda t: math.exp(-0.5 * t * t) / math.sqrt(2.0 * math.pi)
+    for x in xs:
+        phi = quad(pdf, -np.inf, x, epsabs=1e-15, epsrel=1e-13)[0]
+        assert D.gelu_erf(np.array([x]))[0] == pytest.approx(x * phi, rel=1e-10, abs=1e-15)
+
+
+def test_gelu_erf_table_values_and_identities():
+    # Phi(1) = 0.8413447461, Phi(-1) = 0.1586552539, Phi(2) = 0.9772498681 (normal tables)
+    g = D.gelu_erf(np.array([1.0, -1.0, 2.0, 0.0]))
+    assert g[0] == pytest.approx(0.8413447461, abs=1e-10)
+    assert g[1] == pytest.approx(-0.1586552539, abs=1e-10)
+    assert g[2] == pytest.approx(2 * 0.9772498681, abs=1e-9)
+    assert g[3] == 0.0
+    x = synth.rng(5).normal(0, 3, 1000)
+    # Phi(x) + Phi(-x) = 1  =>  GELU(x) - GELU(-x) = x
+    assert np.allclose(D.gelu_erf(x) - D.gelu_erf(-x), x, rtol=0, atol=1e-13)
+    # far tail: Phi(-10) = 7.6198530241605e-24 keeps its relative accuracy
+    assert D.gelu_erf(np.array([-10.0]))[0] == pytest.approx(-10 * 7.6198530241605e-24, rel=1e-9)
+
+
+def test_planted_tanh_gelu_is_caught():
+    """The tanh approximation of GELU is a different function: the quadrature pin rejects it."""
+    x = np.linspace(-4, 4, 81)
+    tanh_form = 0.5 * x * (1 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3)))
+    assert np.max(np.abs(tanh_form - D.gelu_erf(x))) > 1e-4
