@@ -64,8 +64,9 @@ const char* dit_status_str(dit_status s);
 /* Library version, "major.minor.patch" (static storage). */
 const char* dit_version(void);
 
-/* Bytes of workspace every call below needs (a constant; it holds a status word, a
- * completion counter and per-CTA partial sums). */
+/* Bytes of workspace every call below needs (a constant, about 24 MiB: a status word, a
+ * completion counter, per-CTA partial sums, and the int32 partial accumulators with their
+ * arrival tickets of the INT8 GEMM's split-K tail). */
 size_t dit_workspace_bytes(void);
 
 /* Byte offset, inside the workspace, of the uint32 device status word (bit i set means

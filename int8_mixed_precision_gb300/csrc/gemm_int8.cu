@@ -162,7 +162,7 @@ using namespace dit6;
 namespace dit6 {
 dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
                         int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
-                        void* ws, cudaStream_t st);
+                        void* ws, size_t ws_bytes, cudaStream_t st);
 }
 
 extern "C" dit_status dit_qgemm_int8(const void* a, const float* a_scale, const void* b,
@@ -183,7 +183,7 @@ extern "C" dit_status dit_qgemm_int8(const void* a, const float* a_scale, const 
     return DIT_ERR_ALIGNMENT;
   if (ab_dt == DIT_BF16)
     return gemm_int8_tc(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_debug,
-                        ws, reinterpret_cast<cudaStream_t>(stream));
+                        ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
   CUtensorMap ta, tb;
   if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void*>(a), (uint64_t)k,
                       (uint64_t)m, (uint64_t)k, i8::BK, i8::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||

@@ -116,12 +116,15 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 // GELU selects the epilogue activation at compile time (erf GELU after the bias): the wide
 // accumulator drain already runs at the register cap, so the plain instantiation carries none
 // of the activation's code.
-template <int BN, int MC, bool GELU>
+// SPLIT selects the split-K tail instantiation (last partial wave split along K, see launch);
+// the whole-tile instantiation keeps its own loops, untouched by the split's bookkeeping,
+// because this kernel runs at the register cap and its speed follows the code layout.
+template <int BN, int MC, bool GELU, bool SPLIT>
 __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     k_gemm_int8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N,
                    int K, const float* __restrict__ bias, void* __restrict__ y, int epi,
-                   int32_t* __restrict__ acc_out, void* ws, int stall) {
+                   int32_t* __restrict__ acc_out, void* ws, int stall, int tail_base, int parts) {
   using C = Cfg<BN>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -147,6 +150,31 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
   auto tile_n0 = [&](int item) { return (item % n_tiles_n) * BN; };
   const int nkb = (K + BK - 1) / BK;
   const int nchunks = (nkb + KCHUNK_BLOCKS - 1) / KCHUNK_BLOCKS;
+  // SPLIT work items: tiles [0, tail_base) whole; each tile from tail_base on split along K
+  // into `parts` items whose int32 partial sums the last part to finish adds (exactly)
+  const int n_items = tail_base + (n_tiles - tail_base) * parts;
+  struct Item {
+    int m0, n0, kb_lo, kb_hi, slot, part;  // part < 0: a whole tile
+  };
+  auto decode = [&](int item) {
+    Item it;
+    int tile = item;
+    it.slot = 0;
+    it.part = -1;
+    it.kb_lo = 0;
+    it.kb_hi = nkb;
+    if (item >= tail_base) {
+      const int j = item - tail_base;
+      it.slot = j / parts;
+      it.part = j % parts;
+      tile = tail_base + it.slot;
+      it.kb_lo = (int)((int64_t)it.part * nkb / parts);
+      it.kb_hi = (int)((int64_t)(it.part + 1) * nkb / parts);
+    }
+    it.m0 = tile_m0(tile);
+    it.n0 = tile_n0(tile);
+    return it;
+  };
   constexpr uint16_t PEERS = MC > 1 ? (uint16_t)((1u << MC) - 1) : (uint16_t)1;
 
   if (threadIdx.x == 0) {
@@ -180,21 +208,42 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
       prefetch_tmap(&tmB);
       uint32_t kc = 0;
       bool ok = true;
-      for (int item = first_item; item < n_tiles && ok; item += item_step) {
-        const int m0 = tile_m0(item), n0 = tile_n0(item);
-        for (int kb = 0; kb < nkb; ++kb, ++kc) {
-          const int s = kc % S;
-          if (!mbar_wait(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
-            ok = false;
-            break;
+      if constexpr (!SPLIT) {
+        for (int item = first_item; item < n_tiles && ok; item += item_step) {
+          const int m0 = tile_m0(item), n0 = tile_n0(item);
+          for (int kb = 0; kb < nkb; ++kb, ++kc) {
+            const int s = kc % S;
+            if (!mbar_wait(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(full(s), C::STAGE_BYTES);
+            tma_load_2d(sbase + s * C::STAGE_BYTES, &tmA, full(s), kb * BK, m0);
+            if (MC > 1)
+              tma_load_2d_mc(sbase + s * C::STAGE_BYTES + A_BYTES + rank * (C::B_BYTES / MC), &tmB, full(s), kb * BK,
+                             n0 + rank * (BN / MC), PEERS);
+            else
+              tma_load_2d(sbase + s * C::STAGE_BYTES + A_BYTES, &tmB, full(s), kb * BK, n0);
           }
-          mbar_expect_tx(full(s), C::STAGE_BYTES);
-          tma_load_2d(sbase + s * C::STAGE_BYTES, &tmA, full(s), kb * BK, m0);
-          if (MC > 1)
-            tma_load_2d_mc(sbase + s * C::STAGE_BYTES + A_BYTES + rank * (C::B_BYTES / MC), &tmB, full(s), kb * BK,
-                           n0 + rank * (BN / MC), PEERS);
-          else
-            tma_load_2d(sbase + s * C::STAGE_BYTES + A_BYTES, &tmB, full(s), kb * BK, n0);
+        }
+      } else {
+        for (int item = first_item; item < n_items && ok; item += item_step) {
+          const Item it = decode(item);
+          const int m0 = it.m0, n0 = it.n0;
+          for (int kb = it.kb_lo; kb < it.kb_hi; ++kb, ++kc) {
+            const int s = kc % S;
+            if (!mbar_wait(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(full(s), C::STAGE_BYTES);
+            tma_load_2d(sbase + s * C::STAGE_BYTES, &tmA, full(s), kb * BK, m0);
+            if (MC > 1)
+              tma_load_2d_mc(sbase + s * C::STAGE_BYTES + A_BYTES + rank * (C::B_BYTES / MC), &tmB, full(s), kb * BK,
+                             n0 + rank * (BN / MC), PEERS);
+            else
+              tma_load_2d(sbase + s * C::STAGE_BYTES + A_BYTES, &tmB, full(s), kb * BK, n0);
+          }
         }
       }
       if (!ok) {  // let copies still in flight land before the CTA exits
@@ -208,8 +257,15 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
       constexpr uint32_t idesc = idesc_bf16(BM, BN);
       uint32_t kc = 0, cc = 0;
       bool ok = true;
-      for (int item = first_item; item < n_tiles && ok; item += item_step) {
-        for (int ch = 0; ch < nchunks && ok; ++ch, ++cc) {
+      for (int item = first_item; item < (SPLIT ? n_items : n_tiles) && ok; item += item_step) {
+        int kb_lo = 0, kb_hi = nkb, nch = nchunks;
+        if constexpr (SPLIT) {
+          const Item it = decode(item);
+          kb_lo = it.kb_lo;
+          kb_hi = it.kb_hi;
+          nch = (kb_hi - kb_lo + KCHUNK_BLOCKS - 1) / KCHUNK_BLOCKS;
+        }
+        for (int ch = 0; ch < nch && ok; ++ch, ++cc) {
           const int buf = cc & 1;
           if (!mbar_wait(cempty(buf), ((cc >> 1) & 1) ^ 1, ws, abort_flag)) {
             ok = false;
@@ -217,8 +273,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d = tmem + buf * BN;
-          const int kb0 = ch * KCHUNK_BLOCKS;
-          const int kb1 = min(nkb, kb0 + KCHUNK_BLOCKS);
+          const int kb0 = kb_lo + ch * KCHUNK_BLOCKS;
+          const int kb1 = min(kb_hi, kb0 + KCHUNK_BLOCKS);
           for (int kb = kb0; kb < kb1; ++kb, ++kc) {
             const int s = kc % S;
             if (!mbar_wait(full(s), (kc / S) & 1, ws, abort_flag)) {
@@ -250,15 +306,37 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
     const int half = e >> 2;       // which CW-column part of the tile
     uint32_t cc = 0;
     bool ok = true;
-    for (int item = first_item; item < n_tiles && ok; item += item_step) {
-      const int m0 = tile_m0(item), n0 = tile_n0(item);
+    for (int item = first_item; item < (SPLIT ? n_items : n_tiles) && (SPLIT || ok); item += item_step) {
+      int m0, n0, nch = nchunks;
+      Item it;
+      if constexpr (SPLIT) {
+        it = decode(item);
+        m0 = it.m0;
+        n0 = it.n0;
+        nch = (it.kb_hi - it.kb_lo + KCHUNK_BLOCKS - 1) / KCHUNK_BLOCKS;
+        if (!ok) {  // aborted: still arrive on split tickets so that every count returns to zero
+          if (it.part >= 0) {
+            __syncwarp();
+            uint32_t old = 0;
+            if (lane == 0) old = atomicAdd(ws_u32(ws, WS_SPLIT_TICKETS) + it.slot * C::EPI_WARPS + e, 1u);
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (lane == 0 && old == (uint32_t)(parts - 1)) ws_u32(ws, WS_SPLIT_TICKETS)[it.slot * C::EPI_WARPS + e] = 0;
+          }
+          continue;
+        }
+      } else {
+        m0 = tile_m0(item);
+        n0 = tile_n0(item);
+      }
       constexpr int CW = C::CW;
       int acc[CW];
 #pragma unroll
       for (int i = 0; i < CW; ++i) acc[i] = 0;
-      for (int ch = 0; ch < nchunks; ++ch, ++cc) {
+      for (int ch = 0; ch < nch; ++ch, ++cc) {
         const int buf = cc & 1;
-        if (!mbar_wait(cfull(buf), (cc >> 1) & 1, ws, abort_flag)) {
+        // SPLIT: a warp-uniform outcome, as the tickets below are warp-synchronous
+        const bool got = mbar_wait(cfull(buf), (cc >> 1) & 1, ws, abort_flag);
+        if (!(SPLIT ? __all_sync(0xffffffffu, got) : got)) {
           ok = false;
           break;
         }
@@ -275,7 +353,58 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(cempty(buf));
       }
-      if (!ok) break;
+      if constexpr (SPLIT) {
+        if (it.part >= 0) {
+          // split part: publish this warp's 32 x CW int32 partial sums, then take a ticket;
+          // the last of the `parts` arrivals adds the others' sums (exact) and stores the
+          // tile.  Region layout [column group of 8][lane][8]: each warp-wide 256-bit access
+          // covers 1 KB of contiguous memory.
+          uint32_t* ticket = ws_u32(ws, WS_SPLIT_TICKETS) + it.slot * C::EPI_WARPS + e;
+          int32_t* partials = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + WS_SPLIT_PARTIALS);
+          auto region = [&](int part) {
+            return partials + ((size_t)(it.slot * parts + part) * C::EPI_WARPS + e) * 32 * CW + lane * 8;
+          };
+          if (ok) {
+            int32_t* mine = region(it.part);
+#pragma unroll
+            for (int c = 0; c < CW / 8; ++c) {
+              U8x32 o;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o.w[i] = (uint32_t)acc[c * 8 + i];
+              st256(mine + c * 256, o);
+            }
+          }
+          __threadfence();
+          __syncwarp();
+          uint32_t old = 0;
+          if (lane == 0) old = atomicAdd(ticket, 1u);
+          old = __shfl_sync(0xffffffffu, old, 0);
+          if (old != (uint32_t)(parts - 1)) continue;  // another part finishes this region
+          if (lane == 0) *ticket = 0;
+          if (!ok) continue;
+          __threadfence();
+          for (int p = 0; p < parts; ++p) {
+            if (p == it.part) continue;
+            const int32_t* other = region(p);
+#pragma unroll
+            for (int c = 0; c < CW / 8; ++c) {
+              const int4 v0 = __ldcg(reinterpret_cast<const int4*>(other + c * 256));
+              const int4 v1 = __ldcg(reinterpret_cast<const int4*>(other + c * 256 + 4));
+              acc[8 * c] += v0.x;
+              acc[8 * c + 1] += v0.y;
+              acc[8 * c + 2] += v0.z;
+              acc[8 * c + 3] += v0.w;
+              acc[8 * c + 4] += v1.x;
+              acc[8 * c + 5] += v1.y;
+              acc[8 * c + 6] += v1.z;
+              acc[8 * c + 7] += v1.w;
+            }
+          }
+        }
+        if (!ok) continue;
+      } else {
+        if (!ok) break;
+      }
       const int row = m0 + q * 32 + lane;
       const int col0 = n0 + half * CW;
       if (row < M && col0 < N) {
@@ -346,10 +475,21 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
   if (MC > 1) cluster_sync();  // no peer may still multicast into, or arrive on, this CTA
 }
 
+// DIT6_INT8_TC_SPLIT=0 turns the split-K tail off (for comparisons and tests).
+static bool split_tail_enabled() {
+  const char* e = getenv("DIT6_INT8_TC_SPLIT");
+  return !(e && e[0] == '0');
+}
+
+template <int BN, int MC, bool GELU, bool SPLIT>
+dit_status launch_k(const CUtensorMap& ta, const CUtensorMap& tb, const float* a_scale, const float* b_scale,
+                    int64_t m, int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
+                    void* ws, cudaStream_t st, int tail_base, int parts, int64_t items);
+
 template <int BN, int MC, bool GELU>
 dit_status launch(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
                   int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
-                  void* ws, cudaStream_t st) {
+                  void* ws, size_t ws_bytes, cudaStream_t st) {
   using C = Cfg<BN>;
   CUtensorMap ta, tb;
   if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(a), (uint64_t)k, (uint64_t)m,
@@ -357,7 +497,45 @@ dit_status launch(const void* a, const float* a_scale, const void* b, const floa
       !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(b), (uint64_t)k, (uint64_t)n,
                       (uint64_t)k * 2, BK, BN / MC, CU_TENSOR_MAP_SWIZZLE_128B))
     return DIT_ERR_CUDA;
-  auto kern = k_gemm_int8_tc<BN, MC, GELU>;
+  const int64_t tiles = (((m + BM - 1) / BM + MC - 1) / MC) * ((n + BN - 1) / BN);
+  if (tiles > 0x7fffffff / 8) return DIT_ERR_UNSUPPORTED;
+  // Split-K tail: the R tiles of the last, partial wave become R x P items of nkb / P k-blocks
+  // each, so that the wave keeps more SMs busy.  Only for deep K (>= 4096): the partial-sum
+  // exchange and the final epilogue are not split, and on GB300 they cost more than the idle
+  // SMs of a short tile's last wave (measured on the CogVideoX-2B shapes).  Needs
+  // R <= SMs / 2 and room for the R x P partial-sum slots and tickets in the workspace.
+  int tail_base = (int)tiles, parts = 1;
+  if (BN == 256 && MC == 1 && k >= 4096 && split_tail_enabled()) {
+    const int64_t g = num_sms();
+    const int64_t r = tiles % g, nkb = (k + BK - 1) / BK;
+    const int64_t slot_bytes = (int64_t)BM * BN * 4;
+    int64_t p = r > 0 ? g / r : 1;
+    if (p > 4) p = 4;
+    if (p > nkb / 2) p = nkb / 2;
+    while (p > 1 && (r * p * slot_bytes > (int64_t)(ws_bytes - WS_SPLIT_PARTIALS) ||
+                     r * C::EPI_WARPS > WS_SPLIT_MAX_TICKETS))
+      --p;
+    if (p > 1) {
+      tail_base = (int)(tiles - r);
+      parts = (int)p;
+    }
+  }
+  const int64_t items = tail_base + (tiles - tail_base) * parts;
+  if constexpr (BN == 256 && MC == 1) {
+    if (parts > 1)
+      return launch_k<BN, MC, GELU, true>(ta, tb, a_scale, b_scale, m, n, k, bias, y, epi, acc_out, ws, st,
+                                          tail_base, parts, items);
+  }
+  return launch_k<BN, MC, GELU, false>(ta, tb, a_scale, b_scale, m, n, k, bias, y, epi, acc_out, ws, st,
+                                       tail_base, parts, items);
+}
+
+template <int BN, int MC, bool GELU, bool SPLIT>
+dit_status launch_k(const CUtensorMap& ta, const CUtensorMap& tb, const float* a_scale, const float* b_scale,
+                    int64_t m, int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
+                    void* ws, cudaStream_t st, int tail_base, int parts, int64_t items) {
+  using C = Cfg<BN>;
+  auto kern = k_gemm_int8_tc<BN, MC, GELU, SPLIT>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
@@ -366,7 +544,6 @@ dit_status launch(const void* a, const float* a_scale, const void* b, const floa
       return DIT_ERR_CUDA;
     attr_done = true;
   }
-  const int64_t items = (((m + BM - 1) / BM + MC - 1) / MC) * ((n + BN - 1) / BN);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(C::THREADS);
@@ -388,7 +565,7 @@ dit_status launch(const void* a, const float* a_scale, const void* b, const floa
   if (grid > items * MC) grid = items * MC;
   cfg.gridDim = dim3((unsigned)grid);
   if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, epi, acc_out,
-                         ws, MC > 1 ? 0 : test_stall()) != cudaSuccess)
+                         ws, MC > 1 ? 0 : test_stall(), tail_base, parts) != cudaSuccess)
     return DIT_ERR_CUDA;
   return DIT_OK;
 }
@@ -397,15 +574,15 @@ dit_status launch(const void* a, const float* a_scale, const void* b, const floa
 
 dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
                         int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
-                        void* ws, cudaStream_t st) {
+                        void* ws, size_t ws_bytes, cudaStream_t st) {
   const char* e = getenv("DIT6_INT8_TC_BN");
   const char* c = getenv("DIT6_INT8_TC_CLUSTER");
   const int bn = e ? atoi(e) : 256;
   const int mc = c ? atoi(c) : 1;
   const bool g = (epi & EPI_GELU) != 0;
 #define DIT6_I8TC(BN_, MC_)                                                                          \
-  return g ? i8tc::launch<BN_, MC_, true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st) \
-           : i8tc::launch<BN_, MC_, false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
+  return g ? i8tc::launch<BN_, MC_, true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, ws_bytes, st) \
+           : i8tc::launch<BN_, MC_, false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, ws_bytes, st)
   if (bn == 128) DIT6_I8TC(128, 1);
   if (bn == 192) DIT6_I8TC(192, 1);
   if (mc == 2) DIT6_I8TC(256, 2);

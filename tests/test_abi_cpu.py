@@ -64,6 +64,7 @@ def test_sf_index_matches_oracle_layout(L):
 
 def test_host_argument_validation_without_device_work(L):
     nul = None
+    wsb = L.dit_workspace_bytes()
     fake_misaligned = ctypes.c_void_p(0x1001)
     ws = ctypes.c_void_p(0x2000)
     # null pointers, bad sizes, unsupported shapes and misalignment are rejected on the host
@@ -72,21 +73,21 @@ def test_host_argument_validation_without_device_work(L):
     assert L.dit_hadamard_quant_int8(fake_misaligned, 1, 4, 128, 48, fake_misaligned, 2, fake_misaligned, nul) == 3
     assert L.dit_hadamard_quant_int8(fake_misaligned, 1, 4, 128, 64, fake_misaligned, 2, fake_misaligned, nul) == 2
     assert L.dit_hadamard_quant_int8(ws, 1, 4, 128, 64, ws, 0, ws, nul) == 1       # fp32 is no code container
-    assert L.dit_hadamard_quant_nvfp4(ws, 1, 4, 128, 64, nul, nul, nul, nul, ws, 65536, nul) == 1
+    assert L.dit_hadamard_quant_nvfp4(ws, 1, 4, 128, 64, nul, nul, nul, nul, ws, wsb, nul) == 1
     f = ctypes.c_float * 17
-    assert L.dit_gamma_route(fake_misaligned, fake_misaligned, 1, 10, f(), f(), f(), 17, ws, ws, ws, 65536, nul) == 1
-    assert L.dit_gamma_route(fake_misaligned, fake_misaligned, 1, 10, f(), f(), f(), 1, ws, ws, ws, 65536, nul) == 2
-    assert L.dit_qgemm_int8(fake_misaligned, ws, fake_misaligned, ws, 2, 4, 8, 100, nul, 0, ws, 1, nul, ws, 65536, nul) == 3
-    assert L.dit_qgemm_int8(ws, ws, ws, ws, 0, 4, 8, 128, nul, 0, ws, 1, nul, ws, 65536, nul) == 1
-    assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 96, nul, 0, ws, 1, ws, 65536, nul) == 3
+    assert L.dit_gamma_route(fake_misaligned, fake_misaligned, 1, 10, f(), f(), f(), 17, ws, ws, ws, wsb, nul) == 1
+    assert L.dit_gamma_route(fake_misaligned, fake_misaligned, 1, 10, f(), f(), f(), 1, ws, ws, ws, wsb, nul) == 2
+    assert L.dit_qgemm_int8(fake_misaligned, ws, fake_misaligned, ws, 2, 4, 8, 100, nul, 0, ws, 1, nul, ws, wsb, nul) == 3
+    assert L.dit_qgemm_int8(ws, ws, ws, ws, 0, 4, 8, 128, nul, 0, ws, 1, nul, ws, wsb, nul) == 1
+    assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 96, nul, 0, ws, 1, ws, wsb, nul) == 3
     assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 128, nul, 0, ws, 1, ws, 100, nul) == 1
     # an activation code outside dit_act
-    assert L.dit_qgemm_int8(ws, ws, ws, ws, 2, 4, 8, 128, nul, 5, ws, 1, nul, ws, 65536, nul) == 1
-    assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 128, nul, 2, ws, 1, ws, 65536, nul) == 1
+    assert L.dit_qgemm_int8(ws, ws, ws, ws, 2, 4, 8, 128, nul, 5, ws, 1, nul, ws, wsb, nul) == 1
+    assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 128, nul, 2, ws, 1, ws, wsb, nul) == 1
     ws2 = ctypes.c_void_p(0x4000)
-    assert L.dit_tdc_step(0, fake_misaligned, fake_misaligned, nul, ws, ws2, 1, 64, ws, ws, ws, 65536, nul) == 2
-    assert L.dit_tdc_step(0, ws, ws, nul, ws, ws, 1, 64, ws, ws, ws, 65536, nul) == 1   # d1 == d_new
-    assert L.dit_tdc_step(7, ws, ws, nul, ws, ws, 1, 64, ws, ws, ws, 65536, nul) == 1
+    assert L.dit_tdc_step(0, fake_misaligned, fake_misaligned, nul, ws, ws2, 1, 64, ws, ws, ws, wsb, nul) == 2
+    assert L.dit_tdc_step(0, ws, ws, nul, ws, ws, 1, 64, ws, ws, ws, wsb, nul) == 1   # d1 == d_new
+    assert L.dit_tdc_step(7, ws, ws, nul, ws, ws, 1, 64, ws, ws, ws, wsb, nul) == 1
 
 
 def test_host_tdc_state_machine_matches_oracle(L):

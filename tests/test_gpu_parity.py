@@ -304,6 +304,36 @@ def test_gelu_epilogue_elementwise_error_bound(container, ws):
     assert host(y)[x == 0].tolist() == [0.0] * int((x == 0).sum())
 
 
+@pytest.mark.parametrize("m,n,k", [(2560, 1920, 4096), (17776, 1920, 7680), (640, 1920, 12288), (300, 384, 4160)])
+def test_int8_gemm_split_tail_bit_exact(m, n, k, ws, monkeypatch):
+    """The split-K tail (K >= 4096: last partial wave of 128 x 256 tiles spread over idle SMs, int32
+    partial sums added by the last part) gives the same accumulators and outputs, bit for bit,
+    as whole tiles; sampled rows also match the int64 oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = -(-m // 128) * -(-n // 256)
+    if not 0 < tiles % sms <= sms // 2:
+        pytest.skip(f"{tiles} tiles on {sms} SMs: no split tail for this shape")
+    g = synth.rng(m + n + k + 1)
+    a = g.integers(-127, 128, (m, k)).astype(np.int8)
+    b = g.integers(-127, 128, (n, k)).astype(np.int8)
+    sa = (g.random(m) * 0.01).astype(np.float32)
+    sb = (g.random(n) * 0.01).astype(np.float32)
+    ta, tb = _int8_dev(a, torch.bfloat16), _int8_dev(b, torch.bfloat16)
+    outs = {}
+    for split in ("0", "1"):
+        monkeypatch.setenv("DIT6_INT8_TC_SPLIT", split)
+        acc = torch.empty(m, n, dtype=torch.int32, device="cuda")
+        y = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+        dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws, acc_debug=acc, act=dit.ACT_GELU_ERF)
+        _status_clean(ws)
+        outs[split] = (acc, y)
+    assert torch.equal(outs["0"][0], outs["1"][0])
+    assert torch.equal(outs["0"][1].view(torch.int16), outs["1"][1].view(torch.int16))
+    rows = np.unique(np.concatenate([synth.rng(m).choice(m, 24, replace=False), [m - 1]]))
+    ref = D.gemm_int8_acc(a[rows], b)
+    assert np.array_equal(host(outs["1"][0][torch.from_numpy(rows).cuda()]).astype(np.int64), ref)
+
+
 def _adversarial_int8(m, n, k, seed):
     """Operands that push every exact-chunk partial sum towards its 2^24 bound, mix huge and
     unit products after a large running sum, and cancel."""
@@ -487,14 +517,16 @@ def test_tdc_chained_blocks_full_size(ws):
     _status_clean(ws)
 
 
-@pytest.mark.parametrize("route", ["nvfp4", "int8"])
+@pytest.mark.parametrize("route", ["nvfp4", "int8", "int8_split"])
 def test_gemm_bounded_wait_reports_timeout_and_recovers(route, monkeypatch):
     """A GEMM whose producer issues no loads (test hook): the consumers' bounded waits run out
     after ~1 s, the kernel records DIT_ERR_TIMEOUT in the workspace status word, frees its
     tensor memory and exits; the next normal call on the same context is correct."""
     import time
     ws2 = dit.workspace()
-    m, n, k = 256, 256, 128
+    # int8_split: 2 tiles over 4096-deep K, split into 4 parts each; the aborted parts still
+    # arrive on their tickets, so the next call's split finds them at zero
+    m, n, k = (256, 256, 4096) if route == "int8_split" else (256, 256, 128)
     g = synth.rng(55)
     if route == "nvfp4":
         qa, qb, A, B = _nvfp4_operands(m, n, k, seed=56)
