@@ -475,6 +475,355 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
   if (MC > 1) cluster_sync();  // no peer may still multicast into, or arrive on, this CTA
 }
 
+// ------------------------------------------------------------------------------------------
+// CTA-pair variant: tcgen05.mma.cta_group::2, 256 x 256 tiles over two SMs.
+//
+// Each CTA of a 2-CTA cluster stages its own 128 rows of A and its own 128-row half of the
+// tile's B (N split across the pair), so every SM moves 32 KB per 64-deep K step instead of
+// 48 KB for the same MMA work per SM as the single-CTA 128 x 256 tile.  The even CTA (leader)
+// issues the pair's MMAs; they read both CTAs' shared memory at the same offsets and write each
+// CTA's 128 accumulator rows into that CTA's tensor memory.  Both producers signal the leader's
+// full barrier (TMA .cta_group::2), whose expected byte count covers the pair; MMA completion
+// is multicast to both CTAs' empty and chunk-full barriers; both epilogues release a drained
+// chunk buffer by arriving on the leader's chunk-empty barrier.  Tensor memory is allocated and
+// freed by one warp in each CTA together (cta_group::2).  Exactness and the chunked int32
+// accumulation are those of the single-CTA kernel.
+// ------------------------------------------------------------------------------------------
+struct PairCfg {
+  static constexpr int STAGES = 6;
+  static constexpr int B_BYTES = 128 * BK * 2;                 // this CTA's half of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;        // 32 KB
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int CW = 128;
+  static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int TMEM_COLS = 512;                         // two 256-column chunk buffers
+};
+
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, "
+      "p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait with cluster-scope acquire (arrivals come from the peer CTA as well)
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, void* ws, volatile int* abort) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+        raise_status(ws, DIT_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+// TMA load into this CTA's shared memory whose completed bytes count on `bar_cluster`, an
+// mbarrier of either CTA of the pair (shared::cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], "
+      "[%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+template <bool GELU>
+__global__ void __launch_bounds__(PairCfg::THREADS, 1)
+    k_gemm_int8_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N, int K,
+                     const float* __restrict__ bias, void* __restrict__ y, int epi, int32_t* __restrict__ acc_out,
+                     void* ws, int stall) {
+  using P = PairCfg;
+  constexpr int S = P::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * P::STAGE_BYTES);
+  // bars: full[S], empty[S], chunk_full[2], chunk_empty[2], mma_done (same offsets in both CTAs)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t sbase = smem_u32(smem);
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + S + s); };
+  auto cfull = [&](int b) { return smem_u32(bars + 2 * S + b); };
+  auto cempty = [&](int b) { return smem_u32(bars + 2 * S + 2 + b); };
+  const uint32_t mma_done = smem_u32(bars + 2 * S + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
+  const int n_tiles_n = (N + 255) / 256;
+  const int n_items = ((M + 255) / 256) * n_tiles_n;
+  const int first_item = blockIdx.x >> 1, item_step = gridDim.x >> 1;
+  auto tile_m0 = [&](int item) { return (item / n_tiles_n) * 256; };
+  auto tile_n0 = [&](int item) { return (item % n_tiles_n) * 256; };
+  const int nkb = (K + BK - 1) / BK;
+  const int nchunks = (nkb + KCHUNK_BLOCKS - 1) / KCHUNK_BLOCKS;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(cfull(b), 1);
+      mbar_init(cempty(b), 2 * P::EPI_WARPS);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA signal
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(P::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {  // ------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0 && !stall) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      uint32_t kc = 0;
+      bool ok = true;
+      for (int item = first_item; item < n_items && ok; item += item_step) {
+        const int m0 = tile_m0(item) + (int)rank * 128, n0 = tile_n0(item) + (int)rank * 128;
+        for (int kb = 0; kb < nkb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait_cl(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_expect_tx(full(s), 2 * P::STAGE_BYTES);  // both CTAs' bytes
+          const uint32_t fb = mapa_rank(full(s), 0);
+          tma_load_2d_pair(sbase + s * P::STAGE_BYTES, &tmA, fb, kb * BK, m0);
+          tma_load_2d_pair(sbase + s * P::STAGE_BYTES + A_BYTES, &tmB, fb, kb * BK, n0);
+        }
+      }
+      if (!ok && rank == 0) {  // the leader's full barriers count both CTAs' copies in flight
+        volatile int no_abort = 0;
+        const uint32_t first = kc > (uint32_t)S ? kc - S : 0;
+        for (uint32_t c = first; c < kc; ++c) mbar_wait_cl(full(c % S), (c / S) & 1, ws, &no_abort);
+      }
+    }
+  } else if (warp == 1) {  // ----------------------------------------- MMA issuer (leader only)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16(256, 256);
+      uint32_t kc = 0, cc = 0;
+      bool ok = true;
+      for (int item = first_item; item < n_items && ok; item += item_step) {
+        for (int ch = 0; ch < nchunks && ok; ++ch, ++cc) {
+          const int buf = cc & 1;
+          if (!mbar_wait_cl(cempty(buf), ((cc >> 1) & 1) ^ 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + buf * 256;
+          const int kb0 = ch * KCHUNK_BLOCKS;
+          const int kb1 = min(nkb, kb0 + KCHUNK_BLOCKS);
+          for (int kb = kb0; kb < kb1; ++kb, ++kc) {
+            const int s = kc % S;
+            if (!mbar_wait_cl(full(s), (kc / S) & 1, ws, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_s = sbase + s * P::STAGE_BYTES, b_s = a_s + A_BYTES;
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j)
+              tc_mma_pair(d, desc_sw128(a_s + j * 32), desc_sw128(b_s + j * 32), idesc,
+                          (kb > kb0 || j > 0) ? 1u : 0u);
+            tc_commit_pair_mc(empty(s), 3);
+          }
+          if (ok) tc_commit_pair_mc(cfull(buf), 3);
+        }
+      }
+      tc_commit_pair(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait_cl(mma_done, 0, ws, &no_abort);  // every issued MMA has completed
+    }
+    __syncwarp();
+  } else {  // ------------------------------------------------------ epilogue warps (both CTAs)
+    const int e = warp - 2;
+    const int q = warp & 3;   // tensor-memory lane quarter of this warp
+    const int half = e >> 2;  // which 128-column half of the 256-column tile
+    const uint32_t cempty_leader[2] = {mapa_rank(cempty(0), 0), mapa_rank(cempty(1), 0)};
+    uint32_t cc = 0;
+    bool ok = true;
+    for (int item = first_item; item < n_items && ok; item += item_step) {
+      const int m0 = tile_m0(item) + (int)rank * 128, n0 = tile_n0(item);
+      constexpr int CW = P::CW;
+      int acc[CW];
+#pragma unroll
+      for (int i = 0; i < CW; ++i) acc[i] = 0;
+      for (int ch = 0; ch < nchunks; ++ch, ++cc) {
+        const int buf = cc & 1;
+        if (!mbar_wait_cl(cfull(buf), (cc >> 1) & 1, ws, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + half * CW;
+#pragma unroll
+        for (int c = 0; c < CW / 16; ++c) {
+          uint32_t r[16];
+          tc_ld16(base + c * 16, r);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[c * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(cempty_leader[buf]);
+      }
+      if (!ok) break;
+      const int row = m0 + q * 32 + lane;
+      const int col0 = n0 + half * CW;
+      if (row < M && col0 < N) {
+        const float sa = a_scale[row];
+        const int64_t off = (int64_t)row * N + col0;
+#pragma unroll
+        for (int c = 0; c < CW / 16; ++c) {
+          const int cb = col0 + c * 16;
+          if (cb >= N) break;
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = cb + i < N ? cb + i : N - 1;
+            v[i] = __fmul_rn(__fmul_rn((float)acc[c * 16 + i], sa), b_scale[col]);
+            if (bias) v[i] = __fadd_rn(v[i], bias[col]);
+            if (GELU) v[i] = epi_act(v[i], EPI_GELU);
+          }
+          if (cb + 16 <= N && (N % 16) == 0) {
+            if (epi & EPI_BF16) {
+              U8x32 o;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o.w[i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
+              st256(reinterpret_cast<uint16_t*>(y) + off + c * 16, o);
+            } else {
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                U8x32 o;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o.w[i] = __float_as_uint(v[8 * b + i]);
+                st256(reinterpret_cast<float*>(y) + off + c * 16 + 8 * b, o);
+              }
+            }
+            if (acc_out) {
+#pragma unroll
+              for (int b = 0; b < 2; ++b) {
+                U8x32 o;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o.w[i] = (uint32_t)acc[c * 16 + 8 * b + i];
+                st256(acc_out + off + c * 16 + 8 * b, o);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              if (cb + i >= N) continue;
+              if (epi & EPI_BF16)
+                reinterpret_cast<__nv_bfloat16*>(y)[off + c * 16 + i] = __float2bfloat16_rn(v[i]);
+              else
+                reinterpret_cast<float*>(y)[off + c * 16 + i] = v[i];
+              if (acc_out) acc_out[off + c * 16 + i] = acc[c * 16 + i];
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  cluster_sync();  // no MMA, copy or arrival of either CTA still touches the other
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(P::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+template <bool GELU>
+dit_status launch_pair(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
+                       int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out, void* ws,
+                       cudaStream_t st) {
+  using P = PairCfg;
+  CUtensorMap ta, tb;
+  if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(a), (uint64_t)k, (uint64_t)m,
+                      (uint64_t)k * 2, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(b), (uint64_t)k, (uint64_t)n,
+                      (uint64_t)k * 2, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return DIT_ERR_CUDA;
+  auto kern = k_gemm_int8_pair<GELU>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES) != cudaSuccess)
+      return DIT_ERR_CUDA;
+    attr_done = true;
+  }
+  const int64_t items = ((m + 255) / 256) * ((n + 255) / 256);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(P::THREADS);
+  cfg.dynamicSmemBytes = P::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.gridDim = dim3((unsigned)(num_sms() / 2 * 2));
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return DIT_ERR_CUDA;
+  int64_t pairs = clusters;
+  if (pairs > items) pairs = items;
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, epi, acc_out, ws,
+                         test_stall()) != cudaSuccess)
+    return DIT_ERR_CUDA;
+  return DIT_OK;
+}
+
 // DIT6_INT8_TC_SPLIT=0 turns the split-K tail off (for comparisons and tests).
 static bool split_tail_enabled() {
   const char* e = getenv("DIT6_INT8_TC_SPLIT");
@@ -580,6 +929,13 @@ dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, cons
   const int bn = e ? atoi(e) : 256;
   const int mc = c ? atoi(c) : 1;
   const bool g = (epi & EPI_GELU) != 0;
+  // Default: the CTA-pair kernel (256 x 256 tiles over two SMs).  DIT6_INT8_TC_PAIR=0, or an
+  // explicit single-CTA tile (DIT6_INT8_TC_BN / DIT6_INT8_TC_CLUSTER), selects the single-CTA
+  // kernel, which also carries the split-K tail.
+  const char* pr = getenv("DIT6_INT8_TC_PAIR");
+  if (!(pr && pr[0] == '0') && !e && !c)
+    return g ? i8tc::launch_pair<true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
+             : i8tc::launch_pair<false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
 #define DIT6_I8TC(BN_, MC_)                                                                          \
   return g ? i8tc::launch<BN_, MC_, true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, ws_bytes, st) \
            : i8tc::launch<BN_, MC_, false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, ws_bytes, st)

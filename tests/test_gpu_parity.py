@@ -251,11 +251,14 @@ def _int8_dev(a, container):
 
 
 @pytest.mark.parametrize("container,bn", [(torch.int8, None), (torch.bfloat16, "192"), (torch.bfloat16, "128"),
-                                          (torch.bfloat16, "256"), (torch.bfloat16, "256c2")])
+                                          (torch.bfloat16, "256"), (torch.bfloat16, "256c2"), (torch.bfloat16, "pair")])
 @pytest.mark.parametrize("m,n,k", [(256, 512, 128), (300, 384, 1920), (129, 256, 7680), (1, 8, 16),
                                    (200, 136, 208), (700, 5760 // 10, 2112)])
 def test_int8_gemm_exact_accumulators(m, n, k, container, bn, ws, monkeypatch):
-    if bn:
+    if bn == "pair":
+        monkeypatch.setenv("DIT6_INT8_TC_PAIR", "1")
+    elif bn:
+        monkeypatch.setenv("DIT6_INT8_TC_PAIR", "0")
         monkeypatch.setenv("DIT6_INT8_TC_BN", bn[:3])
         monkeypatch.setenv("DIT6_INT8_TC_CLUSTER", "2" if bn.endswith("c2") else "1")
     g = synth.rng(m * n + k)
@@ -320,6 +323,7 @@ def test_int8_gemm_split_tail_bit_exact(m, n, k, ws, monkeypatch):
     sb = (g.random(n) * 0.01).astype(np.float32)
     ta, tb = _int8_dev(a, torch.bfloat16), _int8_dev(b, torch.bfloat16)
     outs = {}
+    monkeypatch.setenv("DIT6_INT8_TC_PAIR", "0")   # the single-CTA kernel carries the split
     for split in ("0", "1"):
         monkeypatch.setenv("DIT6_INT8_TC_SPLIT", split)
         acc = torch.empty(m, n, dtype=torch.int32, device="cuda")
@@ -349,10 +353,14 @@ def _adversarial_int8(m, n, k, seed):
     return a, b
 
 
-@pytest.mark.parametrize("cluster", ["1", "2"])
+@pytest.mark.parametrize("cluster", ["1", "2", "pair"])
 @pytest.mark.parametrize("k", [1024, 1040, 2048, 7680, 12288])
 def test_int8_gemm_bf16_pipe_exact_at_the_bound(k, cluster, ws, monkeypatch):
-    monkeypatch.setenv("DIT6_INT8_TC_CLUSTER", cluster)
+    if cluster == "pair":
+        monkeypatch.setenv("DIT6_INT8_TC_PAIR", "1")
+    else:
+        monkeypatch.setenv("DIT6_INT8_TC_PAIR", "0")
+        monkeypatch.setenv("DIT6_INT8_TC_CLUSTER", cluster)
     """Extreme codes (+-127 everywhere, totals up to 12288 * 127^2 ~ 2^27.6): the chunked fp32
     accumulation on the bf16 tensor pipe still gives the exact int32 accumulators."""
     m, n = 200, 392
@@ -517,7 +525,7 @@ def test_tdc_chained_blocks_full_size(ws):
     _status_clean(ws)
 
 
-@pytest.mark.parametrize("route", ["nvfp4", "int8", "int8_split"])
+@pytest.mark.parametrize("route", ["nvfp4", "int8", "int8_split", "int8_pair"])
 def test_gemm_bounded_wait_reports_timeout_and_recovers(route, monkeypatch):
     """A GEMM whose producer issues no loads (test hook): the consumers' bounded waits run out
     after ~1 s, the kernel records DIT_ERR_TIMEOUT in the workspace status word, frees its
@@ -539,6 +547,7 @@ def test_gemm_bounded_wait_reports_timeout_and_recovers(route, monkeypatch):
         ref = D.gemm_int8(a, sa, b, sb)
         ta, tb = _int8_dev(a, torch.bfloat16), _int8_dev(b, torch.bfloat16)
         call = lambda y: dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws2)
+    monkeypatch.setenv("DIT6_INT8_TC_PAIR", "1" if route == "int8_pair" else "0")
     y = torch.zeros(m, n, dtype=torch.float32, device="cuda")
     monkeypatch.setenv("DIT6_TEST_STALL_PRODUCER", "1")
     t0 = time.time()
