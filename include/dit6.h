@@ -53,7 +53,7 @@ typedef enum { DIT_TDC_COMMIT = 0, DIT_TDC_SKIP = 1 } dit_tdc_mode;
 /* Activation applied in the GEMM epilogue after the bias: none, or GELU in its erf form
  * x * Phi(x) (the FFN activation between the up and down projections of the CogVideoX-shaped
  * block), computed in fp32 before the output is stored, with Phi from the erf approximation
- * of Abramowitz & Stegun 7.1.26 (absolute error of Phi <= 7.5e-8 + fp32 rounding). */
+ * of Abramowitz & Stegun 7.1.28: |computed - x Phi(x)| <= 2.5e-6 |x|. */
 typedef enum { DIT_ACT_NONE = 0, DIT_ACT_GELU_ERF = 1 } dit_act;
 
 #define DIT_MAX_LAYERS 16
@@ -181,6 +181,28 @@ dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a
                            int64_t m, int64_t n, int64_t k, const float* bias, dit_act act,
                            void* y, dit_dtype y_dt, void* ws, size_t ws_bytes,
                            dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * NVFP4 GEMM with fused epilogue quantisation for the next NVFP4 layer (FFN up -> down).
+ * [EN] 2.A Mechanism 2-3 (online block Hadamard before quantisation), applied to the
+ * activation the GEMM produces instead of in a separate pass.
+ *
+ * Z = act(dit_qgemm_nvfp4 product (+ bias)) rounded to bf16 (the values y would hold);
+ * q_codes / q_sf = the NVFP4 encoding of the block Hadamard transform of Z (blocks of
+ * hblock along n) with the CALLER-SUPPLIED tensor scale *q_scale_in: byte for byte what
+ * dit_hadamard_quant_nvfp4(Z, hblock, ..., tensor_scale_in = q_scale_in) writes, layouts
+ * included, so they feed dit_qgemm_nvfp4 as its A operand with a_gs = q_scale_in.
+ * *q_scale_next = max|H Z| / (6 * 448): the tensor scale the unfused quantiser would derive
+ * from this Z (for the next call; a supplied scale below it saturates the largest values).
+ * y : device bf16 [m x n] or NULL (Z not stored).  hblock in {16, 32, 64}; n % 64 == 0;
+ * k % 64 == 0; q_codes [m x n/2] and q_sf (dit_sf_bytes(m, n)) device, 32-byte aligned.
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_qgemm_nvfp4_fused_quant(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
+                                       const uint8_t* b, const uint8_t* b_sf, const float* b_gs,
+                                       int64_t m, int64_t n, int64_t k, const float* bias,
+                                       dit_act act, void* y, int hblock, const float* q_scale_in,
+                                       uint8_t* q_codes, uint8_t* q_sf, float* q_scale_next,
+                                       void* ws, size_t ws_bytes, dit_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * (a7) INT8 GEMM: exact int32 accumulation, per-row x per-column dequantisation.

@@ -143,6 +143,18 @@ def qgemm_nvfp4(a, a_sf, a_gs, b, b_sf, b_gs, y, ws, bias=None, act=ACT_NONE, st
     _check(st, "dit_qgemm_nvfp4")
 
 
+def qgemm_nvfp4_fused_quant(a, a_sf, a_gs, b, b_sf, b_gs, ws, hblock, q_scale_in, q_codes, q_sf, q_scale_next,
+                            y=None, bias=None, act=ACT_NONE, stream=None):
+    """NVFP4 GEMM whose epilogue also NVFP4-quantises the block-Hadamard transform of its bf16
+    output with the supplied tensor scale q_scale_in (device float [1]) into q_codes / q_sf,
+    and writes the output's own tensor scale to q_scale_next; y (bf16) is optional."""
+    m, n, k = a.shape[0], b.shape[0], a.shape[1] * 2
+    st = lib().dit_qgemm_nvfp4_fused_quant(_p(a), _p(a_sf), _p(a_gs), _p(b), _p(b_sf), _p(b_gs), m, n, k, _p(bias),
+                                           act, _p(y), hblock, _p(q_scale_in), _p(q_codes), _p(q_sf),
+                                           _p(q_scale_next), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dit_qgemm_nvfp4_fused_quant")
+
+
 def qgemm_int8(a, a_scale, b, b_scale, y, ws, bias=None, acc_debug=None, act=ACT_NONE, stream=None):
     """a, b: int8 codes (IMMA path) or bf16-held integer codes (tcgen05 bf16 path)."""
     if a.dtype != b.dtype:

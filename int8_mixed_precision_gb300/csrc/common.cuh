@@ -74,29 +74,6 @@ __device__ __forceinline__ uint32_t f2_to_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// GEMM epilogue flags: bit 0 = bf16 output (else fp32), bit 1 = GELU (erf form) after bias
-constexpr int EPI_BF16 = 1, EPI_GELU = 2;
-
-// GELU(x) = x * Phi(x), Phi the standard normal CDF, with Phi from the rational approximation
-// of erf in Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26 (Hastings):
-// for z >= 0, erfc(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2) + e(z),
-// t = 1 / (1 + p z), |e(z)| <= 1.5e-7.  With z = |x| / sqrt 2, Phi(x) = erfc(z) / 2 for x < 0 and
-// 1 - erfc(z) / 2 otherwise, so the negative tail carries no cancellation; the absolute error
-// of Phi is <= 7.5e-8 plus fp32 rounding.  One reciprocal, one exponential and six FMAs: the
-// epilogue warps run it beside the accumulator drain.
-__device__ __forceinline__ float gelu_erf(float x) {
-  const float z = fabsf(x) * 0.70710678118654752f;
-  float t;  // 1 / (1 + p z) to ~1 ulp; the approximation's own error dominates
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, z, 1.0f)));
-  float p = fmaf(1.061405429f, t, -1.453152027f);
-  p = fmaf(p, t, 1.421413741f);
-  p = fmaf(p, t, -0.284496736f);
-  p = fmaf(p, t, 0.254829592f);
-  const float h = 0.5f * (p * t) * __expf(-z * z);   // erfc(z) / 2
-  return x * (x < 0.0f ? h : 1.0f - h);
-}
-
-__device__ __forceinline__ float epi_act(float v, int epi) { return (epi & EPI_GELU) ? gelu_erf(v) : v; }
 
 // ---------------------------------------------------------------------------------------
 // packed fp32x2 arithmetic (one instruction for two lanes, no contraction)
@@ -128,6 +105,54 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   asm("mov.b64 {%0,%1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
   return o;
 }
+
+// GEMM epilogue flags: bit 0 = bf16 output (else fp32), bit 1 = GELU (erf form) after bias
+constexpr int EPI_BF16 = 1, EPI_GELU = 2;
+
+// GELU(x) = x * Phi(x), Phi the standard normal CDF, from the approximation of erf in
+// Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.28 (Hastings):
+// for z >= 0, erfc(z) = (1 + a1 z + a2 z^2 + ... + a6 z^6)^-16 + e(z), |e(z)| <= 3e-7.
+// With z = |x| / sqrt 2, Phi(x) = erfc(z) / 2 for x < 0 and 1 - erfc(z) / 2 otherwise (no
+// cancellation in the negative tail).  One reciprocal and no exponential: the epilogues that
+// apply it are bound by the special-function unit, which the erf forms with exp(-z^2) use
+// twice per element.  Evaluated in fp32 (the 16th power amplifies the rounding of the
+// reciprocal): |computed - x Phi(x)| <= 2.5e-6 |x|, far below bf16 output resolution.
+__device__ __forceinline__ float rcp_approx(float d) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+  return r;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t r, x, y, z;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1,%2};" : "=l"(z) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(y), "l"(z));
+  float2 o;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+  return o;
+}
+__device__ __forceinline__ float2 gelu_erf2(float2 x) {
+  const float2 z = mul2(make_float2(fabsf(x.x), fabsf(x.y)), make_float2(0.70710678118654752f, 0.70710678118654752f));
+  float2 d = fma2(z, make_float2(0.0000430638f, 0.0000430638f), make_float2(0.0002765672f, 0.0002765672f));
+  d = fma2(d, z, make_float2(0.0001520143f, 0.0001520143f));
+  d = fma2(d, z, make_float2(0.0092705272f, 0.0092705272f));
+  d = fma2(d, z, make_float2(0.0422820123f, 0.0422820123f));
+  d = fma2(d, z, make_float2(0.0705230784f, 0.0705230784f));
+  d = fma2(d, z, make_float2(1.0f, 1.0f));
+  float2 r = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+  r = mul2(r, r);
+  r = mul2(r, r);
+  r = mul2(r, r);
+  r = mul2(r, r);                                        // d^-16 = erfc(z)
+  const float2 h = mul2(r, make_float2(0.5f, 0.5f));    // erfc(z) / 2
+  const float2 g = sub2(make_float2(1.0f, 1.0f), h);
+  return mul2(x, make_float2(x.x < 0.0f ? h.x : g.x, x.y < 0.0f ? h.y : g.y));
+}
+__device__ __forceinline__ float gelu_erf(float x) { return gelu_erf2(make_float2(x, 0.0f)).x; }
+
+__device__ __forceinline__ float epi_act(float v, int epi) { return (epi & EPI_GELU) ? gelu_erf(v) : v; }
+__device__ __forceinline__ float2 epi_act2(float2 v, int epi) { return (epi & EPI_GELU) ? gelu_erf2(v) : v; }
 
 // ---------------------------------------------------------------------------------------
 // In-thread fast Walsh-Hadamard transform of 64 values held as 32 pairs (2p, 2p+1).
@@ -180,6 +205,48 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   uint16_t c = (uint16_t)code;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+}
+
+// largest |v| over the pairs [p0, p0 + np)
+__device__ __forceinline__ float amax_range(const float2 (&v)[32], int p0, int np) {
+  float m = 0.f;
+#pragma unroll
+  for (int p = 0; p < 32; ++p)
+    if (p >= p0 && p < p0 + np) m = fmaxf(m, fmaxf(fabsf(v[p].x), fabsf(v[p].y)));
+  return m;
+}
+
+// NVFP4 encoding of one 64-element unit of the transformed tensor (four 16-element blocks)
+// with tensor scale s_g (six_sg = 6 s_g): per block the E4M3 scale RN(amax_b / (6 s_g)),
+// saturating; the block's values times RN(1 / (dec(scale) s_g)) rounded to E2M1.  Returns the
+// four scale codes (block g in byte g); `out` gets the 32 code bytes (element 2i low nibble).
+__device__ __forceinline__ uint32_t nvfp4_encode_unit(const float2 (&v)[32], float s_g, float six_sg,
+                                                      U8x32& out) {
+  uint32_t sfword = 0;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const float ab = amax_range(v, g * 8, 8);
+    uint32_t code = 0;
+    float inv = 0.f;
+    if (s_g > 0.f) {
+      code = e4m3_code(__fdiv_rn(ab, six_sg));
+      const float bs = __fmul_rn(e4m3_value(code), s_g);
+      inv = bs == 0.f ? 0.f : __frcp_rn(bs);
+    }
+    sfword |= code << (8 * g);
+    const float2 iv = make_float2(inv, inv);
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {  // 8 elements -> one 32-bit word of 8 codes
+      uint32_t word = 0;
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const float2 s = mul2(v[g * 8 + w * 4 + pp], iv);
+        word |= e2m1x2(s.x, s.y) << (8 * pp);
+      }
+      out.w[g * 2 + w] = inv == 0.f ? 0u : word;
+    }
+  }
+  return sfword;
 }
 
 // ---------------------------------------------------------------------------------------

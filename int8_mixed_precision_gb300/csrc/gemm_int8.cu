@@ -141,8 +141,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           v0 = __fadd_rn(v0, bias[col]);
           v1 = __fadd_rn(v1, bias[col + 1]);
         }
-        v0 = epi_act(v0, epi);
-        v1 = epi_act(v1, epi);
+        if (epi & EPI_GELU) {
+          const float2 g = gelu_erf2(make_float2(v0, v1));
+          v0 = g.x;
+          v1 = g.y;
+        }
         const int64_t off = (int64_t)row * N + col;
         if (epi & EPI_BF16)
           *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(y) + off) = f2_to_bf16x2(v0, v1);

@@ -420,7 +420,14 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
             const int col = cb + i < N ? cb + i : N - 1;
             v[i] = __fmul_rn(__fmul_rn((float)acc[c * 16 + i], sa), b_scale[col]);
             if (bias) v[i] = __fadd_rn(v[i], bias[col]);
-            if (GELU) v[i] = epi_act(v[i], EPI_GELU);
+          }
+          if (GELU) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float2 g = gelu_erf2(make_float2(v[2 * i], v[2 * i + 1]));
+              v[2 * i] = g.x;
+              v[2 * i + 1] = g.y;
+            }
           }
           if (cb + 16 <= N && (N % 16) == 0) {
             if (epi & EPI_BF16) {
@@ -730,7 +737,14 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
             const int col = cb + i < N ? cb + i : N - 1;
             v[i] = __fmul_rn(__fmul_rn((float)acc[c * 16 + i], sa), b_scale[col]);
             if (bias) v[i] = __fadd_rn(v[i], bias[col]);
-            if (GELU) v[i] = epi_act(v[i], EPI_GELU);
+          }
+          if (GELU) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float2 g = gelu_erf2(make_float2(v[2 * i], v[2 * i + 1]));
+              v[2 * i] = g.x;
+              v[2 * i + 1] = g.y;
+            }
           }
           if (cb + 16 <= N && (N % 16) == 0) {
             if (epi & EPI_BF16) {

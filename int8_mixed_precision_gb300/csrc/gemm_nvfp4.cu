@@ -231,7 +231,14 @@ __global__ void __launch_bounds__(192, 1)
         for (int i = 0; i < 32; ++i) {
           v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
           if (bias && col0 + i < N) v[i] = __fadd_rn(v[i], bias[col0 + i]);
-          v[i] = epi_act(v[i], epi);
+        }
+        if (epi & EPI_GELU) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 g = gelu_erf2(make_float2(v[2 * i], v[2 * i + 1]));
+            v[2 * i] = g.x;
+            v[2 * i + 1] = g.y;
+          }
         }
         const int64_t off = (int64_t)row * N + col0;
         if (col0 + 32 <= N && (N % 16) == 0) {
@@ -457,7 +464,14 @@ __global__ void __launch_bounds__(PCfg<BN, STAGES, ACC_BUFS>::THREADS, 1)
         for (int i = 0; i < 32; ++i) {
           v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
           if (bias) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
-          v[i] = epi_act(v[i], epi);
+        }
+        if (epi & EPI_GELU) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 g = gelu_erf2(make_float2(v[2 * i], v[2 * i + 1]));
+            v[2 * i] = g.x;
+            v[2 * i + 1] = g.y;
+          }
         }
         const int64_t off = (int64_t)row * N + col0;
         if (col0 + 32 <= N && (N % 16) == 0) {
@@ -709,7 +723,14 @@ __global__ void __launch_bounds__(RCfg::THREADS, 1)
         for (int i = 0; i < 32; ++i) {
           v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
           if (bias) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
-          v[i] = epi_act(v[i], epi);
+        }
+        if (epi & EPI_GELU) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 g = gelu_erf2(make_float2(v[2 * i], v[2 * i + 1]));
+            v[2 * i] = g.x;
+            v[2 * i + 1] = g.y;
+          }
         }
         const int64_t off = (int64_t)row * N + col0;
         if (col0 + 32 <= N && (N % 16) == 0) {
@@ -785,8 +806,11 @@ static dit_status launch_r(const CUtensorMap& ta, const CUtensorMap& tb, const u
 // the layout the 32x128b.warpx4 copy would produce), instead of tcgen05.cp on the tensor-core
 // unit.  The MMA thread waits on a per-stage "scales ready" barrier.
 // ---------------------------------------------------------------------------------------
-template <int BN, int STAGES, int CTAS>
+// ACC: tensor-memory accumulator buffers (2: the MMAs of tile t+1 run while the epilogue
+// drains tile t)
+template <int BN, int STAGES, int CTAS, int ACC = 1>
 struct SCfg {
+  static_assert(ACC == 1 || ACC == 2, "accumulator buffers");
   static constexpr int NB = BN / 128;
   static constexpr int B_BYTES = BN * BK / 2;
   static constexpr int SFA_BYTES = 4 * SF_ATOM;
@@ -794,7 +818,7 @@ struct SCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
   static constexpr int SF_COLS = 4 + 4 * NB;
-  static constexpr int SF_BASE = BN;
+  static constexpr int SF_BASE = BN * ACC;
   static constexpr int TMEM_USED = SF_BASE + STAGES * 4 * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
   static constexpr int EPI_WARPS = BN / 32;
@@ -810,27 +834,37 @@ __device__ __forceinline__ void tc_st4(uint32_t taddr, const uint4& v) {
                : "memory");
 }
 
-template <int BN, int STAGES, int CTAS>
-__global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
+// QHB > 0 (16, 32 or 64): fused epilogue quantisation.  The output Z (after bias and
+// activation, rounded to bf16 as it would be stored) is block-Hadamard transformed along N in
+// blocks of QHB and NVFP4-encoded with the given tensor scale *q_sg into q_codes / q_sf (the
+// layouts dit_hadamard_quant_nvfp4 writes, ready as the next GEMM's A operand); y (bf16) is
+// written only when non-null.  max|H Z| over the whole output is reduced through the workspace
+// and the last CTA writes *q_sg_next = max / (6 * 448), the tensor scale the unfused quantiser
+// would derive from this Z.  Needs BN == 128 and N % 64 == 0.
+template <int BN, int STAGES, int CTAS, int QHB = 0, int ACC = 1>
+__global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC>::THREADS, CTAS)
     k_gemm_nvfp4_s(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
                    const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
                    int K, const float* __restrict__ bias, void* __restrict__ y, int epi,
-                   void* ws, int stall) {
-  using C = SCfg<BN, STAGES, CTAS>;
+                   void* ws, int stall, const float* __restrict__ q_sg, float q_isb,
+                   uint8_t* __restrict__ q_codes, uint8_t* __restrict__ q_sf, float* __restrict__ q_sg_next) {
+  static_assert(QHB == 0 || BN == 128, "fused quantisation works on 128-column tiles");
+  using C = SCfg<BN, STAGES, CTAS, ACC>;
   constexpr int S = STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
-  // bars: full[S], empty[S], sf_ready[S], acc_full, acc_empty, mma_done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 3);
+  // bars: full[S], empty[S], sf_ready[S], acc_full[ACC], acc_empty[ACC], mma_done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 2 * ACC + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t sbase = smem_u32(smem);
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto empty = [&](int s) { return smem_u32(bars + S + s); };
   auto sf_ready = [&](int s) { return smem_u32(bars + 2 * S + s); };
-  const uint32_t afull = smem_u32(bars + 3 * S), aempty = smem_u32(bars + 3 * S + 1);
-  const uint32_t mma_done = smem_u32(bars + 3 * S + 2);
+  auto afull = [&](int b) { return smem_u32(bars + 3 * S + b); };
+  auto aempty = [&](int b) { return smem_u32(bars + 3 * S + ACC + b); };
+  const uint32_t mma_done = smem_u32(bars + 3 * S + 2 * ACC);
   auto a_tile = [&](int s) { return sbase + s * C::STAGE_BYTES; };
   auto b_tile = [&](int s) { return a_tile(s) + A_BYTES; };
   auto sfa_tile = [&](int s) { return smem + s * C::STAGE_BYTES + A_BYTES + C::B_BYTES; };
@@ -849,8 +883,10 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
       mbar_init(empty(s), 1);
       mbar_init(sf_ready(s), 4);
     }
-    mbar_init(afull, 1);
-    mbar_init(aempty, C::EPI_WARPS);
+    for (int b = 0; b < ACC; ++b) {
+      mbar_init(afull(b), 1);
+      mbar_init(aempty(b), C::EPI_WARPS);
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -905,8 +941,10 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
       uint32_t kc = 0, tc = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
-        if (!mbar_wait(aempty, (tc & 1) ^ 1, ws, abort_flag)) break;
+        const int buf = tc % ACC;
+        if (!mbar_wait(aempty(buf), ((tc / ACC) & 1) ^ 1, ws, abort_flag)) break;
         tc_fence_after();
+        const uint32_t dacc = tmem + buf * BN;
         for (int kb = 0; kb < num_kb; ++kb, ++kc) {
           const int s = kc % S;
           if (!mbar_wait(full(s), (kc / S) & 1, ws, abort_flag) ||
@@ -918,12 +956,12 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
           const int nsub = min(4, ksteps - kb * 4);
           for (int j = 0; j < nsub; ++j) {
             const uint32_t sfa_col = C::SF_BASE + (s * 4 + j) * C::SF_COLS;
-            tc_mma(tmem, desc_sw128(a_tile(s) + j * 32), desc_sw128(b_tile(s) + j * 32), idesc,
+            tc_mma(dacc, desc_sw128(a_tile(s) + j * 32), desc_sw128(b_tile(s) + j * 32), idesc,
                    tmem + sfa_col, tmem + sfa_col + 4, (kb | j) != 0 ? 1u : 0u);
           }
           tc_commit(empty(s));
         }
-        if (ok) tc_commit(afull);
+        if (ok) tc_commit(afull(buf));
       }
       tc_commit(mma_done);
       volatile int no_abort = 0;
@@ -969,16 +1007,25 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
     const int q = warp & 3;
     const int half = e >> 2;
     const float alpha = __fmul_rn(*a_gs, *b_gs);
+    float q_s = 0.f, q_six = 0.f, q_amax = 0.f;
+    const int64_t q_upr = N / 64;
+    if constexpr (QHB > 0) {
+      q_s = *q_sg;
+      q_six = __fmul_rn(6.0f, q_s);
+    }
     uint32_t tc = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tc) {
       const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
-      if (!mbar_wait(afull, tc & 1, ws, abort_flag)) break;
+      const int buf = tc % ACC;
+      if (!mbar_wait(afull(buf), (tc / ACC) & 1, ws, abort_flag)) break;
       tc_fence_after();
       const int row = m0 + q * 32 + lane;
+      const uint32_t tacc = tmem + buf * BN;
+      if constexpr (QHB == 0) {
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + half * 128 + c * 32, r);
+        tc_ld32(tacc + ((uint32_t)(q * 32) << 16) + half * 128 + c * 32, r);
         const int col0 = n0 + half * 128 + c * 32;
         if (row >= M || col0 >= N) continue;
         float v[32];
@@ -986,7 +1033,14 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
         for (int i = 0; i < 32; ++i) {
           v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
           if (bias) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
-          v[i] = epi_act(v[i], epi);
+        }
+        if (epi & EPI_GELU) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 g = gelu_erf2(make_float2(v[2 * i], v[2 * i + 1]));
+            v[2 * i] = g.x;
+            v[2 * i + 1] = g.y;
+          }
         }
         const int64_t off = (int64_t)row * N + col0;
         if (col0 + 32 <= N && (N % 16) == 0) {
@@ -1021,14 +1075,81 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
           }
         }
       }
+      } else {
+#pragma unroll 1
+      for (int c2 = 0; c2 < 2; ++c2) {  // two 64-column units of the 128-column tile
+        const int col0 = n0 + c2 * 64;
+        float2 v[32];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t r[32];
+          tc_ld32(tacc + ((uint32_t)(q * 32) << 16) + c2 * 64 + hh * 32, r);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int cA = col0 + hh * 32 + 2 * i;
+            float z0 = __fmul_rn(__uint_as_float(r[2 * i]), alpha);
+            float z1 = __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha);
+            if (bias) {
+              z0 = __fadd_rn(z0, bias[cA < N ? cA : N - 1]);
+              z1 = __fadd_rn(z1, bias[cA + 1 < N ? cA + 1 : N - 1]);
+            }
+            // the value the output would hold in bf16 is what gets transformed
+            const float2 za = epi_act2(make_float2(z0, z1), epi);
+            v[hh * 16 + i] = bf16x2_to_f2(f2_to_bf16x2(za.x, za.y));
+          }
+        }
+        if (col0 >= N) continue;
+        const int ri = row & 127;
+        uint32_t* sfw = reinterpret_cast<uint32_t*>(q_sf + ((int64_t)(row >> 7) * q_upr + col0 / 64) * 512 +
+                                                    (ri & 31) * 16 + (ri >> 5) * 4);
+        if (row >= M) {  // rows padding the scale layout to a multiple of 128: zero scales
+          *sfw = 0u;
+          continue;
+        }
+        if (y) {
+          uint16_t* yp = reinterpret_cast<uint16_t*>(y) + (int64_t)row * N + col0;
+#pragma unroll
+          for (int b4 = 0; b4 < 4; ++b4) {
+            U8x32 o;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o.w[i] = f2_to_bf16x2(v[b4 * 8 + i].x, v[b4 * 8 + i].y);
+            st256(yp + b4 * 16, o);
+          }
+        }
+        fwht64<QHB>(v);
+        const float2 c = make_float2(q_isb, q_isb);
+#pragma unroll
+        for (int p = 0; p < 32; ++p) v[p] = mul2(v[p], c);
+        q_amax = fmaxf(q_amax, amax_range(v, 0, 32));
+        U8x32 out;
+        *sfw = nvfp4_encode_unit(v, q_s, q_six, out);
+        st256(q_codes + (int64_t)row * (N / 2) + col0 / 2, out);
+      }
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(aempty);
+      if (lane == 0) mbar_arrive(aempty(buf));
     }
     tc_fence_before();
+    if constexpr (QHB > 0) {
+      const float m = warp_max_f(q_amax);
+      if (lane == 0) atomicMax(ws_u32(ws, WS_AMAX), __float_as_uint(m));
+    }
   }
 
   __syncthreads();
+  if constexpr (QHB > 0) {  // the last CTA turns the whole output's max|H Z| into its tensor scale
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const uint32_t t = atomicAdd(ws_u32(ws, WS_TICKET), 1u);
+      if (t == gridDim.x - 1) {
+        __threadfence();
+        const float amax = __uint_as_float(atomicExch(ws_u32(ws, WS_AMAX), 0u));
+        *q_sg_next = __fdiv_rn(amax, 2688.0f);
+        *ws_u32(ws, WS_TICKET) = 0u;
+      }
+    }
+  }
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
@@ -1036,13 +1157,14 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS>::THREADS, CTAS)
   }
 }
 
-template <int BN, int STAGES, int CTAS>
+template <int BN, int STAGES, int CTAS, int QHB = 0, int ACC = 1>
 static dit_status launch_s(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf, const uint8_t* b_sf,
                            const float* a_gs, const float* b_gs, int M, int N, int K, const float* bias, void* y,
-                           int epi, void* ws, cudaStream_t st) {
-  using C = SCfg<BN, STAGES, CTAS>;
+                           int epi, void* ws, cudaStream_t st, const float* q_sg = nullptr, float q_isb = 0.f,
+                           uint8_t* q_codes = nullptr, uint8_t* q_sf = nullptr, float* q_sg_next = nullptr) {
+  using C = SCfg<BN, STAGES, CTAS, ACC>;
   static bool attr_done = false;
-  auto kern = k_gemm_nvfp4_s<BN, STAGES, CTAS>;
+  auto kern = k_gemm_nvfp4_s<BN, STAGES, CTAS, QHB, ACC>;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
       return DIT_ERR_CUDA;
@@ -1052,7 +1174,8 @@ static dit_status launch_s(const CUtensorMap& ta, const CUtensorMap& tb, const u
   int64_t grid = (int64_t)num_sms() * CTAS;
   if (grid > tiles) grid = tiles;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y,
-                                                         epi, ws, test_stall());
+                                                         epi, ws, test_stall(), q_sg, q_isb, q_codes, q_sf,
+                                                         q_sg_next);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -1115,6 +1238,41 @@ static int nvfp4_tile_cfg() {
   return e ? atoi(e) : 10;
 }
 
+extern "C" dit_status dit_qgemm_nvfp4_fused_quant(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
+                                                  const uint8_t* b, const uint8_t* b_sf, const float* b_gs,
+                                                  int64_t m, int64_t n, int64_t k, const float* bias,
+                                                  dit_act act, void* y, int hblock, const float* q_scale_in,
+                                                  uint8_t* q_codes, uint8_t* q_sf, float* q_scale_next,
+                                                  void* ws, size_t ws_bytes, dit_stream_t stream) {
+  if (!a || !a_sf || !a_gs || !b || !b_sf || !b_gs || !q_scale_in || !q_codes || !q_sf || !q_scale_next || !ws ||
+      ws_bytes < WS_BYTES)
+    return DIT_ERR_INVALID_ARG;
+  if (m <= 0 || n <= 0 || k <= 0 || m > 0x7fffffff || n > 0x7fffffff || k > 0x7fffffff)
+    return DIT_ERR_INVALID_ARG;
+  if (act != DIT_ACT_NONE && act != DIT_ACT_GELU_ERF) return DIT_ERR_INVALID_ARG;
+  if (hblock != 16 && hblock != 32 && hblock != 64) return DIT_ERR_UNSUPPORTED;
+  if (k % 64 || n % 64) return DIT_ERR_UNSUPPORTED;
+  if (!aligned32(a) || !aligned32(b) || !aligned32(a_sf) || !aligned32(b_sf) || !aligned32(q_codes) ||
+      !aligned32(q_sf) || !aligned32(ws) || (y && !aligned32(y)))
+    return DIT_ERR_ALIGNMENT;
+  CUtensorMap ta, tb;
+  if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(k / 2),
+                      (uint64_t)m, (uint64_t)(k / 2), f4::BK / 2, f4::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(b), (uint64_t)(k / 2),
+                      (uint64_t)n, (uint64_t)(k / 2), f4::BK / 2, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return DIT_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int epi = EPI_BF16 | (act == DIT_ACT_GELU_ERF ? EPI_GELU : 0);
+  const float isb = (float)(1.0 / sqrt((double)hblock));
+#define DIT6_FQ(HB_)                                                                                          \
+  return f4::launch_s<128, 3, 2, HB_>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, epi, ws, \
+                                      st, q_scale_in, isb, q_codes, q_sf, q_scale_next)
+  if (hblock == 16) DIT6_FQ(16);
+  if (hblock == 32) DIT6_FQ(32);
+  DIT6_FQ(64);
+#undef DIT6_FQ
+}
+
 extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
                                       const uint8_t* b, const uint8_t* b_sf, const float* b_gs,
                                       int64_t m, int64_t n, int64_t k, const float* bias,
@@ -1156,6 +1314,8 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
     default: return f4::launch_s<128, 3, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 11: return f4::launch_s<256, 4, 1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 12: return f4::launch_s<128, 6, 1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 13: return f4::launch_s<128, 6, 1, 0, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 14: return f4::launch_s<128, 4, 1, 0, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 0: return f4::launch<128, 3, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
   }
 }

@@ -92,13 +92,6 @@ __device__ __forceinline__ void transform_raw(const RawUnit<T>& raw, float2 (&v)
   for (int p = 0; p < 32; ++p) v[p] = mul2(v[p], c);
 }
 
-__device__ __forceinline__ float amax_range(const float2 (&v)[32], int p0, int np) {
-  float m = 0.f;
-#pragma unroll
-  for (int p = 0; p < 32; ++p)
-    if (p >= p0 && p < p0 + np) m = fmaxf(m, fmaxf(fabsf(v[p].x), fabsf(v[p].y)));
-  return m;
-}
 
 // ---------------------------------------------------------------------------------------
 // INT8: CTA = `tr` whole rows x `upr` units per row; row amax through shared memory.
@@ -239,30 +232,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const void* __restrict__ x,
     transform_raw<T, HB>(cur, v, inv_sqrt_b);
     cur = nxt;
     U8x32 out;
-    uint32_t sfword = 0;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {  // four 16-element scale blocks
-      const float ab = amax_range(v, g * 8, 8);
-      uint32_t code = 0;
-      float inv = 0.f;
-      if (s_g > 0.f) {
-        code = e4m3_code(__fdiv_rn(ab, six_sg));
-        const float bs = __fmul_rn(e4m3_value(code), s_g);
-        inv = bs == 0.f ? 0.f : __frcp_rn(bs);
-      }
-      sfword |= code << (8 * g);
-      const float2 iv = make_float2(inv, inv);
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {  // 8 elements -> one 32-bit word of 8 codes
-        uint32_t word = 0;
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-          const float2 s = mul2(v[g * 8 + w * 4 + pp], iv);
-          word |= e2m1x2(s.x, s.y) << (8 * pp);
-        }
-        out.w[g * 2 + w] = inv == 0.f ? 0u : word;
-      }
-    }
+    const uint32_t sfword = nvfp4_encode_unit(v, s_g, six_sg, out);
     st256(codes + u * 32, out);
     *sfw = sfword;
   }

@@ -3,7 +3,8 @@
   python -m int8_mixed_precision_gb300.kernel_bench --case gemm_nvfp4 --m 17776 --n 5760 --k 1920
 
 Cases: quant_int8, quant_nvfp4 (two passes), quant_nvfp4_given (one pass, tensor scale
-given), gamma, tdc_commit, tdc_skip, gemm_int8, gemm_nvfp4.  Inputs are synthetic bf16
+given), gamma, tdc_commit, tdc_skip, gemm_int8, gemm_nvfp4, ffn_nvfp4_fused / ffn_nvfp4_unfused
+(FFN up + GELU + quantisation for the next NVFP4 layer).  Inputs are synthetic bf16
 activations (N(0,1), 1% outlier channels x50) and N(0,0.02) weights.  Prints one JSON line
 with the median time and the algorithmic rate (GB/s for streaming kernels, TFLOP/s for
 GEMMs).  Also the small cases used for ncu captures.
@@ -26,6 +27,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--int8-container", choices=["bf16", "int8"], default="bf16")
+    ap.add_argument("--act", choices=["none", "gelu"], default="none", help="GEMM epilogue activation")
     a = ap.parse_args(argv)
 
     import torch
@@ -74,18 +76,43 @@ def main(argv=None):
             fn = lambda: dit.tdc_step(dit.TDC_SKIP, xi, ws, x_out_skip=out, d1=d1)
             units = m * k * 6
         unit = "GB/s"
+    elif case in ("ffn_nvfp4_fused", "ffn_nvfp4_unfused"):
+        # FFN up with GELU whose output feeds an NVFP4 layer: the GEMM with the quantisation
+        # fused in its epilogue (supplied tensor scale), or the GEMM writing bf16 followed by
+        # the quantiser (two passes); the rate counts the GEMM FLOPs
+        x = act(m, k)
+        w = torch.randn(n, k, device=dev, generator=g) * 0.02
+        lin = dit.RoutedLinear(dit.QuantizedWeight(w, a.hblock, ws), m, ws, dev)
+        y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        lin(x, dit.ROUTE_NVFP4, y, act=dit.ACT_GELU_ERF)
+        q = dit.alloc_nvfp4(m, n, dev)
+        dit.hadamard_quant_nvfp4(y, a.hblock, q["codes"], q["sf"], q["gs"], ws)
+        nxt = torch.empty(1, dtype=torch.float32, device=dev)
+        A, W = lin.a4, lin.w.nvfp4
+        if case == "ffn_nvfp4_fused":
+            fn = lambda: dit.qgemm_nvfp4_fused_quant(A["codes"], A["sf"], A["gs"], W["codes"], W["sf"], W["gs"], ws,
+                                                     a.hblock, q["gs"], q["codes"], q["sf"], nxt,
+                                                     act=dit.ACT_GELU_ERF)
+        else:
+            def fn():
+                dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], W["codes"], W["sf"], W["gs"], y, ws,
+                                act=dit.ACT_GELU_ERF)
+                dit.hadamard_quant_nvfp4(y, a.hblock, q["codes"], q["sf"], q["gs"], ws)
+        units, unit = 2 * m * n * k, "TFLOP/s"
     elif case in ("gemm_int8", "gemm_nvfp4"):
         x = act(m, k)
         w = torch.randn(n, k, device=dev, generator=g) * 0.02
         lin = dit.RoutedLinear(dit.QuantizedWeight(w, a.hblock, ws, int8_container=a.int8_container), m, ws, dev)
         y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        act_code = dit.ACT_GELU_ERF if a.act == "gelu" else dit.ACT_NONE
         if case == "gemm_int8":
             lin(x, dit.ROUTE_INT8, y)
-            fn = lambda: dit.qgemm_int8(lin.a8["q"], lin.a8["scale"], lin.w.int8["q"], lin.w.int8["scale"], y, ws)
+            fn = lambda: dit.qgemm_int8(lin.a8["q"], lin.a8["scale"], lin.w.int8["q"], lin.w.int8["scale"], y, ws,
+                                        act=act_code)
         else:
             lin(x, dit.ROUTE_NVFP4, y)
             fn = lambda: dit.qgemm_nvfp4(lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], lin.w.nvfp4["codes"],
-                                         lin.w.nvfp4["sf"], lin.w.nvfp4["gs"], y, ws)
+                                         lin.w.nvfp4["sf"], lin.w.nvfp4["gs"], y, ws, act=act_code)
         units, unit = 2 * m * n * k, "TFLOP/s"
     else:
         raise SystemExit(f"unknown case {case}")
