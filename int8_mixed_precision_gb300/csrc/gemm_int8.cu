@@ -182,7 +182,8 @@ extern "C" dit_status dit_qgemm_int8(const void* a, const float* a_scale, const 
   const int epi = (y_dt == DIT_BF16 ? EPI_BF16 : 0) | (act == DIT_ACT_GELU_ERF ? EPI_GELU : 0);
   if (k % 16 || n % 8) return DIT_ERR_UNSUPPORTED;
   if (!aligned32(a) || !aligned32(b) || !aligned32(y) || !aligned32(ws) ||
-      (acc_debug && !aligned32(acc_debug)))
+      (acc_debug && !aligned32(acc_debug)) || (reinterpret_cast<uintptr_t>(b_scale) & 15) ||
+      (bias && (reinterpret_cast<uintptr_t>(bias) & 15)))
     return DIT_ERR_ALIGNMENT;
   if (ab_dt == DIT_BF16)
     return gemm_int8_tc(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_debug,

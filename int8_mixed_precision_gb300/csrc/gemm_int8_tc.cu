@@ -568,7 +568,11 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-template <bool GELU>
+// F2: K spans at most two exact chunks and no raw accumulators are requested.  Each chunk sum
+// is then an exact fp32 integer and one fp32 addition rounds their exact total once, as the
+// conversion of the int32 total to fp32 does, so the chunks are summed in fp32 and the output
+// is the same bit for bit without the int32 round trip.
+template <bool GELU, bool F2>
 __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     k_gemm_int8_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N, int K,
@@ -715,7 +719,12 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
           uint32_t r[16];
           tc_ld16(base + c * 16, r);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc[c * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+          for (int i = 0; i < 16; ++i) {
+            if constexpr (F2)  // acc starts as +0.0f, and 0 + c0 = c0 exactly
+              acc[c * 16 + i] = __float_as_int(__fadd_rn(__int_as_float(acc[c * 16 + i]), __uint_as_float(r[i])));
+            else
+              acc[c * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -732,11 +741,33 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
           const int cb = col0 + c * 16;
           if (cb >= N) break;
           float v[16];
+          auto accf = [&](int i) { return F2 ? __int_as_float(acc[c * 16 + i]) : (float)acc[c * 16 + i]; };
+          if (cb + 16 <= N) {  // packed: (acc * sa) * sb (+ bias), each product rounded as before
+            const float4* sb4 = reinterpret_cast<const float4*>(b_scale + cb);
+            const float4* bi4 = reinterpret_cast<const float4*>(bias + cb);
+            const float2 sa2 = make_float2(sa, sa);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = cb + i < N ? cb + i : N - 1;
-            v[i] = __fmul_rn(__fmul_rn((float)acc[c * 16 + i], sa), b_scale[col]);
-            if (bias) v[i] = __fadd_rn(v[i], bias[col]);
+            for (int j = 0; j < 4; ++j) {
+              const float4 sb = sb4[j];
+              float2 lo = mul2(mul2(make_float2(accf(4 * j), accf(4 * j + 1)), sa2), make_float2(sb.x, sb.y));
+              float2 hi = mul2(mul2(make_float2(accf(4 * j + 2), accf(4 * j + 3)), sa2), make_float2(sb.z, sb.w));
+              if (bias) {
+                const float4 bb = bi4[j];
+                lo = add2(lo, make_float2(bb.x, bb.y));
+                hi = add2(hi, make_float2(bb.z, bb.w));
+              }
+              v[4 * j] = lo.x;
+              v[4 * j + 1] = lo.y;
+              v[4 * j + 2] = hi.x;
+              v[4 * j + 3] = hi.y;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int col = cb + i < N ? cb + i : N - 1;
+              v[i] = __fmul_rn(__fmul_rn(accf(i), sa), b_scale[col]);
+              if (bias) v[i] = __fadd_rn(v[i], bias[col]);
+            }
           }
           if (GELU) {
 #pragma unroll
@@ -796,7 +827,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
   }
 }
 
-template <bool GELU>
+template <bool GELU, bool F2>
 dit_status launch_pair(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
                        int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out, void* ws,
                        cudaStream_t st) {
@@ -807,7 +838,7 @@ dit_status launch_pair(const void* a, const float* a_scale, const void* b, const
       !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(b), (uint64_t)k, (uint64_t)n,
                       (uint64_t)k * 2, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return DIT_ERR_CUDA;
-  auto kern = k_gemm_int8_pair<GELU>;
+  auto kern = k_gemm_int8_pair<GELU, F2>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES) != cudaSuccess)
@@ -948,8 +979,14 @@ dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, cons
   // kernel, which also carries the split-K tail.
   const char* pr = getenv("DIT6_INT8_TC_PAIR");
   if (!(pr && pr[0] == '0') && !e && !c)
-    return g ? i8tc::launch_pair<true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
-             : i8tc::launch_pair<false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
+  {
+    const bool f2 = !acc_out && (k + 1023) / 1024 <= 2;
+    if (f2)
+      return g ? i8tc::launch_pair<true, true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
+               : i8tc::launch_pair<false, true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
+    return g ? i8tc::launch_pair<true, false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
+             : i8tc::launch_pair<false, false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
+  }
 #define DIT6_I8TC(BN_, MC_)                                                                          \
   return g ? i8tc::launch<BN_, MC_, true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, ws_bytes, st) \
            : i8tc::launch<BN_, MC_, false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, ws_bytes, st)
