@@ -715,15 +715,15 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
         tc_fence_after();
         const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + half * CW;
 #pragma unroll
-        for (int c = 0; c < CW / 16; ++c) {
-          uint32_t r[16];
-          tc_ld16(base + c * 16, r);
+        for (int c = 0; c < CW / 32; ++c) {
+          uint32_t r[32];
+          tc_ld32(base + c * 32, r);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
+          for (int i = 0; i < 32; ++i) {
             if constexpr (F2)  // acc starts as +0.0f, and 0 + c0 = c0 exactly
-              acc[c * 16 + i] = __float_as_int(__fadd_rn(__int_as_float(acc[c * 16 + i]), __uint_as_float(r[i])));
+              acc[c * 32 + i] = __float_as_int(__fadd_rn(__int_as_float(acc[c * 32 + i]), __uint_as_float(r[i])));
             else
-              acc[c * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
+              acc[c * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
           }
         }
         tc_fence_before();
