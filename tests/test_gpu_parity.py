@@ -63,15 +63,17 @@ def test_int8_quant_parity(rows, k, dtype, hb, container):
     assert n_ex <= max(2, q.numel() // 10000)
 
 
-def test_int8_quant_zero_and_constant_rows():
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_int8_quant_zero_and_constant_rows(dtype):
     x = np.zeros((5, 128), np.float32)
     x[1] = 3.0
     x[2, 7] = -1e-3
     x[4] = np.linspace(-2, 2, 128, dtype=np.float32)
+    xin = x if dtype == "f32" else F.f32_to_bf16_bits(x)
     q = torch.empty(5, 128, dtype=torch.int8, device="cuda")
     s = torch.empty(5, dtype=torch.float32, device="cuda")
-    dit.hadamard_quant_int8(dev_f32(x), 16, q, s)
-    check_int8(host(q), host(s), x, "f32", 16)
+    dit.hadamard_quant_int8(dev_f32(x) if dtype == "f32" else dev_bf16(xin), 16, q, s)
+    check_int8(host(q), host(s), xin, dtype, 16)
     assert host(s)[0] == 0 and not host(q)[0].any()
 
 
