@@ -39,6 +39,32 @@ LINEARS = [("qkv", HIDDEN, 3 * HIDDEN), ("out", HIDDEN, HIDDEN), ("ffn_up", HIDD
            ("ffn_down", FFN, HIDDEN)]
 
 
+def measured_traffic(kind: str):
+    """DRAM bytes per launch of a kernel type from the committed ncu summary of this workload,
+    or None when the kernel sources have changed since that capture (their hash differs)."""
+    import glob
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", "dram_traffic_cogvideox2b_step.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    csrc = os.path.join(ROOT, "int8_mixed_precision_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
+                   [os.path.join(ROOT, "include", "dit6.h")])
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    m = re.search(r"sources sha256: ([0-9a-f]{64})", text)
+    if not m or m.group(1) != h.hexdigest():
+        return None
+    row = re.search(r"^\| " + re.escape(kind) + r" \| \d+ \| [\d.]+ \| [\d.]+ \| (\d+) \|", text, re.M)
+    return int(row.group(1)) if row else None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -461,12 +487,13 @@ def run_ours(args, rank, world, local_rank):
             peak = pk["bf16_tflops_sustained"] * 6.0
             peak_note = f"{src} bf16 sustained x 6 (nominal dense fp4/bf16 ratio)"
         roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": None, "kernel": dominant, "peak_source": peak_note}
+                "frac": round(achieved / peak, 4), "traffic": measured_traffic(dominant), "kernel": dominant,
+                "peak_source": peak_note}
     else:
         achieved = unit_per_launch / (avg_ms * 1e-3) / 1e9
         peak = pk["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None, "kernel": dominant,
+                "frac": round(achieved / peak, 4), "traffic": measured_traffic(dominant), "kernel": dominant,
                 "peak_source": f"{src} HBM copy"}
     kern_times = {k: round(v, 3) for k, v in tot.items()}
     hbm = {k: round(units[k] / (tot[k] * 1e-3) / 1e9, 1) for k in ("quant_int8", "quant_nvfp4", "tdc_commit")
