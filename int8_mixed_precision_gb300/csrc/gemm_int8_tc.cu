@@ -101,14 +101,6 @@ __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
                "h"(mask)
                : "memory");
 }
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 
 // MC = 1: independent CTAs.  MC = 2: clusters of two CTAs on adjacent 128-row M blocks and the
 // same N block; each loads half of the shared B tile and multicasts it to both, halving the
@@ -507,65 +499,12 @@ struct PairCfg {
   static constexpr int TMEM_COLS = 512;                         // two 256-column chunk buffers
 };
 
-__device__ __forceinline__ uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, "
-      "p; }"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// bounded wait with cluster-scope acquire (arrivals come from the peer CTA as well)
-__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, void* ws, volatile int* abort) {
-  if (mbar_try_wait_cl(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cl(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-        raise_status(ws, DIT_ERR_TIMEOUT);
-        *abort = 1;
-        return false;
-      }
-    }
-  }
-}
-// TMA load into this CTA's shared memory whose completed bytes count on `bar_cluster`, an
-// mbarrier of either CTA of the pair (shared::cluster address)
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
-                                                 int32_t c0, int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], "
-      "[%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
-      : "memory");
-}
 __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
-}
-__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(mask)
-               : "memory");
-}
-__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // F2: K spans at most two exact chunks and no raw accumulators are requested.  Each chunk sum

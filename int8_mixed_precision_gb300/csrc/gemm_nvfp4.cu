@@ -1222,6 +1222,7 @@ static dit_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const uin
   return DIT_OK;
 }
 
+
 }  // namespace f4
 }  // namespace dit6
 
