@@ -308,6 +308,24 @@ def prepare_weight(w: np.ndarray, b: int) -> dict:
     return {"nvfp4": quant_nvfp4(wt), "int8": quant_int8_rows(wt), "wt": wt}
 
 
+def nvfp4_weight_to_int8(codes: np.ndarray, sf: np.ndarray, s_g) -> dict:
+    """INT8 weights derived from NVFP4-only weights ([ZH] 2.A, weight handling: every weight is
+    quantised offline to NVFP4, and converted only when a layer needs INT8 activations).
+
+    Reading: the NVFP4 weight's value in float32 -- dec(code) * dec(block scale) is exact (at
+    most 6 significant bits), then one rounding for the product with the tensor scale s_g --
+    quantised per output channel like quant_int8_rows.  No second Hadamard transform: the
+    NVFP4 weight is already in the rotated basis.  codes [rows x K] unpacked, sf [rows x K/16].
+    """
+    rows, k = codes.shape
+    val = F.E2M1_VALUES[codes].astype(np.float32).reshape(rows, k // 16, 16)
+    sc = F.E4M3_VALUES[sf].astype(np.float32)[:, :, None]
+    w = ((val * sc).astype(np.float32) * np.float32(s_g)).astype(np.float32).reshape(rows, k)
+    r = quant_int8_rows(w)
+    r["w"] = w
+    return r
+
+
 def routed_linear(x: np.ndarray, wprep: dict, b: int, route: int) -> np.ndarray:
     """Y = quantised (X H)(W H)^T along the given route, float64."""
     y = block_fwht_f32(np.asarray(x, np.float32), b)

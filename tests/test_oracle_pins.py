@@ -547,3 +547,52 @@ def test_planted_tanh_gelu_is_caught():
     x = np.linspace(-4, 4, 81)
     tanh_form = 0.5 * x * (1 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x ** 3)))
     assert np.max(np.abs(tanh_form - D.gelu_erf(x))) > 1e-4
+
+
+# ----------------------------------------------------------------------------------------
+# INT8 weights derived from NVFP4-only weights
+# ----------------------------------------------------------------------------------------
+
+
+def _golden_nvfp4_to_int8():
+    g, _ = load_golden("nvfp4_weight_to_int8.txt")
+    codes = np.array([[int(v) for v in g["codes_row0"]], [int(v) for v in g["codes_row1"]]], np.uint8)
+    sf = np.array([[int(v, 16) for v in g["sf_row0"]], [int(v, 16) for v in g["sf_row1"]]], np.uint8)
+    return g, codes, sf, np.float32(g["s_g"][0])
+
+
+def test_nvfp4_weight_to_int8_worked_example():
+    g, codes, sf, sg = _golden_nvfp4_to_int8()
+    r = D.nvfp4_weight_to_int8(codes, sf, sg)
+    assert r["q"][0].tolist() == [int(v) for v in g["q_row0"]]
+    assert r["q"][1].tolist() == [int(v) for v in g["q_row1"]]
+    num, den = (np.float32(v) for v in g["scale_row0"])
+    assert r["scale"][0] == num / den and r["scale"][1] == 0
+
+
+def test_nvfp4_weight_to_int8_scales_with_the_tensor_scale():
+    """A power-of-two tensor scale changes no code and scales the row scale exactly."""
+    g = synth.rng(71)
+    codes = g.integers(0, 16, (6, 64)).astype(np.uint8)
+    sf = g.integers(0x20, 0x50, (6, 4)).astype(np.uint8)
+    a = D.nvfp4_weight_to_int8(codes, sf, np.float32(0.25))
+    b = D.nvfp4_weight_to_int8(codes, sf, np.float32(4.0))
+    assert np.array_equal(a["q"], b["q"])
+    assert np.array_equal(b["scale"], a["scale"] * np.float32(16.0))
+
+
+def test_nvfp4_weight_to_int8_error_bound():
+    """|q s - w| <= s / 2 (plus the float32 rounding of 1/s) for the dequantised NVFP4 weight."""
+    g = synth.rng(72)
+    codes = g.integers(0, 16, (16, 128)).astype(np.uint8)
+    sf = g.integers(0x18, 0x60, (16, 8)).astype(np.uint8)
+    r = D.nvfp4_weight_to_int8(codes, sf, np.float32(0.01))
+    w = D.dequant_nvfp4(codes, sf, np.float32(0.01))
+    err = np.abs(r["q"].astype(np.float64) * r["scale"][:, None] - w)
+    assert (err <= r["scale"][:, None] * (0.5 + 1e-5)).all()
+
+
+def test_planted_wrong_block_scale_index_is_caught():
+    g, codes, sf, sg = _golden_nvfp4_to_int8()
+    r = D.nvfp4_weight_to_int8(codes, sf[:, ::-1].copy(), sg)     # the blocks' scales swapped
+    assert r["q"][0].tolist() != [int(v) for v in g["q_row0"]]
