@@ -196,9 +196,10 @@ class Workload:
         a = self.torch.cuda.Event(enable_timing=True)
         z = self.torch.cuda.Event(enable_timing=True)
         a.record()
-        fn()
+        r = fn()
         z.record()
         self.timers[kind].append((a, z))
+        return r
 
     def step(self, before_block=None):
         """One pass over the blocks; before_block(b), if given, runs on the host before block b's
@@ -217,8 +218,11 @@ class Workload:
                 act = dit.ACT_GELU_ERF if name == "ffn_up" else dit.ACT_NONE
                 if route == dit.ROUTE_INT8:
                     self._timed("quant_int8", lambda: dit.hadamard_quant_int8(x, HBLOCK, lin.a8["q"], lin.a8["scale"]))
-                    self._timed("gemm_int8", lambda: dit.qgemm_int8(lin.a8["q"], lin.a8["scale"], lin.w.int8["q"],
-                                                                    lin.w.int8["scale"], y, self.ws, act=act))
+                    w8 = lin.w.int8
+                    if w8 is None:  # NVFP4-only weights: derive the INT8 weights for this call
+                        w8 = self._timed("w_nvfp4_to_int8", lambda: lin.w.int8_into(lin.w8_scratch))
+                    self._timed("gemm_int8", lambda: dit.qgemm_int8(lin.a8["q"], lin.a8["scale"], w8["q"],
+                                                                    w8["scale"], y, self.ws, act=act))
                 else:
                     self._timed("quant_nvfp4", lambda: dit.hadamard_quant_nvfp4(
                         x, HBLOCK, lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], self.ws))
@@ -246,6 +250,42 @@ class Workload:
                     u["quant_nvfp4"] += M * k * 2 + M * k // 2 + M * k // 16
             u["tdc_commit"] += M * HIDDEN * 8
         return u
+
+
+def run_nvfp4_only_weights(wl, steps: int = 5):
+    """The same step with every weight resident in NVFP4 only ([ZH] 2.A weight handling): each
+    INT8-routed layer derives its INT8 weights per call into one scratch buffer per K."""
+    import torch
+    import int8_mixed_precision_gb300 as dit
+    dev = wl.dev
+    scratch = {k: dit.alloc_int8(max(n for _, kk, n in LINEARS if kk == k), k, dev) for _, k, _ in LINEARS}
+    saved = []
+    for blk in wl.blocks:
+        for name, k, n in LINEARS:
+            lin = blk["lin"][name]
+            saved.append((lin, lin.w, lin.w8_scratch))
+            lin.w = lin.w.without_int8()
+            lin.w8_scratch = scratch[k]
+    both = sum(w.resident_bytes() for _, w, _ in saved)
+    only = sum(lin.w.resident_bytes() for lin, _, _ in saved)
+    wl.step()
+    wl.timers = {"w_nvfp4_to_int8": []}
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        wl.step()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    conv_ms = sum(a.elapsed_time(z) for a, z in wl.timers["w_nvfp4_to_int8"]) / steps
+    wl.timers = None
+    for lin, w, sc in saved:
+        lin.w, lin.w8_scratch = w, sc
+    return {"ms_per_step": round(ms, 3), "value": round(wl.flops_step / (ms * 1e-3) / 1e12, 3), "unit": UNIT,
+            "weight_conversion_ms_per_step": round(conv_ms, 3),
+            "resident_weight_bytes": int(only), "resident_weight_bytes_nvfp4_and_int8": int(both),
+            "note": "weights resident in NVFP4 only; INT8-routed layers convert theirs per call (dit_nvfp4_to_int8)"}
 
 
 def run_tdc_loop(wl, steps: int = 50, tau: float = 0.05, seed: int = 77):
@@ -521,6 +561,8 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": int(wl.launches_per_step() * args.steps),
         "clocks": clk.summary(),
     }
+    if not args.no_nvfp4_only:
+        line["nvfp4_only_weights"] = run_nvfp4_only_weights(wl)
     if not args.no_tdc_loop:
         line["tdc_loop"] = run_tdc_loop(wl, steps=args.tdc_steps)
     if not args.no_cpu_baseline:
@@ -622,6 +664,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-tdc-loop", action="store_true")
+    ap.add_argument("--no-nvfp4-only", action="store_true", help="skip the NVFP4-only-weights variant")
     ap.add_argument("--tdc-steps", type=int, default=50)
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -165,6 +165,22 @@ dit_status dit_hadamard_quant_int8(const void* x, dit_dtype dt, int64_t rows, in
                                    dit_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * INT8 weights from NVFP4-only weights.  [ZH] 2.A, weight handling: all weights are held
+ * in NVFP4 and converted only when a layer routes INT8.
+ *
+ * w[r, c] = (dec(code[r, c]) * dec(sf[r, c/16])) * (*tensor_scale)  in fp32 (the first
+ * product is exact), then per row s = amax_row|w| / 127, q = round_half_even(w * rcp(s)) --
+ * the INT8 encoding of dit_hadamard_quant_int8, with no transform (the NVFP4 weight is
+ * already in the rotated basis).
+ * codes : device packed E2M1 [rows x k/2]; sf : device tile-layout scales (dit_sf_bytes);
+ * tensor_scale : device float.  q : device [rows x k] in container q_dt (DIT_I8 or DIT_BF16);
+ * row_scale : device float [rows].  k % 64 == 0, k <= 16384; codes, sf, q 32-byte aligned.
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_nvfp4_to_int8(const uint8_t* codes, const uint8_t* sf, const float* tensor_scale,
+                             int64_t rows, int64_t k, void* q, dit_dtype q_dt, float* row_scale,
+                             dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * (a6) NVFP4 GEMM on the block-scaled tensor cores (tcgen05 kind::mxf4nvf4).
  * [EN] 1. Problem Statement "Hardware Gap", 3. Key Contributions 4 (NVFP4 on Blackwell).
  *

@@ -222,29 +222,68 @@ def alloc_int8(rows: int, k: int, device="cuda", container: str = "bf16") -> dic
             "scale": torch.empty(rows, dtype=torch.float32, device=device)}
 
 
-class QuantizedWeight:
-    """A weight W [N x K] prepared offline in both formats (block Hadamard along K, then an
-    NVFP4 copy and a per-output-channel INT8 copy), all on the device."""
+def nvfp4_to_int8(codes, sf, tensor_scale, q, row_scale, stream=None):
+    """Per-output-channel INT8 (int8 or bf16-held codes in q) of NVFP4 weights [rows x K]."""
+    rows, k = codes.shape[0], codes.shape[1] * 2
+    st = lib().dit_nvfp4_to_int8(_p(codes), _p(sf), _p(tensor_scale), rows, k, _p(q), _dt(q), _p(row_scale),
+                                 _stream(stream))
+    _check(st, "dit_nvfp4_to_int8")
 
-    def __init__(self, w, hblock: int, ws, int8_container: str = "bf16"):
+
+class QuantizedWeight:
+    """A weight W [N x K] prepared offline: block Hadamard along K, then an NVFP4 copy and a
+    per-output-channel INT8 copy, all on the device.  nvfp4_only=True keeps the NVFP4 copy
+    alone; the INT8 weights are then derived from it when a layer routes INT8 (int8_into)."""
+
+    def __init__(self, w, hblock: int, ws, int8_container: str = "bf16", nvfp4_only: bool = False):
         n, k = w.shape
         self.n, self.k, self.hblock = n, k, hblock
+        self.int8_container = int8_container
         self.nvfp4 = alloc_nvfp4(n, k, w.device)
-        self.int8 = alloc_int8(n, k, w.device, int8_container)
         hadamard_quant_nvfp4(w, hblock, self.nvfp4["codes"], self.nvfp4["sf"], self.nvfp4["gs"], ws)
-        hadamard_quant_int8(w, hblock, self.int8["q"], self.int8["scale"])
+        self.int8 = None
+        if not nvfp4_only:
+            self.int8 = alloc_int8(n, k, w.device, int8_container)
+            hadamard_quant_int8(w, hblock, self.int8["q"], self.int8["scale"])
+
+    def without_int8(self) -> "QuantizedWeight":
+        """The same weight with its NVFP4 copy only (shared, not copied)."""
+        other = object.__new__(QuantizedWeight)
+        other.__dict__.update(self.__dict__)
+        other.int8 = None
+        return other
+
+    def resident_bytes(self) -> int:
+        tensors = list(self.nvfp4.values()) + (list(self.int8.values()) if self.int8 else [])
+        return sum(t.numel() * t.element_size() for t in tensors)
+
+    def int8_into(self, scratch, stream=None) -> dict:
+        """The INT8 weights: the resident copy, or (NVFP4-only) converted into scratch, a dict
+        like alloc_int8's with at least N rows, and returned as views of it."""
+        if self.int8 is not None:
+            return self.int8
+        q, s = scratch["q"][:self.n], scratch["scale"][:self.n]
+        nvfp4_to_int8(self.nvfp4["codes"], self.nvfp4["sf"], self.nvfp4["gs"], q, s, stream=stream)
+        return {"q": q, "scale": s}
 
 
 class RoutedLinear:
     """Y = quant(X H) quant(W H)^T along a route chosen per call; the activation buffers for
     both routes are allocated once for a maximum token count."""
 
-    def __init__(self, weight: QuantizedWeight, max_tokens: int, ws, device="cuda"):
+    def __init__(self, weight: QuantizedWeight, max_tokens: int, ws, device="cuda", int8_scratch=None):
+        """int8_scratch: for NVFP4-only weights, a buffer (alloc_int8 of at least N rows x K)
+        the INT8 weights are derived into on each INT8-routed call; several layers may share
+        one.  Allocated here when not given."""
         self.w = weight
         self.ws = ws
         self.a4 = alloc_nvfp4(max_tokens, weight.k, device)
-        container = "bf16" if weight.int8["q"].dtype == _torch().bfloat16 else "int8"
+        container = weight.int8_container
         self.a8 = alloc_int8(max_tokens, weight.k, device, container)
+        self.w8_scratch = None
+        if weight.int8 is None:
+            self.w8_scratch = int8_scratch if int8_scratch is not None else alloc_int8(weight.n, weight.k, device,
+                                                                                      container)
 
     def __call__(self, x, route: int, y, bias=None, tensor_scale_in=None, act=ACT_NONE, stream=None):
         m = x.shape[0]
@@ -252,7 +291,8 @@ class RoutedLinear:
         if route == ROUTE_INT8:
             q, s = self.a8["q"][:m], self.a8["scale"][:m]
             hadamard_quant_int8(x, w.hblock, q, s, stream=stream)
-            qgemm_int8(q, s, w.int8["q"], w.int8["scale"], y, self.ws, bias=bias, act=act, stream=stream)
+            w8 = w.int8_into(self.w8_scratch, stream=stream)
+            qgemm_int8(q, s, w8["q"], w8["scale"], y, self.ws, bias=bias, act=act, stream=stream)
         else:
             c = self.a4["codes"][:m]
             hadamard_quant_nvfp4(x, w.hblock, c, self.a4["sf"], self.a4["gs"], self.ws,

@@ -153,6 +153,84 @@ __global__ void __launch_bounds__(256) k_quant_int8(const void* __restrict__ x, 
 }
 
 // ---------------------------------------------------------------------------------------
+// NVFP4 weights -> per-output-channel INT8 ([ZH] 2.A, weight handling: weights held in NVFP4
+// only, converted when a layer routes INT8).  w = (dec(code) * dec(block scale)) * s_g in
+// fp32 (the first product exact), then the INT8 encoding of k_quant_int8 (no transform: the
+// NVFP4 weight is already in the rotated basis).  CTA = `tr` rows x `upr` 64-element units.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float e2m1_decode(uint32_t n) {
+  const uint32_t e = (n >> 1) & 3u, m = n & 1u;
+  const float mag = e == 0 ? (m ? 0.5f : 0.0f) : __uint_as_float(((e + 126u) << 23) | (m << 22));
+  return (n & 8u) ? -mag : mag;
+}
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(256) k_nvfp4_to_int8(const uint8_t* __restrict__ codes,
+                                                       const uint8_t* __restrict__ sf,
+                                                       const float* __restrict__ gs, int64_t rows, int upr,
+                                                       int tr, void* __restrict__ q,
+                                                       float* __restrict__ row_scale) {
+  __shared__ unsigned row_amax[256];
+  const int t = threadIdx.x;
+  if (t < tr) row_amax[t] = 0u;
+  __syncthreads();
+  const int rl = t / upr, j = t - rl * upr;
+  const int64_t row = (int64_t)blockIdx.x * tr + rl;
+  const bool active = rl < tr && row < rows;
+  const int64_t unit = row * upr + j;
+  float2 v[32];
+  if (active) {
+    const float s_g = *gs;
+    const U8x32 c = ld256_nc(codes + unit * 32);
+    const int64_t ri = row & 127;
+    const uint32_t sfw = *reinterpret_cast<const uint32_t*>(sf + ((row >> 7) * upr + j) * 512 + (ri & 31) * 16 +
+                                                            (ri >> 5) * 4);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {  // four 16-element blocks, one scale byte each
+      const float sc = e4m3_value((sfw >> (8 * g)) & 0xffu);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // byte p = 8g + i holds elements 2p (low nibble), 2p + 1
+        const uint32_t byte = (c.w[(8 * g + i) >> 2] >> (8 * ((8 * g + i) & 3))) & 0xffu;
+        v[8 * g + i] = make_float2(__fmul_rn(__fmul_rn(e2m1_decode(byte & 15u), sc), s_g),
+                                   __fmul_rn(__fmul_rn(e2m1_decode(byte >> 4), sc), s_g));
+      }
+    }
+    atomicMax(&row_amax[rl], __float_as_uint(amax_range(v, 0, 32)));
+  }
+  __syncthreads();
+  if (!active) return;
+  const float amax = __uint_as_float(row_amax[rl]);
+  const float s = __fdiv_rn(amax, 127.0f);
+  const float inv = s == 0.f ? 0.f : __frcp_rn(s);
+  const float2 iv = make_float2(inv, inv);
+  if (OUT_BF16) {
+    U8x32 out[4];
+#pragma unroll
+    for (int p = 0; p < 32; ++p) {
+      const float2 a = mul2(v[p], iv);
+      out[p / 8].w[p % 8] = f2_to_bf16x2(rintf(a.x), rintf(a.y));
+    }
+    char* dst = reinterpret_cast<char*>(q) + unit * (UNIT * 2);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) st256(dst + 32 * c4, out[c4]);
+  } else {
+    U8x32 out[2];
+#pragma unroll
+    for (int p = 0; p < 32; p += 2) {
+      const float2 a = mul2(v[p], iv), b = mul2(v[p + 1], iv);
+      const int q0 = __float2int_rn(a.x), q1 = __float2int_rn(a.y);
+      const int q2 = __float2int_rn(b.x), q3 = __float2int_rn(b.y);
+      out[p / 16].w[(p % 16) / 2] = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) |
+                                    ((uint32_t)(q2 & 0xff) << 16) | ((uint32_t)(q3 & 0xff) << 24);
+    }
+    int8_t* dst = reinterpret_cast<int8_t*>(q) + unit * UNIT;
+    st256(dst, out[0]);
+    st256(dst + 32, out[1]);
+  }
+  if (j == 0) row_scale[row] = s;
+}
+
+// ---------------------------------------------------------------------------------------
 // NVFP4 pass 1: amax of the transformed tensor -> s_g = amax / 2688 (workspace + output)
 // ---------------------------------------------------------------------------------------
 template <typename T, int HB>
@@ -332,6 +410,26 @@ extern "C" dit_status dit_hadamard_quant_nvfp4(const void* x, dit_dtype dt, int6
     else DIT_NV(float, 64);
   }
 #undef DIT_NV
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
+extern "C" dit_status dit_nvfp4_to_int8(const uint8_t* codes, const uint8_t* sf, const float* tensor_scale,
+                                        int64_t rows, int64_t k, void* q, dit_dtype q_dt, float* row_scale,
+                                        dit_stream_t stream) {
+  if (!codes || !sf || !tensor_scale || !q || !row_scale || rows <= 0 || k <= 0) return DIT_ERR_INVALID_ARG;
+  if (q_dt != DIT_I8 && q_dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
+  if (k % UNIT || k > 256 * UNIT) return DIT_ERR_UNSUPPORTED;
+  if (!aligned32(codes) || !aligned32(sf) || !aligned32(q)) return DIT_ERR_ALIGNMENT;
+  const int upr = (int)(k / UNIT);
+  const int tr = upr >= 256 ? 1 : 256 / upr;
+  const int64_t grid = (rows + tr - 1) / tr;
+  if (grid > 0x7fffffff) return DIT_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (q_dt == DIT_BF16)
+    k_nvfp4_to_int8<true><<<(unsigned)grid, tr * upr, 0, st>>>(codes, sf, tensor_scale, rows, upr, tr, q, row_scale);
+  else
+    k_nvfp4_to_int8<false><<<(unsigned)grid, tr * upr, 0, st>>>(codes, sf, tensor_scale, rows, upr, tr, q, row_scale);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }

@@ -472,6 +472,81 @@ def test_nvfp4_fused_epilogue_quant_full_size_sampled(ws):
     assert not ((got != r["codes"]) & ~ex).any()
 
 
+# ------------------------------------------------------------------------------ NVFP4-only weights
+
+
+@pytest.mark.parametrize("rows,k", [(5760 // 20, 1920), (129, 7680), (1, 64), (300, 3072)])
+@pytest.mark.parametrize("container", [torch.int8, torch.bfloat16])
+def test_nvfp4_to_int8_parity(rows, k, container):
+    """INT8 weights derived on the GPU from NVFP4 weights equal the oracle's: scales bit-exact,
+    codes bit-exact except elements on a rounding boundary."""
+    g = synth.rng(rows * 3 + k)
+    w = (g.standard_normal((rows, k)) * 0.02).astype(np.float32)
+    w[:, ::97] *= 30.0
+    r4 = D.quant_nvfp4(D.block_fwht_f32(w, 64))
+    codes = torch.from_numpy(D.pack_e2m1(r4["codes"])).cuda()
+    sf = torch.from_numpy(F.sf_to_tiled(r4["sf"], rows, k)).cuda()
+    gs = torch.tensor([float(r4["s_g"])], dtype=torch.float32, device="cuda")
+    q = torch.empty(rows, k, dtype=container, device="cuda")
+    sc = torch.empty(rows, dtype=torch.float32, device="cuda")
+    dit.nvfp4_to_int8(codes, sf, gs, q, sc)
+    torch.cuda.synchronize()
+    ref = D.nvfp4_weight_to_int8(r4["codes"], r4["sf"], r4["s_g"])
+    assert np.array_equal(host(sc).view(np.uint32), ref["scale"].view(np.uint32))
+    qh = _codes(q)
+    bad = (qh != ref["q"]) & ~(D.int8_rounding_margin(ref["v"]) <= 1e-5)
+    assert not bad.any(), int(bad.sum())
+
+
+def test_nvfp4_to_int8_worked_example():
+    """The hand-worked fixture (padded from K = 32 to 64 with zero codes and scales)."""
+    from conftest import load_golden
+    gd, _ = load_golden("nvfp4_weight_to_int8.txt")
+    codes = np.zeros((2, 64), np.uint8)
+    codes[0, :32] = [int(v) for v in gd["codes_row0"]]
+    codes[1, :32] = [int(v) for v in gd["codes_row1"]]
+    sf = np.zeros((2, 4), np.uint8)
+    sf[0, :2] = [int(v, 16) for v in gd["sf_row0"]]
+    q = torch.empty(2, 64, dtype=torch.int8, device="cuda")
+    sc = torch.empty(2, dtype=torch.float32, device="cuda")
+    dit.nvfp4_to_int8(torch.from_numpy(D.pack_e2m1(codes)).cuda(), torch.from_numpy(F.sf_to_tiled(sf, 2, 64)).cuda(),
+                      torch.tensor([float(gd["s_g"][0])], device="cuda"), q, sc)
+    qh = host(q)
+    assert qh[0, :32].tolist() == [int(v) for v in gd["q_row0"]] and not qh[0, 32:].any()
+    assert not qh[1].any()
+    num, den = (np.float32(v) for v in gd["scale_row0"])
+    assert host(sc)[0] == num / den and host(sc)[1] == 0
+
+
+@pytest.mark.parametrize("container", ["bf16", "int8"])
+def test_routed_linear_nvfp4_only_weights(container, ws):
+    """A linear whose weights are resident in NVFP4 only: the INT8 route derives the INT8
+    weights on the fly; output against the oracle on the GPU's own quantised operands."""
+    m, k, n, hb = 300, 1920, 576, 64
+    x, xd = make_x(m, k, "bf16", seed=81)
+    w = synth.weights(n, k, seed=82)
+    wq = dit.QuantizedWeight(dev_f32(w), hb, ws, int8_container=container, nvfp4_only=True)
+    full = dit.QuantizedWeight(dev_f32(w), hb, ws, int8_container=container)
+    # NVFP4 (0.5625 B/weight) alone vs NVFP4 plus the INT8 copy (1 or 2 B/weight)
+    assert wq.int8 is None and wq.resident_bytes() * (4 if container == "bf16" else 2.5) < full.resident_bytes()
+    lin = dit.RoutedLinear(wq, m, ws)
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    lin(xd, dit.ROUTE_INT8, y)
+    _status_clean(ws)
+    w8 = D.nvfp4_weight_to_int8(D.unpack_e2m1(host(wq.nvfp4["codes"])), F.sf_from_tiled(host(wq.nvfp4["sf"]), n, k),
+                                host(wq.nvfp4["gs"])[0])
+    assert np.array_equal(_codes(lin.w8_scratch["q"]), w8["q"])
+    ref = D.gemm_int8(_codes(lin.a8["q"]), host(lin.a8["scale"]), w8["q"], w8["scale"])
+    assert rel_fro(host(y), ref) <= GEMM_TOL
+    # NVFP4 route of the same layer is unaffected
+    lin(xd, dit.ROUTE_NVFP4, y)
+    torch.cuda.synchronize()
+    ref4 = D.gemm_nvfp4(D.unpack_e2m1(host(lin.a4["codes"])), F.sf_from_tiled(host(lin.a4["sf"]), m, k),
+                        host(lin.a4["gs"])[0], D.unpack_e2m1(host(wq.nvfp4["codes"])),
+                        F.sf_from_tiled(host(wq.nvfp4["sf"]), n, k), host(wq.nvfp4["gs"])[0])
+    assert rel_fro(host(y), ref4) <= GEMM_TOL
+
+
 # ------------------------------------------------------------------------------ routed linear
 
 
