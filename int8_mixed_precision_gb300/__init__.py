@@ -194,6 +194,16 @@ class TdcState(ctypes.Structure):
         lib().dit_tdc_update(ctypes.byref(self), mode, float(gamma), float(sim if has else math.inf),
                              int(has))
 
+    def to_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+    @classmethod
+    def from_dict(cls, d: dict) -> "TdcState":
+        st = cls()
+        for name, _ in cls._fields_:
+            setattr(st, name, d[name])
+        return st
+
     def routes(self, alpha, beta, thr) -> list[int]:
         n = len(alpha)
         arr = ctypes.c_float * n
@@ -350,3 +360,23 @@ class DeltaCachedBlock:
         self.state.update(TDC_COMMIT, gamma, sim if self.had_delta else None)
         self.had_delta = True
         self.pending = False
+
+    def state_dict(self) -> dict:
+        """What resuming this block's delta cache needs: the decision state (host) and the
+        cached delta of the last computed step (copied to the host).  A commit must have been
+        absorbed first."""
+        if self.pending:
+            raise DitError("absorb the pending commit before saving the delta-cache state")
+        return {"tdc": self.state.to_dict(), "had_delta": self.had_delta,
+                "delta": self.d[0].detach().cpu() if self.had_delta else None,
+                "tau": self.tau, "alpha": list(self.alpha), "beta": list(self.beta), "thr": list(self.thr)}
+
+    def load_state_dict(self, sd: dict) -> None:
+        if sd["delta"] is not None and sd["delta"].numel() != self.d[0].numel():
+            raise DitError("delta-cache state of a different block size")
+        self.state = TdcState.from_dict(sd["tdc"])
+        self.had_delta = bool(sd["had_delta"])
+        self.pending = False
+        self.tau, self.alpha, self.beta, self.thr = sd["tau"], list(sd["alpha"]), list(sd["beta"]), list(sd["thr"])
+        if sd["delta"] is not None:
+            self.d[0].copy_(sd["delta"].to(self.d[0].dtype))

@@ -153,3 +153,23 @@ def test_workspace_and_version(L):
     assert L.dit_workspace_bytes() >= 33 * 1024
     assert L.dit_ws_status_offset() == 0
     assert L.dit_version().decode().count(".") == 2
+
+
+def test_tdc_state_round_trip(L):
+    """The delta-cache decision state survives to_dict / from_dict: a restored copy makes the
+    same decisions as the original from then on."""
+    import int8_mixed_precision_gb300 as dit
+    st = dit.TdcState()
+    seq = [(0, 0.11, None), (0, 0.07, 0.02), (1,), (0, 0.05, 0.01)]
+    for ev in seq:
+        if ev[0] == dit.TDC_SKIP:
+            st.update(dit.TDC_SKIP)
+        else:
+            st.update(dit.TDC_COMMIT, ev[1], ev[2])
+    cp = dit.TdcState.from_dict(st.to_dict())
+    assert cp.to_dict() == st.to_dict()
+    for tau in (0.005, 0.02, 0.1):
+        assert cp.decide(tau) == st.decide(tau)
+    for s_ in (st, cp):
+        s_.update(dit.TDC_SKIP)
+    assert cp.to_dict() == st.to_dict() and cp.routes([1.0], [0.0], [0.05]) == st.routes([1.0], [0.0], [0.05])

@@ -699,3 +699,49 @@ def test_gemm_bounded_wait_reports_timeout_and_recovers(route, monkeypatch):
     torch.cuda.synchronize()
     assert dit.device_status(ws2) == 0
     assert rel_fro(host(y), ref) <= GEMM_TOL
+
+
+def test_delta_cache_checkpoint_resume(ws):
+    """A block's delta cache saved mid-run (decision state + cached delta) and loaded into a
+    fresh block continues exactly like the original: same decisions, same outputs bit for bit."""
+    n, steps, cut = 4096 + 32, 10, 4
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    x_in = torch.randn(n, generator=g, device="cuda").to(torch.bfloat16)
+    base = torch.randn(n, generator=g, device="cuda") * 0.05
+    deltas = [(base * (1 + 0.002 * t)).to(torch.bfloat16) for t in range(steps)]
+    gam = torch.zeros(2, dtype=torch.float32, device="cuda")
+    sim = torch.zeros(2, dtype=torch.float32, device="cuda")
+
+    def make(slot):
+        return dit.DeltaCachedBlock(n, torch.bfloat16, 0.007, [1.0], [0.0], [0.05], ws, gam[slot:slot + 1],
+                                    sim[slot:slot + 1])
+
+    def run(blk, slot, t0, t1):
+        trace = []
+        for t in range(t0, t1):
+            out = torch.empty_like(x_in)
+            mode = blk.decide()
+            if mode == dit.TDC_SKIP:
+                blk.skip(x_in, out)
+            else:
+                out.copy_((x_in.float() + deltas[t].float()).to(torch.bfloat16))
+                blk.commit(x_in, out)
+                torch.cuda.synchronize()
+                blk.absorb(float(gam[slot]), float(sim[slot]))
+            trace.append((mode, blk.routes(), out.clone()))
+        return trace
+
+    a = make(0)
+    run(a, 0, 0, cut)
+    sd = a.state_dict()
+    rest_a = run(a, 0, cut, steps)
+    b = make(1)
+    b.load_state_dict(sd)
+    rest_b = run(b, 1, cut, steps)
+    modes = [m for m, _, _ in rest_a]
+    assert modes == [m for m, _, _ in rest_b] and dit.TDC_SKIP in modes and dit.TDC_COMMIT in modes
+    assert [r for _, r, _ in rest_a] == [r for _, r, _ in rest_b]
+    for (_, _, oa), (_, _, ob) in zip(rest_a, rest_b):
+        assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+    _status_clean(ws)
