@@ -34,6 +34,7 @@ from . import formats as F
 
 ROUTE_NVFP4 = 0
 ROUTE_INT8 = 1
+ROUTE_BF16 = 2
 
 # ----------------------------------------------------------------------------------------
 # Gamma predictor and routing
@@ -72,6 +73,28 @@ def route_layers(gamma: float | None, alpha, beta, thr) -> list[int]:
         return [ROUTE_INT8] * n
     e = alpha * float(gamma) + beta
     return [ROUTE_INT8 if e[i] > thr[i] else ROUTE_NVFP4 for i in range(n)]
+
+
+def outlier_ratio(x: np.ndarray, k_sigma: float = 6.0) -> float:
+    """Fraction of the elements of a block activation with |x| > k_sigma * RMS(x), float64.
+
+    gist.science EN 2.C (first bullet) and ZH 2.C: PDR forces full precision when a layer's
+    input has a high outlier ratio, which the pages do not define.  Reading: RMS over the
+    whole tensor, k_sigma = 6, strict >.  An empty or all-zero tensor has ratio 0.
+    """
+    x = np.asarray(x, np.float64).ravel()
+    if x.size == 0:
+        return 0.0
+    rms = math.sqrt(float(np.sum(x * x)) / x.size)
+    return float(np.count_nonzero(np.abs(x) > k_sigma * rms)) / x.size
+
+
+def route_layers_pdr(gamma: float | None, alpha, beta, thr, ratio: float, rho: float) -> list[int]:
+    """route_layers, overridden by the outlier-ratio rule of PDR (EN 2.C, ZH 2.C): a block whose
+    input's outlier ratio exceeds rho (strict >) runs every layer in BF16.  rho = +inf turns
+    the override off (the default of the workloads)."""
+    routes = route_layers(gamma, alpha, beta, thr)
+    return [ROUTE_BF16] * len(routes) if ratio > rho else routes
 
 
 def route_margin(gamma: float, alpha: float, beta: float, thr: float) -> float:
@@ -290,6 +313,14 @@ def gemm_nvfp4(a_codes, a_sf, a_sg, b_codes, b_sf, b_sg, bias=None) -> np.ndarra
     ad = dequant_nvfp4(a_codes, a_sf, 1.0)
     bd = dequant_nvfp4(b_codes, b_sf, 1.0)
     y = (ad @ bd.T) * (float(a_sg) * float(b_sg))
+    if bias is not None:
+        y = y + np.asarray(bias, np.float64)[None, :]
+    return y
+
+
+def gemm_bf16(x: np.ndarray, w: np.ndarray, bias=None) -> np.ndarray:
+    """BF16 route (PDR full precision): Y = X W^T on the untransformed bf16 operands, float64."""
+    y = np.asarray(x, np.float64) @ np.asarray(w, np.float64).T
     if bias is not None:
         y = y + np.asarray(bias, np.float64)[None, :]
     return y

@@ -596,3 +596,49 @@ def test_planted_wrong_block_scale_index_is_caught():
     g, codes, sf, sg = _golden_nvfp4_to_int8()
     r = D.nvfp4_weight_to_int8(codes, sf[:, ::-1].copy(), sg)     # the blocks' scales swapped
     assert r["q"][0].tolist() != [int(v) for v in g["q_row0"]]
+
+
+# ----------------------------------------------------------------------------------------
+# PDR outlier ratio and the BF16 route
+# ----------------------------------------------------------------------------------------
+
+
+def test_outlier_ratio_hand_counted():
+    """n = 1000 values: 990 ones and 10 spikes of 40.  Sum of squares 990 + 10 * 1600 = 16990,
+    RMS = sqrt(16.99) = 4.1219, 6 RMS = 24.73: the 10 spikes exceed it, the ones do not."""
+    x = np.ones(1000)
+    x[::100] = 40.0
+    assert D.outlier_ratio(x) == 10 / 1000
+    x[::100] = -40.0                                  # the sign does not matter
+    assert D.outlier_ratio(x) == 10 / 1000
+    # spikes of 20 (< 6 RMS = 6 sqrt((990 + 4000) / 1000) = 13.40)? 20 > 13.40: still outliers
+    x[::100] = 20.0
+    assert D.outlier_ratio(x) == 10 / 1000
+    # spikes of 5: RMS = sqrt((990 + 250) / 1000) = 1.1136, 6 RMS = 6.68 > 5: none
+    x[::100] = 5.0
+    assert D.outlier_ratio(x) == 0.0
+    assert D.outlier_ratio(np.zeros(7)) == 0.0 and D.outlier_ratio(np.zeros(0)) == 0.0
+    # spikes of 7 sit between 6 mean|x| (6.36) and 6 RMS (6 sqrt(1.48) = 7.30): an RMS rule
+    # counts none, a mean-|x| rule would count all ten
+    x[::100] = 7.0
+    assert D.outlier_ratio(x) == 0.0
+
+
+def test_outlier_ratio_gaussian_tail():
+    """For N(0,1) data RMS -> 1, and the ratio at k = 2 tends to P(|Z| > 2) = 0.0455 (tables)."""
+    z = synth.rng(73).standard_normal(2_000_000)
+    assert D.outlier_ratio(z, 2.0) == pytest.approx(0.0455, abs=1.5e-3)
+
+
+def test_route_layers_pdr_override():
+    assert D.route_layers_pdr(0.01, [1, 1], [0, 0], [0.05, 0.05], 0.02, 0.01) == [D.ROUTE_BF16] * 2
+    assert D.route_layers_pdr(0.01, [1, 1], [0, 0], [0.05, 0.05], 0.01, 0.01) == [D.ROUTE_NVFP4] * 2  # strict >
+    assert D.route_layers_pdr(None, [1], [0], [0.05], 0.0, math.inf) == [D.ROUTE_INT8]
+
+
+def test_gemm_bf16_small_brute_force():
+    x = np.array([[1.0, 2.0, -1.0], [0.5, 0.0, 4.0]])
+    w = np.array([[1.0, 1.0, 1.0], [2.0, -1.0, 0.25], [0.0, 3.0, -2.0], [1.0, 0.0, 0.0]])
+    want = np.array([[2.0, -0.25, 8.0, 1.0], [4.5, 2.0, -8.0, 0.5]])        # worked by hand
+    assert np.array_equal(D.gemm_bf16(x, w), want)
+    assert np.array_equal(D.gemm_bf16(x, w, bias=np.array([1.0, 0, 0, -1])), want + [1.0, 0, 0, -1])
