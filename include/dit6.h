@@ -48,7 +48,7 @@ typedef enum {
 } dit_status;
 
 typedef enum { DIT_F32 = 0, DIT_BF16 = 1, DIT_I8 = 2 } dit_dtype;
-typedef enum { DIT_ROUTE_NVFP4 = 0, DIT_ROUTE_INT8 = 1 } dit_route;
+typedef enum { DIT_ROUTE_NVFP4 = 0, DIT_ROUTE_INT8 = 1, DIT_ROUTE_BF16 = 2 } dit_route;
 typedef enum { DIT_TDC_COMMIT = 0, DIT_TDC_SKIP = 1 } dit_tdc_mode;
 /* Activation applied in the GEMM epilogue after the bias: none, or GELU in its erf form
  * x * Phi(x) (the FFN activation between the up and down projections of the CogVideoX-shaped
@@ -221,6 +221,29 @@ dit_status dit_qgemm_nvfp4_fused_quant(const uint8_t* a, const uint8_t* a_sf, co
                                        void* ws, size_t ws_bytes, dit_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * PDR outlier ratio and the BF16 route.  [EN] 2.C first bullet, [ZH] 2.C: a layer whose
+ * input has a high outlier ratio runs in full precision.  The pages do not define the
+ * ratio; reading: the fraction of elements with |x| > k_sigma * RMS(x) over the whole block
+ * input (k_sigma = 6 in the workloads), strict >.
+ *
+ * dit_outlier_ratio: two passes (sum of squares, fixed-order fp64 reduction -> threshold
+ * k_sigma * sqrt(sum / n); then the count of |x| > threshold).  ratio_dev: device float
+ * (count / n); count_dev: device int64 or NULL.  x: device [n] of dtype dt, 32-byte aligned.
+ *
+ * dit_gemm_bf16: Y = act(X W^T (+ bias)) on untransformed bf16 operands (the BF16 route),
+ * fp32 accumulation.  x [m x k], w [n x k] bf16 K-major; k % 16 == 0, n % 8 == 0; bias
+ * device float [n] (16-byte aligned) or NULL.
+ *
+ * dit_route_host_pdr: dit_route_host, except that outlier_ratio > rho sends every layer to
+ * DIT_ROUTE_BF16 (rho = +inf: no override).
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_outlier_ratio(const void* x, dit_dtype dt, int64_t n, float k_sigma, float* ratio_dev,
+                             int64_t* count_dev, void* ws, size_t ws_bytes, dit_stream_t stream);
+dit_status dit_gemm_bf16(const void* x, const void* w, int64_t m, int64_t n, int64_t k,
+                         const float* bias, dit_act act, void* y, dit_dtype y_dt, void* ws,
+                         size_t ws_bytes, dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * (a7) INT8 GEMM: exact int32 accumulation, per-row x per-column dequantisation.
  * [EN] 2.A Mechanism 3 (INT8 route); [ZH] 2.A weight handling.
  *
@@ -280,6 +303,9 @@ int dit_tdc_decide(const dit_tdc_state* st, double tau); /* returns dit_tdc_mode
 void dit_tdc_update(dit_tdc_state* st, int mode, double gamma, double sim, int has_sim);
 void dit_route_host(const dit_tdc_state* st, const float* alpha, const float* beta,
                     const float* thr, int n_layers, int32_t* routes);
+void dit_route_host_pdr(const dit_tdc_state* st, const float* alpha, const float* beta,
+                        const float* thr, int n_layers, double outlier_ratio, double rho,
+                        int32_t* routes);
 
 /* ------------------------------------------------------------------------------------
  * Block-scale tile layout helpers (host).  The scales of a [rows x k] NVFP4 tensor are

@@ -15,6 +15,7 @@ from ._lib import LibraryMissing, lib, library_path  # noqa: F401
 
 ROUTE_NVFP4 = 0
 ROUTE_INT8 = 1
+ROUTE_BF16 = 2
 TDC_COMMIT = 0
 TDC_SKIP = 1
 ACT_NONE = 0
@@ -204,11 +205,16 @@ class TdcState(ctypes.Structure):
             setattr(st, name, d[name])
         return st
 
-    def routes(self, alpha, beta, thr) -> list[int]:
+    def routes(self, alpha, beta, thr, outlier_ratio: float | None = None, rho: float = math.inf) -> list[int]:
+        """Routes from Gamma; with an outlier ratio above rho every layer goes to BF16 (PDR)."""
         n = len(alpha)
         arr = ctypes.c_float * n
         out = (ctypes.c_int32 * n)()
-        lib().dit_route_host(ctypes.byref(self), arr(*alpha), arr(*beta), arr(*thr), n, out)
+        if outlier_ratio is None:
+            lib().dit_route_host(ctypes.byref(self), arr(*alpha), arr(*beta), arr(*thr), n, out)
+        else:
+            lib().dit_route_host_pdr(ctypes.byref(self), arr(*alpha), arr(*beta), arr(*thr), n,
+                                     float(outlier_ratio), float(rho), out)
         return list(out)
 
 
@@ -232,6 +238,22 @@ def alloc_int8(rows: int, k: int, device="cuda", container: str = "bf16") -> dic
             "scale": torch.empty(rows, dtype=torch.float32, device=device)}
 
 
+def outlier_ratio(x, ws, ratio, count=None, k_sigma: float = 6.0, stream=None):
+    """ratio (device float [1]) = fraction of |x| > k_sigma * RMS(x); count (device int64 [1])."""
+    st = lib().dit_outlier_ratio(_p(x), _dt(x), x.numel(), float(k_sigma), _p(ratio), _p(count), _p(ws),
+                                 ws.numel(), _stream(stream))
+    _check(st, "dit_outlier_ratio")
+
+
+def gemm_bf16(x, w, y, ws, bias=None, act=ACT_NONE, stream=None):
+    """The BF16 route: y = act(x w^T (+ bias)) on untransformed bf16 operands."""
+    m, k = x.shape
+    n = w.shape[0]
+    st = lib().dit_gemm_bf16(_p(x), _p(w), m, n, k, _p(bias), act, _p(y), _dt(y), _p(ws), ws.numel(),
+                             _stream(stream))
+    _check(st, "dit_gemm_bf16")
+
+
 def nvfp4_to_int8(codes, sf, tensor_scale, q, row_scale, stream=None):
     """Per-output-channel INT8 (int8 or bf16-held codes in q) of NVFP4 weights [rows x K]."""
     rows, k = codes.shape[0], codes.shape[1] * 2
@@ -245,10 +267,13 @@ class QuantizedWeight:
     per-output-channel INT8 copy, all on the device.  nvfp4_only=True keeps the NVFP4 copy
     alone; the INT8 weights are then derived from it when a layer routes INT8 (int8_into)."""
 
-    def __init__(self, w, hblock: int, ws, int8_container: str = "bf16", nvfp4_only: bool = False):
+    def __init__(self, w, hblock: int, ws, int8_container: str = "bf16", nvfp4_only: bool = False,
+                 keep_bf16: bool = False):
+        """keep_bf16: also keep the untransformed weight in bf16, for the BF16 route of PDR."""
         n, k = w.shape
         self.n, self.k, self.hblock = n, k, hblock
         self.int8_container = int8_container
+        self.bf16 = w.to(_torch().bfloat16).contiguous() if keep_bf16 else None
         self.nvfp4 = alloc_nvfp4(n, k, w.device)
         hadamard_quant_nvfp4(w, hblock, self.nvfp4["codes"], self.nvfp4["sf"], self.nvfp4["gs"], ws)
         self.int8 = None
@@ -264,7 +289,8 @@ class QuantizedWeight:
         return other
 
     def resident_bytes(self) -> int:
-        tensors = list(self.nvfp4.values()) + (list(self.int8.values()) if self.int8 else [])
+        tensors = list(self.nvfp4.values()) + (list(self.int8.values()) if self.int8 else []) + \
+            ([self.bf16] if self.bf16 is not None else [])
         return sum(t.numel() * t.element_size() for t in tensors)
 
     def int8_into(self, scratch, stream=None) -> dict:
@@ -298,6 +324,12 @@ class RoutedLinear:
     def __call__(self, x, route: int, y, bias=None, tensor_scale_in=None, act=ACT_NONE, stream=None):
         m = x.shape[0]
         w = self.w
+        if route == ROUTE_BF16:
+            if w.bf16 is None:
+                raise DitError("BF16 route needs QuantizedWeight(..., keep_bf16=True)")
+            gemm_bf16(x if x.dtype == _torch().bfloat16 else x.to(_torch().bfloat16), w.bf16, y, self.ws, bias=bias,
+                      act=act, stream=stream)
+            return y
         if route == ROUTE_INT8:
             q, s = self.a8["q"][:m], self.a8["scale"][:m]
             hadamard_quant_int8(x, w.hblock, q, s, stream=stream)
@@ -339,8 +371,10 @@ class DeltaCachedBlock:
     def decide(self) -> int:
         return self.state.decide(self.tau)
 
-    def routes(self) -> list[int]:
-        return self.state.routes(self.alpha, self.beta, self.thr)
+    def routes(self, outlier_ratio: float | None = None, rho: float = math.inf) -> list[int]:
+        """Routes of this block's layers; with outlier_ratio (the block input's, from
+        outlier_ratio()) above rho every layer runs BF16 (PDR)."""
+        return self.state.routes(self.alpha, self.beta, self.thr, outlier_ratio, rho)
 
     def skip(self, x_in, x_out, stream=None):
         tdc_step(TDC_SKIP, x_in.reshape(-1), self.ws, x_out_skip=x_out.reshape(-1), d1=self.d[0], stream=stream)

@@ -41,6 +41,10 @@ SIGNATURES = {
     "dit_tdc_decide": (_i32, [_vp, ctypes.c_double]),
     "dit_tdc_update": (None, [_vp, _i32, ctypes.c_double, ctypes.c_double, _i32]),
     "dit_route_host": (None, [_vp, _f, _f, _f, _i32, ctypes.POINTER(ctypes.c_int32)]),
+    "dit_route_host_pdr": (None, [_vp, _f, _f, _f, _i32, ctypes.c_double, ctypes.c_double,
+                                  ctypes.POINTER(ctypes.c_int32)]),
+    "dit_outlier_ratio": (_i32, [_vp, _i32, _i64, ctypes.c_float, _vp, _vp, _vp, _sz, _vp]),
+    "dit_gemm_bf16": (_i32, [_vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _sz, _vp]),
     "dit_sf_index": (_i64, [_i64, _i64, _i64, _i64]),
     "dit_sf_bytes": (_sz, [_i64, _i64]),
 }

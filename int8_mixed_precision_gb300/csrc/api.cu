@@ -145,4 +145,14 @@ void dit_route_host(const dit_tdc_state* st, const float* alpha, const float* be
   }
 }
 
+void dit_route_host_pdr(const dit_tdc_state* st, const float* alpha, const float* beta, const float* thr,
+                        int n_layers, double outlier_ratio, double rho, int32_t* routes) {
+  if (!routes || n_layers <= 0) return;
+  if (outlier_ratio > rho) {
+    for (int l = 0; l < n_layers; ++l) routes[l] = DIT_ROUTE_BF16;
+    return;
+  }
+  dit_route_host(st, alpha, beta, thr, n_layers, routes);
+}
+
 }  // extern "C"

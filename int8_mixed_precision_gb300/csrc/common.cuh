@@ -18,6 +18,7 @@ constexpr size_t WS_STATUS = 0;      // uint32: OR of (1 << dit_status) raised o
 constexpr size_t WS_TICKET = 4;      // uint32: CTA completion counter (reset by last CTA)
 constexpr size_t WS_AMAX = 8;        // uint32: float bits of a running amax (reset)
 constexpr size_t WS_SG = 12;         // float : tensor scale produced by the amax pass
+constexpr size_t WS_THR = 16;        // double: outlier threshold k * RMS from the first pass
 constexpr size_t WS_PARTIALS = 256;  // double[MAX_RED_CTAS][4]
 constexpr int MAX_RED_CTAS = 1024;
 // split-K tail of the INT8 GEMM: one uint32 arrival ticket per (split tile, epilogue warp),

@@ -507,11 +507,14 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
       : "memory");
 }
 
-// F2: K spans at most two exact chunks and no raw accumulators are requested.  Each chunk sum
-// is then an exact fp32 integer and one fp32 addition rounds their exact total once, as the
-// conversion of the int32 total to fp32 does, so the chunks are summed in fp32 and the output
-// is the same bit for bit without the int32 round trip.
-template <bool GELU, bool F2>
+// ACCM 0: INT8 codes, exact chunks summed in int32.
+// ACCM 1: INT8 codes, K spans at most two exact chunks and no raw accumulators are requested.
+//         Each chunk sum is then an exact fp32 integer and one fp32 addition rounds their exact
+//         total once, as the conversion of the int32 total to fp32 does, so the chunks are
+//         summed in fp32 and the output is the same bit for bit without the int32 round trip.
+// ACCM 2: a plain bf16 GEMM (the BF16 route of PDR): fp32 accumulation over the whole K in one
+//         tensor-memory chunk, no scales.
+template <bool GELU, int ACCM>
 __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     k_gemm_int8_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N, int K,
@@ -540,7 +543,9 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
   auto tile_m0 = [&](int item) { return (item / n_tiles_n) * 256; };
   auto tile_n0 = [&](int item) { return (item % n_tiles_n) * 256; };
   const int nkb = (K + BK - 1) / BK;
-  const int nchunks = (nkb + KCHUNK_BLOCKS - 1) / KCHUNK_BLOCKS;
+  // exactness chunks of the INT8 modes; the bf16 mode accumulates all of K in one chunk
+  const int kchunk = ACCM == 2 ? nkb : KCHUNK_BLOCKS;
+  const int nchunks = ACCM == 2 ? 1 : (nkb + KCHUNK_BLOCKS - 1) / KCHUNK_BLOCKS;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -608,8 +613,8 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d = tmem + buf * 256;
-          const int kb0 = ch * KCHUNK_BLOCKS;
-          const int kb1 = min(nkb, kb0 + KCHUNK_BLOCKS);
+          const int kb0 = ch * kchunk;
+          const int kb1 = min(nkb, kb0 + kchunk);
           for (int kb = kb0; kb < kb1; ++kb, ++kc) {
             const int s = kc % S;
             if (!mbar_wait_cl(full(s), (kc / S) & 1, ws, abort_flag)) {
@@ -659,7 +664,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
           tc_ld32(base + c * 32, r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            if constexpr (F2)  // acc starts as +0.0f, and 0 + c0 = c0 exactly
+            if constexpr (ACCM >= 1)  // acc starts as +0.0f, and 0 + c0 = c0 exactly
               acc[c * 32 + i] = __float_as_int(__fadd_rn(__int_as_float(acc[c * 32 + i]), __uint_as_float(r[i])));
             else
               acc[c * 32 + i] += __float2int_rn(__uint_as_float(r[i]));
@@ -673,23 +678,27 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
       const int row = m0 + q * 32 + lane;
       const int col0 = n0 + half * CW;
       if (row < M && col0 < N) {
-        const float sa = a_scale[row];
+        const float sa = ACCM == 2 ? 1.0f : a_scale[row];
         const int64_t off = (int64_t)row * N + col0;
 #pragma unroll
         for (int c = 0; c < CW / 16; ++c) {
           const int cb = col0 + c * 16;
           if (cb >= N) break;
           float v[16];
-          auto accf = [&](int i) { return F2 ? __int_as_float(acc[c * 16 + i]) : (float)acc[c * 16 + i]; };
+          auto accf = [&](int i) { return ACCM >= 1 ? __int_as_float(acc[c * 16 + i]) : (float)acc[c * 16 + i]; };
           if (cb + 16 <= N) {  // packed: (acc * sa) * sb (+ bias), each product rounded as before
             const float4* sb4 = reinterpret_cast<const float4*>(b_scale + cb);
             const float4* bi4 = reinterpret_cast<const float4*>(bias + cb);
             const float2 sa2 = make_float2(sa, sa);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const float4 sb = sb4[j];
-              float2 lo = mul2(mul2(make_float2(accf(4 * j), accf(4 * j + 1)), sa2), make_float2(sb.x, sb.y));
-              float2 hi = mul2(mul2(make_float2(accf(4 * j + 2), accf(4 * j + 3)), sa2), make_float2(sb.z, sb.w));
+              float2 lo = make_float2(accf(4 * j), accf(4 * j + 1));
+              float2 hi = make_float2(accf(4 * j + 2), accf(4 * j + 3));
+              if constexpr (ACCM != 2) {
+                const float4 sb = sb4[j];
+                lo = mul2(mul2(lo, sa2), make_float2(sb.x, sb.y));
+                hi = mul2(mul2(hi, sa2), make_float2(sb.z, sb.w));
+              }
               if (bias) {
                 const float4 bb = bi4[j];
                 lo = add2(lo, make_float2(bb.x, bb.y));
@@ -704,7 +713,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int col = cb + i < N ? cb + i : N - 1;
-              v[i] = __fmul_rn(__fmul_rn(accf(i), sa), b_scale[col]);
+              v[i] = ACCM == 2 ? accf(i) : __fmul_rn(__fmul_rn(accf(i), sa), b_scale[col]);
               if (bias) v[i] = __fadd_rn(v[i], bias[col]);
             }
           }
@@ -766,7 +775,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
   }
 }
 
-template <bool GELU, bool F2>
+template <bool GELU, int ACCM>
 dit_status launch_pair(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
                        int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out, void* ws,
                        cudaStream_t st) {
@@ -777,7 +786,7 @@ dit_status launch_pair(const void* a, const float* a_scale, const void* b, const
       !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(b), (uint64_t)k, (uint64_t)n,
                       (uint64_t)k * 2, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return DIT_ERR_CUDA;
-  auto kern = k_gemm_int8_pair<GELU, F2>;
+  auto kern = k_gemm_int8_pair<GELU, ACCM>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES) != cudaSuccess)
@@ -921,10 +930,10 @@ dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, cons
   {
     const bool f2 = !acc_out && (k + 1023) / 1024 <= 2;
     if (f2)
-      return g ? i8tc::launch_pair<true, true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
-               : i8tc::launch_pair<false, true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
-    return g ? i8tc::launch_pair<true, false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
-             : i8tc::launch_pair<false, false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
+      return g ? i8tc::launch_pair<true, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
+               : i8tc::launch_pair<false, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
+    return g ? i8tc::launch_pair<true, 0>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
+             : i8tc::launch_pair<false, 0>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
   }
 #define DIT6_I8TC(BN_, MC_)                                                                          \
   return g ? i8tc::launch<BN_, MC_, true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, ws_bytes, st) \
@@ -937,3 +946,25 @@ dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, cons
 }
 
 }  // namespace dit6
+
+// BF16 route of PDR ([EN] 2.C, [ZH] 2.C: full precision for a block whose input has a high
+// outlier ratio): Y = act(X W^T (+ bias)) on the untransformed bf16 operands, fp32 accumulation,
+// on the CTA-pair kernel in its bf16 mode.
+extern "C" dit_status dit_gemm_bf16(const void* x, const void* w, int64_t m, int64_t n, int64_t k, const float* bias,
+                                    dit_act act, void* y, dit_dtype y_dt, void* ws, size_t ws_bytes,
+                                    dit_stream_t stream) {
+  using namespace dit6;
+  if (!x || !w || !y || !ws || ws_bytes < WS_BYTES) return DIT_ERR_INVALID_ARG;
+  if (m <= 0 || n <= 0 || k <= 0 || m > 0x7fffffff || n > 0x7fffffff || k > 0x7fffffff) return DIT_ERR_INVALID_ARG;
+  if (y_dt != DIT_F32 && y_dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
+  if (act != DIT_ACT_NONE && act != DIT_ACT_GELU_ERF) return DIT_ERR_INVALID_ARG;
+  if (k % 16 || n % 8) return DIT_ERR_UNSUPPORTED;
+  if (!aligned32(x) || !aligned32(w) || !aligned32(y) || !aligned32(ws) ||
+      (bias && (reinterpret_cast<uintptr_t>(bias) & 15)))
+    return DIT_ERR_ALIGNMENT;
+  const int epi = (y_dt == DIT_BF16 ? EPI_BF16 : 0) | (act == DIT_ACT_GELU_ERF ? EPI_GELU : 0);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return act == DIT_ACT_GELU_ERF
+             ? dit6::i8tc::launch_pair<true, 2>(x, nullptr, w, nullptr, m, n, k, bias, y, epi, nullptr, ws, st)
+             : dit6::i8tc::launch_pair<false, 2>(x, nullptr, w, nullptr, m, n, k, bias, y, epi, nullptr, ws, st);
+}

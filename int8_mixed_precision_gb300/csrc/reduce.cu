@@ -191,6 +191,56 @@ __global__ void __launch_bounds__(RED_THREADS) k_gamma_route(const void* __restr
   }
 }
 
+// PDR outlier ratio ([EN] 2.C, [ZH] 2.C; reading: the fraction of |x| > k * RMS(x) over the
+// whole block input).  Pass 1: sum of squares (per-thread fp32, CTA and final sums in fp64,
+// fixed order) -> threshold k * sqrt(sum / n) in fp64 in the workspace.  Pass 2: count of
+// |x| > threshold (integers, exact in the fp32/fp64 partial sums) -> count and count / n.
+template <typename T>
+__global__ void __launch_bounds__(RED_THREADS) k_sumsq(const void* __restrict__ x, int64_t n, float k_sigma,
+                                                       void* ws) {
+  constexpr int N = Vec<T>::N;
+  const int64_t nv = n / N;
+  float s[1] = {0.f};
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+    float a[N];
+    Vec<T>::load(x, i, a);
+#pragma unroll
+    for (int k = 0; k < N; ++k) s[0] = fmaf(a[k], a[k], s[0]);
+  }
+  for (int64_t i = nv * N + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float a = Vec<T>::scalar(x, i);
+    s[0] = fmaf(a, a, s[0]);
+  }
+  double r[1];
+  if (!reduce_partials<1>(s, ws, r)) return;
+  *reinterpret_cast<double*>(reinterpret_cast<char*>(ws) + WS_THR) = (double)k_sigma * sqrt(r[0] / (double)n);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(RED_THREADS) k_count_over(const void* __restrict__ x, int64_t n, void* ws,
+                                                            float* ratio_out, int64_t* count_out) {
+  constexpr int N = Vec<T>::N;
+  const double thr = *reinterpret_cast<const double*>(reinterpret_cast<const char*>(ws) + WS_THR);
+  const int64_t nv = n / N;
+  uint32_t c = 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+    float a[N];
+    Vec<T>::load(x, i, a);
+#pragma unroll
+    for (int k = 0; k < N; ++k) c += (double)fabsf(a[k]) > thr ? 1u : 0u;
+  }
+  for (int64_t i = nv * N + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    c += (double)fabsf(Vec<T>::scalar(x, i)) > thr ? 1u : 0u;
+  const float s[1] = {(float)c};  // per-thread counts stay far below 2^24: exact
+  double r[1];
+  if (!reduce_partials<1>(s, ws, r)) return;
+  const int64_t count = (int64_t)r[0];
+  if (count_out) *count_out = count;
+  *ratio_out = (float)((double)count / (double)n);
+}
+
 // COMMIT: delta = store(xo - xi) -> dnew; sums |xo-xi|, |xi|, |delta - d1|, |d1|
 template <typename T>
 __global__ void __launch_bounds__(RED_THREADS) k_tdc_commit(const void* __restrict__ xi,
@@ -432,6 +482,25 @@ extern "C" dit_status dit_gamma_route_noalloc(const void* x_in, const void* x_ou
   else
     k_gamma_route<float><<<grid, RED_THREADS, 0, st>>>(x_in, x_out, n, rp, gamma_dev,
                                                        routes_dev, scratch);
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
+extern "C" dit_status dit_outlier_ratio(const void* x, dit_dtype dt, int64_t n, float k_sigma, float* ratio_dev,
+                                        int64_t* count_dev, void* ws, size_t ws_bytes, dit_stream_t stream) {
+  if (!x || n <= 0 || !ratio_dev || !ws || ws_bytes < WS_BYTES || !(k_sigma >= 0.f)) return DIT_ERR_INVALID_ARG;
+  if (dt != DIT_F32 && dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
+  if (!aligned32(x) || !aligned32(ws)) return DIT_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == DIT_BF16) {
+    const unsigned g = red_grid(n, 16);
+    k_sumsq<__nv_bfloat16><<<g, RED_THREADS, 0, st>>>(x, n, k_sigma, ws);
+    k_count_over<__nv_bfloat16><<<g, RED_THREADS, 0, st>>>(x, n, ws, ratio_dev, count_dev);
+  } else {
+    const unsigned g = red_grid(n, 8);
+    k_sumsq<float><<<g, RED_THREADS, 0, st>>>(x, n, k_sigma, ws);
+    k_count_over<float><<<g, RED_THREADS, 0, st>>>(x, n, ws, ratio_dev, count_dev);
+  }
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }

@@ -4,7 +4,8 @@
 
 Cases: quant_int8, quant_nvfp4 (two passes), quant_nvfp4_given (one pass, tensor scale
 given), gamma, tdc_commit, tdc_skip, gemm_int8, gemm_nvfp4, ffn_nvfp4_fused / ffn_nvfp4_unfused
-(FFN up + GELU + quantisation for the next NVFP4 layer).  Inputs are synthetic bf16
+(FFN up + GELU + quantisation for the next NVFP4 layer), outlier_ratio and gemm_bf16 (the
+PDR full-precision route).  Inputs are synthetic bf16
 activations (N(0,1), 1% outlier channels x50) and N(0,0.02) weights.  Prints one JSON line
 with the median time and the algorithmic rate (GB/s for streaming kernels, TFLOP/s for
 GEMMs).  Also the small cases used for ncu captures.
@@ -98,6 +99,18 @@ def main(argv=None):
                 dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], W["codes"], W["sf"], W["gs"], y, ws,
                                 act=dit.ACT_GELU_ERF)
                 dit.hadamard_quant_nvfp4(y, a.hblock, q["codes"], q["sf"], q["gs"], ws)
+        units, unit = 2 * m * n * k, "TFLOP/s"
+    elif case == "outlier_ratio":
+        x = act(m, k)
+        r = torch.empty(1, dtype=torch.float32, device=dev)
+        fn = lambda: dit.outlier_ratio(x, ws, r)
+        units, unit = m * k * 2, "GB/s"     # one algorithmic read of the activation (the kernel reads it twice)
+    elif case == "gemm_bf16":
+        x = act(m, k)
+        w = (torch.randn(n, k, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+        y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        act_code = dit.ACT_GELU_ERF if a.act == "gelu" else dit.ACT_NONE
+        fn = lambda: dit.gemm_bf16(x, w, y, ws, act=act_code)
         units, unit = 2 * m * n * k, "TFLOP/s"
     elif case in ("gemm_int8", "gemm_nvfp4"):
         x = act(m, k)

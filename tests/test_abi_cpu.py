@@ -36,7 +36,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["dit_gamma_route", "dit_hadamard_quant_nvfp4", "dit_hadamard_quant_int8",
-              "dit_qgemm_nvfp4", "dit_qgemm_nvfp4_fused_quant", "dit_nvfp4_to_int8", "dit_qgemm_int8", "dit_tdc_step", "dit_sf_index", "dit_status_str"]:
+              "dit_qgemm_nvfp4", "dit_qgemm_nvfp4_fused_quant", "dit_nvfp4_to_int8", "dit_qgemm_int8",
+              "dit_outlier_ratio", "dit_gemm_bf16", "dit_route_host_pdr", "dit_tdc_step", "dit_sf_index", "dit_status_str"]:
         assert n in names
 
 
@@ -91,6 +92,12 @@ def test_host_argument_validation_without_device_work(L):
     assert L.dit_nvfp4_to_int8(nul, ws, ws, 4, 128, ws, 2, ws, nul) == 1
     assert L.dit_nvfp4_to_int8(ws, ws, ws, 4, 96, ws, 2, ws, nul) == 3
     assert L.dit_nvfp4_to_int8(fake_misaligned, ws, ws, 4, 128, ws, 2, ws, nul) == 2
+    # outlier ratio: null output, negative k; BF16 GEMM: n not a multiple of 8, misaligned bias
+    assert L.dit_outlier_ratio(ws, 1, 64, 6.0, nul, nul, ws, wsb, nul) == 1
+    assert L.dit_outlier_ratio(ws, 1, 64, -1.0, ws, nul, ws, wsb, nul) == 1
+    assert L.dit_outlier_ratio(fake_misaligned, 1, 64, 6.0, ws, nul, ws, wsb, nul) == 2
+    assert L.dit_gemm_bf16(ws, ws, 4, 12, 64, nul, 0, ws, 1, ws, wsb, nul) == 3
+    assert L.dit_gemm_bf16(ws, ws, 4, 16, 64, fake_misaligned, 0, ws, 1, ws, wsb, nul) == 2
     # an activation code outside dit_act
     assert L.dit_qgemm_int8(ws, ws, ws, ws, 2, 4, 8, 128, nul, 5, ws, 1, nul, ws, wsb, nul) == 1
     assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 128, nul, 2, ws, 1, ws, wsb, nul) == 1
@@ -173,3 +180,20 @@ def test_tdc_state_round_trip(L):
     for s_ in (st, cp):
         s_.update(dit.TDC_SKIP)
     assert cp.to_dict() == st.to_dict() and cp.routes([1.0], [0.0], [0.05]) == st.routes([1.0], [0.0], [0.05])
+
+
+def test_host_pdr_routes_match_oracle(L):
+    """The host routing with the PDR outlier-ratio override against the oracle's."""
+    import int8_mixed_precision_gb300 as dit
+    g = synth.rng(74)
+    for _ in range(200):
+        st = dit.TdcState()
+        gamma = None
+        if g.random() < 0.8:
+            gamma = float(g.random() * 0.2)
+            st.update(dit.TDC_COMMIT, gamma, None)
+        alpha, beta, thr = [1.0, 0.5], [0.0, 0.01], [0.05, 0.04]
+        ratio, rho = float(g.random() * 0.02), float(g.choice([0.005, 0.01, math.inf]))
+        f32 = lambda v: np.float32(v).astype(np.float64)      # the C interface takes float parameters
+        want = D.route_layers_pdr(gamma, f32(alpha), f32(beta), f32(thr), ratio, rho)
+        assert st.routes(alpha, beta, thr, ratio, rho) == want

@@ -745,3 +745,73 @@ def test_delta_cache_checkpoint_resume(ws):
     for (_, _, oa), (_, _, ob) in zip(rest_a, rest_b):
         assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
     _status_clean(ws)
+
+
+# ------------------------------------------------------------------------------ PDR: outlier ratio, BF16 route
+
+
+@pytest.mark.parametrize("n,dtype", [(17776 * 1920, "bf16"), (300 * 1920 + 7, "bf16"), (4096 + 3, "f32"), (5, "f32")])
+def test_outlier_ratio_parity(n, dtype, ws):
+    """Count of |x| > 6 RMS against the oracle: exact, except elements within 1e-6 relative of
+    the threshold (the GPU's RMS comes from a different summation order)."""
+    g = synth.rng(n % 9973)
+    x = g.standard_normal(n).astype(np.float32)
+    x[:: 97] *= 40.0                                       # outlier channels
+    xd = dev_f32(x) if dtype == "f32" else dev_bf16(F.f32_to_bf16_bits(x))
+    xv = x if dtype == "f32" else F.bf16_bits_to_f32(F.f32_to_bf16_bits(x))
+    ratio = torch.empty(1, dtype=torch.float32, device="cuda")
+    count = torch.empty(1, dtype=torch.int64, device="cuda")
+    dit.outlier_ratio(xd, ws, ratio, count)
+    _status_clean(ws)
+    x64 = xv.astype(np.float64)
+    thr = 6.0 * math.sqrt(float(np.sum(x64 * x64)) / n)
+    want = int(np.count_nonzero(np.abs(x64) > thr))
+    near = int(np.count_nonzero(np.abs(np.abs(x64) - thr) <= 1e-6 * thr))
+    assert abs(int(count.item()) - want) <= near
+    assert D.outlier_ratio(xv) == want / n
+    assert ratio.item() == pytest.approx(int(count.item()) / n, rel=1e-6)
+
+
+@pytest.mark.parametrize("m,n,k", [(256, 512, 128), (300, 384, 1920), (129, 256, 7680), (1, 8, 16), (700, 576, 2112)])
+@pytest.mark.parametrize("act", [0, 1])
+def test_gemm_bf16_parity(m, n, k, act, ws):
+    """The BF16 route against the float64 oracle: fp32 output within 1e-5 relative Frobenius
+    (fp32 accumulation of exact bf16 products), bf16 output against the oracle rounded to bf16."""
+    g = synth.rng(m + n + k + act)
+    xb = F.f32_to_bf16_bits(g.standard_normal((m, k)).astype(np.float32))
+    wb = F.f32_to_bf16_bits((g.standard_normal((n, k)) * 0.05).astype(np.float32))
+    bias = (g.standard_normal(n) * 0.1).astype(np.float32)
+    ref = D.gemm_bf16(F.bf16_bits_to_f32(xb), F.bf16_bits_to_f32(wb), bias)
+    if act:
+        ref = D.gelu_erf(ref)
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    dit.gemm_bf16(dev_bf16(xb), dev_bf16(wb), y, ws, bias=dev_f32(bias), act=act)
+    _status_clean(ws)
+    assert rel_fro(host(y), ref) <= 1e-5
+    yb = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    dit.gemm_bf16(dev_bf16(xb), dev_bf16(wb), yb, ws, bias=dev_f32(bias), act=act)
+    refb = F.bf16_bits_to_f32(F.f32_to_bf16_bits(ref.astype(np.float32)))
+    assert rel_fro(F.bf16_bits_to_f32(host(yb)), refb) <= GEMM_TOL
+
+
+def test_routed_linear_bf16_route_and_pdr_override(ws):
+    """A block input with a high outlier ratio sends every layer to BF16 (PDR); the BF16 route
+    of a linear computes X W^T on the untransformed weight."""
+    m, k, n = 300, 1920, 576
+    x, xd = make_x(m, k, "bf16", seed=91)
+    w = synth.weights(n, k, seed=92)
+    wq = dit.QuantizedWeight(dev_f32(w), 64, ws, keep_bf16=True)
+    lin = dit.RoutedLinear(wq, m, ws)
+    ratio = torch.empty(1, dtype=torch.float32, device="cuda")
+    dit.outlier_ratio(xd, ws, ratio)
+    r = ratio.item()
+    assert r > 0
+    st = dit.TdcState()
+    st.update(dit.TDC_COMMIT, 0.01, None)
+    assert st.routes([1.0] * 4, [0.0] * 4, [0.05] * 4, r, r / 2) == [dit.ROUTE_BF16] * 4
+    assert st.routes([1.0] * 4, [0.0] * 4, [0.05] * 4, r, 2 * r) == [dit.ROUTE_NVFP4] * 4
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    lin(xd, dit.ROUTE_BF16, y)
+    _status_clean(ws)
+    ref = D.gemm_bf16(F.bf16_bits_to_f32(x), F.bf16_bits_to_f32(F.f32_to_bf16_bits(w)))
+    assert rel_fro(host(y), ref) <= 1e-5
