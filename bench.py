@@ -538,6 +538,20 @@ def run_ours(args, rank, world, local_rank):
     kern_times = {k: round(v, 3) for k, v in tot.items()}
     hbm = {k: round(units[k] / (tot[k] * 1e-3) / 1e9, 1) for k in ("quant_int8", "quant_nvfp4", "tdc_commit")
            if tot.get(k)}
+    # every kernel type against its own bound (event-timed launches of one instrumented step)
+    kern_roof = {}
+    for k, t in tot.items():
+        if not t:
+            continue
+        if k.startswith("gemm"):
+            a = units[k] / (t * 1e-3) / 1e12
+            p = pk["bf16_tflops_sustained"] * (6.0 if k == "gemm_nvfp4" else 1.0)
+            kern_roof[k] = {"bound": "tensor", "achieved": round(a, 1), "peak": round(p, 1), "unit": "TFLOP/s",
+                            "frac": round(a / p, 4)}
+        else:
+            a = units[k] / (t * 1e-3) / 1e9
+            kern_roof[k] = {"bound": "hbm", "achieved": round(a, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(a / pk["hbm_gbs"], 4)}
     value = aggregate_value(wl.flops_step, world, ms)
     e2e_val = aggregate_value(wl.flops_step, world, e2e_ms)
     routes_flat = [r for rr in wl.routes for r in rr]
@@ -554,6 +568,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roof,
         "kernel_ms_per_step": kern_times,
         "hbm_gbs_algorithmic": hbm,
+        "kernel_roofline": kern_roof,
         "e2e": {"value": round(e2e_val, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 3), "steps": e_steps,
                 "copies": "pinned host -> device on a copy stream into ping-pong device buffers, one event "

@@ -66,6 +66,23 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base, uint64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale factors in the MMA tile layout ([row blocks of 128][K / 64 atoms][512 bytes]) as a
+// 3-D tensor of 32-bit words {128 words per atom, atoms along K, row blocks}; a box of
+// {128, 4, box_blocks} is one 256-deep K stage of box_blocks row blocks.  Atoms past K and
+// row blocks past the padded rows read as zeros.
+bool encode_tmap_sf(CUtensorMap* map, const void* sf, int64_t rows, int64_t k, uint32_t box_blocks) {
+  encode_tiled_fn fn = get_encode_tiled();
+  if (!fn) return false;
+  const uint64_t atoms = (uint64_t)(k / 64), blocks = (uint64_t)((rows + 127) / 128);
+  cuuint64_t dims[3] = {128, atoms, blocks};
+  cuuint64_t strides[2] = {512, 512 * atoms};
+  cuuint32_t box[3] = {128, 4, box_blocks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(sf), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace dit6
 
 extern "C" {

@@ -217,6 +217,35 @@ __device__ __forceinline__ float amax_range(const float2 (&v)[32], int p0, int n
   return m;
 }
 
+// NVFP4 encoding of one 16-element block of the transformed tensor (pairs v[0..7]) with tensor
+// scale s_g (six_sg = 6 s_g): the E4M3 scale RN(amax_b / (6 s_g)), saturating; the values times
+// RN(1 / (dec(scale) s_g)) rounded to E2M1.  Returns the scale code; `out` gets the 8 code bytes
+// (element 2i in the low nibble of byte i).
+__device__ __forceinline__ uint32_t nvfp4_encode_block16(const float2* v, float s_g, float six_sg, uint32_t (&out)[2]) {
+  float ab = 0.f;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) ab = fmaxf(ab, fmaxf(fabsf(v[p].x), fabsf(v[p].y)));
+  uint32_t code = 0;
+  float inv = 0.f;
+  if (s_g > 0.f) {
+    code = e4m3_code(__fdiv_rn(ab, six_sg));
+    const float bs = __fmul_rn(e4m3_value(code), s_g);
+    inv = bs == 0.f ? 0.f : __frcp_rn(bs);
+  }
+  const float2 iv = make_float2(inv, inv);
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {  // 8 elements -> one 32-bit word of 8 codes
+    uint32_t word = 0;
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+      const float2 s = mul2(v[w * 4 + pp], iv);
+      word |= e2m1x2(s.x, s.y) << (8 * pp);
+    }
+    out[w] = inv == 0.f ? 0u : word;
+  }
+  return code;
+}
+
 // NVFP4 encoding of one 64-element unit of the transformed tensor (four 16-element blocks)
 // with tensor scale s_g (six_sg = 6 s_g): per block the E4M3 scale RN(amax_b / (6 s_g)),
 // saturating; the block's values times RN(1 / (dec(scale) s_g)) rounded to E2M1.  Returns the
@@ -226,26 +255,10 @@ __device__ __forceinline__ uint32_t nvfp4_encode_unit(const float2 (&v)[32], flo
   uint32_t sfword = 0;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    const float ab = amax_range(v, g * 8, 8);
-    uint32_t code = 0;
-    float inv = 0.f;
-    if (s_g > 0.f) {
-      code = e4m3_code(__fdiv_rn(ab, six_sg));
-      const float bs = __fmul_rn(e4m3_value(code), s_g);
-      inv = bs == 0.f ? 0.f : __frcp_rn(bs);
-    }
-    sfword |= code << (8 * g);
-    const float2 iv = make_float2(inv, inv);
-#pragma unroll
-    for (int w = 0; w < 2; ++w) {  // 8 elements -> one 32-bit word of 8 codes
-      uint32_t word = 0;
-#pragma unroll
-      for (int pp = 0; pp < 4; ++pp) {
-        const float2 s = mul2(v[g * 8 + w * 4 + pp], iv);
-        word |= e2m1x2(s.x, s.y) << (8 * pp);
-      }
-      out.w[g * 2 + w] = inv == 0.f ? 0u : word;
-    }
+    uint32_t w[2];
+    sfword |= nvfp4_encode_block16(&v[g * 8], s_g, six_sg, w) << (8 * g);
+    out.w[g * 2] = w[0];
+    out.w[g * 2 + 1] = w[1];
   }
   return sfword;
 }
@@ -392,6 +405,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
       : "memory");
 }
+// 3-D tiled TMA load, completion on an mbarrier of either CTA of the pair
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], "
+      "[%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
                    bar),
@@ -418,6 +440,9 @@ int num_sms();  // SM count of the current device (cached per device)
 int test_stall();
 bool aligned32(const void* p);
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda needed)
+// the block-scale array of an NVFP4 operand of `rows` x `k` as a TMA source (one K stage of
+// box_blocks 128-row blocks per load)
+bool encode_tmap_sf(CUtensorMap* map, const void* sf, int64_t rows, int64_t k, uint32_t box_blocks);
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base, uint64_t inner,
                     uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                     CUtensorMapSwizzle swz);

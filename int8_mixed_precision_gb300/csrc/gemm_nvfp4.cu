@@ -100,6 +100,20 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// tcgen05.ld of 32 columns without the wait (the caller waits once for several loads)
+__device__ __forceinline__ void tc_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
 template <int BN, int STAGES, bool SPLIT_N>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -833,6 +847,24 @@ __device__ __forceinline__ void tc_st4(uint32_t taddr, const uint4& v) {
                "r"(v.z), "r"(v.w)
                : "memory");
 }
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
 
 // QHB > 0 (16, 32 or 64): fused epilogue quantisation.  The output Z (after bias and
 // activation, rounded to bf16 as it would be stored) is block-Hadamard transformed along N in
@@ -974,28 +1006,33 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC>::THREADS, CTAS)
     uint32_t kc = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-      const int n0 = (tile % n_tiles_n) * BN;
-      int nb_valid = (N - n0 + 127) / 128;
-      if (nb_valid > C::NB) nb_valid = C::NB;
       for (int kb = 0; kb < num_kb; ++kb, ++kc) {
         const int s = kc % S;
         if (!mbar_wait(full(s), (kc / S) & 1, ws, abort_flag)) {
           ok = false;
           break;
         }
-        const int nsub = min(4, ksteps - kb * 4);
         // lane l gets the 16-byte line l of each 512-byte atom: the four scale words of
-        // rows l, l+32, l+64, l+96 -- the same words the warpx4 copy puts in every quarter
-        for (int j = 0; j < nsub; ++j) {
-          const uint32_t sfa_col = C::SF_BASE + (s * 4 + j) * C::SF_COLS;
-          const uint4 va = *reinterpret_cast<const uint4*>(sfa_tile(s) + j * SF_ATOM + lane * 16);
-          tc_st4(lane_base + sfa_col, va);
-          for (int nb = 0; nb < nb_valid; ++nb) {
-            const uint4 vb =
-                *reinterpret_cast<const uint4*>(sfb_tile(s) + nb * 4 * SF_ATOM + j * SF_ATOM + lane * 16);
-            tc_st4(lane_base + sfa_col + 4 + 4 * nb, vb);
+        // rows l, l+32, l+64, l+96 -- the same words the warpx4 copy puts in every quarter.
+        // The stage's 4 x SF_COLS columns go out in one or two wide stores; columns of K steps
+        // past the end of K, or of B atoms past N, hold stale words whose products are never
+        // stored.
+        uint32_t r[4 * C::SF_COLS];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int a = 0; a <= C::NB; ++a) {
+            const uint8_t* src = a == 0 ? sfa_tile(s) + j * SF_ATOM : sfb_tile(s) + (a - 1) * 4 * SF_ATOM + j * SF_ATOM;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + lane * 16);
+            r[j * C::SF_COLS + 4 * a + 0] = v.x;
+            r[j * C::SF_COLS + 4 * a + 1] = v.y;
+            r[j * C::SF_COLS + 4 * a + 2] = v.z;
+            r[j * C::SF_COLS + 4 * a + 3] = v.w;
           }
         }
+        const uint32_t col = C::SF_BASE + s * 4 * C::SF_COLS;
+        tc_st32(lane_base + col, r);
+        if constexpr (C::SF_COLS == 12) tc_st16(lane_base + col + 32, r + 32);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
@@ -1223,6 +1260,599 @@ static dit_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const uin
 }
 
 
+// Epilogue of 32 accumulator columns of one output row: Y = acc * (s_gA s_gB) (+ bias), then
+// GELU when asked, stored as bf16 or fp32 (256-bit stores when the chunk is whole and aligned).
+__device__ __forceinline__ void epi_store32(const uint32_t (&r)[32], float alpha, int row, int col0, int M, int N,
+                                            const float* __restrict__ bias, void* __restrict__ y, int epi) {
+  if (row >= M || col0 >= N) return;
+  float v[32];
+  const float2 al = make_float2(alpha, alpha);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 p = mul2(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), al);
+    v[2 * i] = p.x;
+    v[2 * i + 1] = p.y;
+  }
+  if (bias) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
+  }
+  if (epi & EPI_GELU) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 g = gelu_erf2(make_float2(v[2 * i], v[2 * i + 1]));
+      v[2 * i] = g.x;
+      v[2 * i + 1] = g.y;
+    }
+  }
+  const int64_t off = (int64_t)row * N + col0;
+  if (col0 + 32 <= N && (N % 16) == 0) {
+    if (epi & EPI_BF16) {
+      U8x32 o0, o1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        o0.w[i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
+        o1.w[i] = f2_to_bf16x2(v[16 + 2 * i], v[16 + 2 * i + 1]);
+      }
+      uint16_t* yp = reinterpret_cast<uint16_t*>(y) + off;
+      st256(yp, o0);
+      st256(yp + 16, o1);
+    } else {
+      float* yp = reinterpret_cast<float*>(y) + off;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        U8x32 o;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o.w[i] = __float_as_uint(v[8 * b + i]);
+        st256(yp + 8 * b, o);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (col0 + i >= N) continue;
+      if (epi & EPI_BF16)
+        reinterpret_cast<__nv_bfloat16*>(y)[off + i] = __float2bfloat16_rn(v[i]);
+      else
+        reinterpret_cast<float*>(y)[off + i] = v[i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// CTA-pair variant: tcgen05.mma.cta_group::2 ... block_scale on 256 x 256 output tiles over
+// the two SMs of a 2-CTA cluster.
+//
+// Each CTA stages its own 128 rows of A and its own 128-row half of the tile's B, so an SM
+// moves 32 KB of operands per 256-deep K stage for the MMA work that a single-CTA 128 x 256
+// tile needs 48 KB for: shared memory, which carries both the TMA writes and the MMA's operand
+// reads, stops being the bound.  The even CTA (leader) issues the pair's MMAs; each CTA's
+// tensor core reads A and its scales from its own memories and B from both CTAs' shared
+// memory.  Scale factors reach tensor memory through WG groups of four scale-writer warps per
+// CTA (tcgen05.st, off the tensor unit; the groups take alternate stages): each CTA writes the
+// scales of its own A rows and those of all 256 B rows of the tile (the pair MMA reads the B
+// scales of the whole N extent from each CTA's tensor memory).
+// Barriers: the leader's full[s] counts both CTAs' A/B copies; each CTA's sf_full[s] its own
+// scale copies; the leader's sf_ready[s] takes the eight scale-writer warps of the pair; MMA
+// completion is multicast to both CTAs' empty[s] and acc_full; both epilogues release the
+// accumulator on the leader's acc_empty.  One 256-column accumulator per CTA (the scale slots
+// of the five stages use the other 240 columns).
+// ---------------------------------------------------------------------------------------
+template <int WG>
+struct Pair4Cfg {
+  static constexpr int STAGES = 5;
+  static constexpr int B_BYTES = 128 * BK / 2;                  // this CTA's half of B
+  static constexpr int SFA_BYTES = 4 * SF_ATOM;                 // own 128 rows, 4 K steps
+  static constexpr int SFB_ATOMS = 2;                           // the scales of all 256 B rows
+  static constexpr int SFB_BYTES = SFB_ATOMS * 4 * SF_ATOM;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int SF_COLS = 4 + 4 * SFB_ATOMS;             // tensor-memory columns per K step
+  static constexpr int SF_BASE = 256;
+  static constexpr int TMEM_USED = SF_BASE + STAGES * 4 * SF_COLS;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int SF_WARP0 = 2 + EPI_WARPS;
+  static constexpr int THREADS = (2 + EPI_WARPS + 4 * WG) * 32;
+  static_assert(TMEM_USED <= TMEM_COLS, "tensor memory");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ void tc_mma_pair_f4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                               uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
+      "[%5], p; }" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+
+template <int WG>
+__global__ void __launch_bounds__(Pair4Cfg<WG>::THREADS, 1)
+    k_gemm_nvfp4_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
+                      const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N, int K,
+                      const float* __restrict__ bias, void* __restrict__ y, int epi, void* ws, int stall) {
+  using C = Pair4Cfg<WG>;
+  constexpr int S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
+  // bars: full[S], empty[S], sf_full[S], sf_ready[S], acc_full, acc_empty, mma_done (same offsets in both CTAs)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * S + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t sbase = smem_u32(smem);
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + S + s); };
+  auto sf_full = [&](int s) { return smem_u32(bars + 2 * S + s); };
+  auto sf_ready = [&](int s) { return smem_u32(bars + 3 * S + s); };
+  const uint32_t acc_full = smem_u32(bars + 4 * S);
+  const uint32_t acc_empty = smem_u32(bars + 4 * S + 1);
+  const uint32_t mma_done = smem_u32(bars + 4 * S + 2);
+  auto a_tile = [&](int s) { return sbase + s * C::STAGE_BYTES; };
+  auto b_tile = [&](int s) { return a_tile(s) + A_BYTES; };
+  auto sfa_tile = [&](int s) { return smem + s * C::STAGE_BYTES + A_BYTES + C::B_BYTES; };
+  auto sfb_tile = [&](int s) { return sfa_tile(s) + C::SFA_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
+  const int ksteps = K / KSTEP;
+  const int num_kb = (ksteps + 3) / 4;
+  const int k_atoms = ksteps;             // scale atoms per 128-row block along K
+  const int a_blocks = (M + 127) / 128;   // 128-row blocks present in the scale arrays
+  const int b_blocks = (N + 127) / 128;
+  const int n_tiles_n = (N + 255) / 256;
+  const int n_items = ((M + 255) / 256) * n_tiles_n;
+  const int first_item = blockIdx.x >> 1, item_step = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+      mbar_init(sf_full(s), 1);
+      mbar_init(sf_ready(s), 8);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 2 * C::EPI_WARPS);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA signal
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {  // ------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0 && !stall) {  // stall: a test hook that issues no loads at all
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      uint32_t kc = 0;
+      bool ok = true;
+      for (int item = first_item; item < n_items && ok; item += item_step) {
+        const int mt = item / n_tiles_n, nt = item % n_tiles_n;
+        const int m0 = mt * 256 + (int)rank * 128, n0 = nt * 256 + (int)rank * 128;
+        const int ablk = mt * 2 + (int)rank;  // this CTA's row block of the A scales
+        const bool a_sf_ok = ablk < a_blocks; // rows past the padded scale array: nothing to stage
+        const int nb_first = nt * 2;
+        int nb_cnt = b_blocks - nb_first;
+        nb_cnt = nb_cnt < 0 ? 0 : (nb_cnt > C::SFB_ATOMS ? C::SFB_ATOMS : nb_cnt);
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait_cl(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_expect_tx(full(s), 2 * (A_BYTES + C::B_BYTES));  // both CTAs' bytes
+          const uint32_t fb = mapa_rank(full(s), 0);
+          tma_load_2d_pair(a_tile(s), &tmA, fb, kb * (BK / 2), m0);
+          tma_load_2d_pair(b_tile(s), &tmB, fb, kb * (BK / 2), n0);
+          const int nsub = min(4, ksteps - kb * 4);
+          mbar_expect_tx(sf_full(s), nsub * SF_ATOM * ((a_sf_ok ? 1 : 0) + nb_cnt));
+          if (a_sf_ok)
+            bulk_load(smem_u32(sfa_tile(s)), a_sf + ((size_t)ablk * k_atoms + kb * 4) * SF_ATOM, nsub * SF_ATOM,
+                      sf_full(s));
+          for (int nb = 0; nb < nb_cnt; ++nb)
+            bulk_load(smem_u32(sfb_tile(s)) + nb * 4 * SF_ATOM,
+                      b_sf + ((size_t)(nb_first + nb) * k_atoms + kb * 4) * SF_ATOM, nsub * SF_ATOM, sf_full(s));
+        }
+      }
+      if (!ok) {  // let this CTA's copies in flight land before it leaves
+        volatile int no_abort = 0;
+        const uint32_t first = kc > (uint32_t)S ? kc - S : 0;
+        for (uint32_t c = first; c < kc; ++c) {
+          mbar_wait(sf_full(c % S), (c / S) & 1, ws, &no_abort);
+          if (rank == 0) mbar_wait_cl(full(c % S), (c / S) & 1, ws, &no_abort);  // counts both CTAs' A/B
+        }
+      }
+    }
+  } else if (warp == 1) {  // ----------------------------------------- MMA issuer (leader only)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_nvf4(256, 256);
+      uint32_t kc = 0, tc = 0;
+      bool ok = true;
+      for (int item = first_item; item < n_items && ok; item += item_step, ++tc) {
+        if (!mbar_wait_cl(acc_empty, (tc & 1) ^ 1, ws, abort_flag)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait_cl(full(s), (kc / S) & 1, ws, abort_flag) ||
+              !mbar_wait_cl(sf_ready(s), (kc / S) & 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nsub = min(4, ksteps - kb * 4);
+          for (int j = 0; j < nsub; ++j) {
+            const uint32_t col = C::SF_BASE + (s * 4 + j) * C::SF_COLS;
+            tc_mma_pair_f4(tmem, desc_sw128(a_tile(s) + j * 32), desc_sw128(b_tile(s) + j * 32), idesc, tmem + col,
+                           tmem + col + 4, (kb | j) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(empty(s), 3);
+        }
+        if (ok) tc_commit_pair_mc(acc_full, 3);
+      }
+      tc_commit_pair(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait_cl(mma_done, 0, ws, &no_abort);  // every issued MMA has completed
+    }
+    __syncwarp();
+  } else if (warp >= C::SF_WARP0) {  // -------------------------- scale writers (both CTAs)
+    const int q = warp & 3;                        // the lane quarter this warp may write
+    const int grp = (warp - C::SF_WARP0) >> 2;     // writer group: stages kc with kc % WG == grp
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    uint32_t kc = 0;
+    bool ok = true;
+    for (int item = first_item; item < n_items && ok; item += item_step) {
+      for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+        if ((int)(kc % WG) != grp) continue;
+        const int s = kc % S;
+        if (!mbar_wait(sf_full(s), (kc / S) & 1, ws, abort_flag)) {
+          ok = false;
+          break;
+        }
+        // lane l gets the 16-byte line l of each 512-byte atom: the four scale words of rows
+        // l, l+32, l+64, l+96 -- the words the 32x128b.warpx4 copy puts in every lane quarter.
+        // A stage's 48 columns (per K step: A rows, B rows 0-127, B rows 128-255) go out in two
+        // stores; columns of K steps past the end of K hold stale words no MMA reads.
+        uint32_t r[48];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 a = *reinterpret_cast<const uint4*>(sfa_tile(s) + j * SF_ATOM + lane * 16);
+          const uint4 b0 = *reinterpret_cast<const uint4*>(sfb_tile(s) + j * SF_ATOM + lane * 16);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(sfb_tile(s) + 4 * SF_ATOM + j * SF_ATOM + lane * 16);
+          r[12 * j + 0] = a.x, r[12 * j + 1] = a.y, r[12 * j + 2] = a.z, r[12 * j + 3] = a.w;
+          r[12 * j + 4] = b0.x, r[12 * j + 5] = b0.y, r[12 * j + 6] = b0.z, r[12 * j + 7] = b0.w;
+          r[12 * j + 8] = b1.x, r[12 * j + 9] = b1.y, r[12 * j + 10] = b1.z, r[12 * j + 11] = b1.w;
+        }
+        const uint32_t col = C::SF_BASE + s * 4 * C::SF_COLS;
+        tc_st32(lane_base + col, r);
+        tc_st16(lane_base + col + 32, r + 32);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_rank(sf_ready(s), 0));
+      }
+    }
+  } else {  // ------------------------------------------------------ epilogue warps (both CTAs)
+    const int e = warp - 2;
+    const int q = warp & 3;   // tensor-memory lane quarter of this warp
+    const int half = e >> 2;  // which 128-column half of the 256-column tile
+    const float alpha = __fmul_rn(*a_gs, *b_gs);
+    const uint32_t acc_empty_leader = mapa_rank(acc_empty, 0);
+    uint32_t tc = 0;
+    for (int item = first_item; item < n_items; item += item_step, ++tc) {
+      const int m0 = (item / n_tiles_n) * 256 + (int)rank * 128, n0 = (item % n_tiles_n) * 256;
+      if (!mbar_wait_cl(acc_full, tc & 1, ws, abort_flag)) break;
+      tc_fence_after();
+      const int row = m0 + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + half * 128 + c * 32, r);
+        epi_store32(r, alpha, row, n0 + half * 128 + c * 32, M, N, bias, y, epi);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  cluster_sync();  // no MMA, copy or arrival of either CTA still touches the other
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+template <int WG>
+static dit_status launch_pair4(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf,
+                               const uint8_t* b_sf, const float* a_gs, const float* b_gs, int M, int N, int K,
+                               const float* bias, void* y, int epi, void* ws, cudaStream_t st) {
+  using C = Pair4Cfg<WG>;
+  auto kern = k_gemm_nvfp4_pair<WG>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+      return DIT_ERR_CUDA;
+    attr_done = true;
+  }
+  const int64_t items = (int64_t)((M + 255) / 256) * ((N + 255) / 256);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.gridDim = dim3((unsigned)(num_sms() / 2 * 2));
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return DIT_ERR_CUDA;
+  int64_t pairs = clusters;
+  if (pairs > items) pairs = items;
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y, epi, ws, test_stall()) !=
+      cudaSuccess)
+    return DIT_ERR_CUDA;
+  return DIT_OK;
+}
+
+
+// ---------------------------------------------------------------------------------------
+// CTA-pair variant with scale copies on the tensor pipe: the same 256 x 256 tiles, but each
+// CTA's scale atoms arrive by TMA with its operand tiles (one leader barrier per stage for the
+// pair's A, B and scale bytes), and the leader's MMA thread moves them into both CTAs' tensor
+// memory itself with tcgen05.cp.cta_group::2 (every CTA copies its own shared memory into its
+// own tensor memory) right before the MMAs that read them; copies and MMAs issued by one
+// thread run in order, so no scale barrier and no writer warps are needed.
+// ---------------------------------------------------------------------------------------
+struct PairCpCfg {
+  static constexpr int STAGES = 5;
+  static constexpr int B_BYTES = 128 * BK / 2;                  // this CTA's half of B
+  static constexpr int SFA_BYTES = 4 * SF_ATOM;                 // own 128 rows, 4 K steps
+  static constexpr int SFB_BYTES = 2 * 4 * SF_ATOM;             // all 256 B rows, 4 K steps
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int SF_COLS = 12;                            // tensor-memory columns per K step
+  static constexpr int SF_BASE = 256;
+  static constexpr int TMEM_USED = SF_BASE + STAGES * 4 * SF_COLS;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int THREADS = (2 + EPI_WARPS) * 32;
+  static_assert(TMEM_USED <= TMEM_COLS, "tensor memory");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// EARLY: each epilogue thread first drains its 128 accumulator columns into registers and
+// releases the accumulator, so the MMAs of the next tile overlap this tile's conversion and
+// stores (one 256-column accumulator, no second buffer in tensor memory).
+template <bool EARLY>
+__global__ void __launch_bounds__(PairCpCfg::THREADS, 1)
+    k_gemm_nvfp4_pair_cp(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                         const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N, int K,
+                         const float* __restrict__ bias, void* __restrict__ y, int epi, void* ws, int stall) {
+  using C = PairCpCfg;
+  constexpr int S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
+  // bars: full[S], empty[S], acc_full, acc_empty, mma_done (same offsets in both CTAs)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t sbase = smem_u32(smem);
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + S + s); };
+  const uint32_t acc_full = smem_u32(bars + 2 * S);
+  const uint32_t acc_empty = smem_u32(bars + 2 * S + 1);
+  const uint32_t mma_done = smem_u32(bars + 2 * S + 2);
+  auto a_tile = [&](int s) { return sbase + s * C::STAGE_BYTES; };
+  auto b_tile = [&](int s) { return a_tile(s) + A_BYTES; };
+  auto sfa_tile = [&](int s) { return b_tile(s) + C::B_BYTES; };
+  auto sfb_tile = [&](int s) { return sfa_tile(s) + C::SFA_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's copies and MMAs
+  const int ksteps = K / KSTEP;
+  const int num_kb = (ksteps + 3) / 4;
+  const int n_tiles_n = (N + 255) / 256;
+  const int n_items = ((M + 255) / 256) * n_tiles_n;
+  const int first_item = blockIdx.x >> 1, item_step = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 2 * C::EPI_WARPS);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA signal
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {  // ------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0 && !stall) {  // stall: a test hook that issues no loads at all
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      prefetch_tmap(&tmSA);
+      prefetch_tmap(&tmSB);
+      uint32_t kc = 0;
+      bool ok = true;
+      for (int item = first_item; item < n_items && ok; item += item_step) {
+        const int mt = item / n_tiles_n, nt = item % n_tiles_n;
+        const int m0 = mt * 256 + (int)rank * 128, n0 = nt * 256 + (int)rank * 128;
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait_cl(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_expect_tx(full(s), 2 * C::STAGE_BYTES);  // both CTAs' bytes
+          const uint32_t fb = mapa_rank(full(s), 0);
+          tma_load_2d_pair(a_tile(s), &tmA, fb, kb * (BK / 2), m0);
+          tma_load_2d_pair(b_tile(s), &tmB, fb, kb * (BK / 2), n0);
+          tma_load_3d_pair(sfa_tile(s), &tmSA, fb, 0, kb * 4, mt * 2 + (int)rank);
+          tma_load_3d_pair(sfb_tile(s), &tmSB, fb, 0, kb * 4, nt * 2);
+        }
+      }
+      if (!ok && rank == 0) {  // the leader's full barriers count both CTAs' copies in flight
+        volatile int no_abort = 0;
+        const uint32_t first = kc > (uint32_t)S ? kc - S : 0;
+        for (uint32_t c = first; c < kc; ++c) mbar_wait_cl(full(c % S), (c / S) & 1, ws, &no_abort);
+      }
+    }
+  } else if (warp == 1) {  // ----------------------------------------- MMA issuer (leader only)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_nvf4(256, 256);
+      uint32_t kc = 0, tc = 0;
+      bool ok = true;
+      for (int item = first_item; item < n_items && ok; item += item_step, ++tc) {
+        if (!mbar_wait_cl(acc_empty, (tc & 1) ^ 1, ws, abort_flag)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
+          const int s = kc % S;
+          if (!mbar_wait_cl(full(s), (kc / S) & 1, ws, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nsub = min(4, ksteps - kb * 4);
+          for (int j = 0; j < nsub; ++j) {
+            const uint32_t col = C::SF_BASE + (s * 4 + j) * C::SF_COLS;
+            tc_cp_sf_pair(tmem + col, desc_sf(sfa_tile(s) + j * SF_ATOM));
+            tc_cp_sf_pair(tmem + col + 4, desc_sf(sfb_tile(s) + j * SF_ATOM));
+            tc_cp_sf_pair(tmem + col + 8, desc_sf(sfb_tile(s) + 4 * SF_ATOM + j * SF_ATOM));
+            tc_mma_pair_f4(tmem, desc_sw128(a_tile(s) + j * 32), desc_sw128(b_tile(s) + j * 32), idesc, tmem + col,
+                           tmem + col + 4, (kb | j) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(empty(s), 3);
+        }
+        if (ok) tc_commit_pair_mc(acc_full, 3);
+      }
+      tc_commit_pair(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait_cl(mma_done, 0, ws, &no_abort);  // every issued copy and MMA has completed
+    }
+    __syncwarp();
+  } else {  // ------------------------------------------------------ epilogue warps (both CTAs)
+    const int e = warp - 2;
+    const int q = warp & 3;   // tensor-memory lane quarter of this warp
+    const int half = e >> 2;  // which 128-column half of the 256-column tile
+    const float alpha = __fmul_rn(*a_gs, *b_gs);
+    const uint32_t acc_empty_leader = mapa_rank(acc_empty, 0);
+    uint32_t tc = 0;
+    for (int item = first_item; item < n_items; item += item_step, ++tc) {
+      const int m0 = (item / n_tiles_n) * 256 + (int)rank * 128, n0 = (item % n_tiles_n) * 256;
+      if (!mbar_wait_cl(acc_full, tc & 1, ws, abort_flag)) break;
+      tc_fence_after();
+      const int row = m0 + q * 32 + lane;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + half * 128;
+      if constexpr (EARLY) {
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc_ld32_nowait(tbase + c * 32, r[c]);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) epi_store32(r[c], alpha, row, n0 + half * 128 + c * 32, M, N, bias, y, epi);
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tc_ld32(tbase + c * 32, r);
+          epi_store32(r, alpha, row, n0 + half * 128 + c * 32, M, N, bias, y, epi);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  cluster_sync();  // no MMA, copy or arrival of either CTA still touches the other
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+template <bool EARLY>
+static dit_status launch_pair_cp(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf,
+                                 const uint8_t* b_sf, const float* a_gs, const float* b_gs, int M, int N, int K,
+                                 const float* bias, void* y, int epi, void* ws, cudaStream_t st) {
+  using C = PairCpCfg;
+  CUtensorMap tsa, tsb;
+  if (!encode_tmap_sf(&tsa, a_sf, M, K, 1) || !encode_tmap_sf(&tsb, b_sf, N, K, 2)) return DIT_ERR_CUDA;
+  auto kern = k_gemm_nvfp4_pair_cp<EARLY>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+      return DIT_ERR_CUDA;
+    attr_done = true;
+  }
+  const int64_t items = (int64_t)((M + 255) / 256) * ((N + 255) / 256);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.gridDim = dim3((unsigned)(num_sms() / 2 * 2));
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return DIT_ERR_CUDA;
+  int64_t pairs = clusters;
+  if (pairs > items) pairs = items;
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, a_gs, b_gs, M, N, K, bias, y, epi, ws, test_stall()) !=
+      cudaSuccess)
+    return DIT_ERR_CUDA;
+  return DIT_OK;
+}
+
+
 }  // namespace f4
 }  // namespace dit6
 
@@ -1318,5 +1948,9 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
     case 13: return f4::launch_s<128, 6, 1, 0, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 14: return f4::launch_s<128, 4, 1, 0, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 0: return f4::launch<128, 3, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 15: return f4::launch_pair4<2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 16: return f4::launch_pair4<1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 18: return f4::launch_pair_cp<true>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 17: return f4::launch_pair_cp<false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
   }
 }

@@ -48,6 +48,8 @@ def _status_clean(ws):
     (129, 7680, "bf16", 64),      # FFN-down width
     (7, 3072, "bf16", 32),
     (1, 12288, "bf16", 64),
+    (5003, 1920, "bf16", 64),     # thousands of row groups, ragged tail
+    (1203, 12288, "bf16", 16),
 ])
 @pytest.mark.parametrize("container", [torch.int8, torch.bfloat16])
 def test_int8_quant_parity(rows, k, dtype, hb, container):
@@ -83,6 +85,8 @@ def test_int8_quant_zero_and_constant_rows(dtype):
     (129, 7680, "bf16", 64),
     (7, 3072, "bf16", 32),
     (1000, 3072, "bf16", 64),
+    (4100, 1920, "bf16", 64),     # several grid-stride passes per thread, ragged 128-row tail
+    (2051, 640, "f32", 32),
 ])
 def test_nvfp4_quant_parity(rows, k, dtype, hb, ws):
     x, xd = make_x(rows, k, dtype, seed=3 * rows + k, dist="laplace" if k == 3072 else "normal")
@@ -389,7 +393,7 @@ def _nvfp4_operands(m, n, k, seed):
     return qa, qb, out[0], out[1]
 
 
-@pytest.mark.parametrize("cfg", ["0", "1", "2", "3", "4", "5", "6", "7", "8", "9", "10", "11", "12", "13", "14"])
+@pytest.mark.parametrize("cfg", ["0", "1", "2", "3", "4", "5", "6", "7", "8", "9", "10", "11", "12", "13", "14", "15", "16", "17", "18"])
 @pytest.mark.parametrize("m,n,k", [(256, 512, 128), (300, 384, 1920), (129, 256, 7680), (128, 128, 64),
                                    (77, 136, 320)])
 def test_nvfp4_gemm_parity(m, n, k, cfg, ws, monkeypatch):
