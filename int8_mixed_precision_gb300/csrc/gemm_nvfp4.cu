@@ -1858,12 +1858,13 @@ static dit_status launch_pair_cp(const CUtensorMap& ta, const CUtensorMap& tb, c
 
 using namespace dit6;
 
-// Tile configuration, selectable for experiments through DIT6_NVFP4_TILE (0 = default).
 // Tile configuration.  The default (10) is the persistent 128 x 128 kernel with two CTAs per
-// SM whose scale atoms are written into tensor memory by four dedicated warps (tcgen05.st):
-// scale copies on the tensor-core unit (tcgen05.cp) serialise with the MMAs, and two
-// independent MMA streams per SM hide the pipeline latency best (measured on GB300 across the
-// CogVideoX shapes).  DIT6_NVFP4_TILE selects another one for experiments and tests.
+// SM whose scale atoms are written into tensor memory by four dedicated warps (tcgen05.st, one
+// wide store per stage): scale copies on the tensor-core unit (tcgen05.cp) cost ~110 cycles of
+// tensor time each, and two independent MMA streams per SM hide the pipeline latency (and each
+// other's epilogue) best.  The CTA-pair kernels (15: scale writers, 18: tcgen05.cp with early
+// accumulator release) are exact but slower on every CogVideoX shape and at 8192^3 (measured on
+// GB300).  DIT6_NVFP4_TILE selects another configuration for experiments and tests.
 static int nvfp4_tile_cfg() {
   const char* e = getenv("DIT6_NVFP4_TILE");
   return e ? atoi(e) : 10;
@@ -1949,8 +1950,6 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
     case 14: return f4::launch_s<128, 4, 1, 0, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 0: return f4::launch<128, 3, false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 15: return f4::launch_pair4<2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
-    case 16: return f4::launch_pair4<1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 18: return f4::launch_pair_cp<true>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
-    case 17: return f4::launch_pair_cp<false>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
   }
 }
