@@ -75,27 +75,35 @@ def peaks():
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi sampling (every 100 ms) around the timed region: the sampler starts half a
+    second early, mark() brackets the timed region, and the summary keeps the samples whose
+    timestamps fall inside it (all samples if none does)."""
 
     def __init__(self, index: int):
         self.proc = None
         self.index = index
+        self.window = None
 
     def __enter__(self):
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)
         except OSError:
             self.proc = None
         return self
 
+    def mark(self, start: float, end: float):
+        self.window = (start, end)
+
     def __exit__(self, *a):
         self.lines = []
         if self.proc:
+            time.sleep(0.15)   # one more sample period after the timed region
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -104,21 +112,34 @@ class Clocks:
                 out, _ = self.proc.communicate()
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
+    @staticmethod
+    def parse(lines, window=None):
+        """Samples (time, sm MHz, max MHz, set of active throttle reasons) from nvidia-smi csv
+        lines, restricted to the wall-clock window when one is given and holds any; the flag
+        says whether the restriction applied."""
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
+        rows = []
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]),
+                             {n for n, v in zip(names, f[6:10]) if v.lower() == "active"}))
             except (ValueError, IndexError):
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if window:
+            inside = [r for r in rows if window[0] - 0.05 <= r[0] <= window[1] + 0.05]
+            if inside:
+                return inside, True
+        return rows, False
+
+    def summary(self):
+        rows, inside = self.parse(getattr(self, "lines", []), self.window)
+        reasons = set().union(*[r[3] for r in rows]) if rows else set()
+        return {"sm_mhz": statistics.median([r[1] for r in rows]) if rows else None,
+                "sm_max_mhz": rows[-1][2] if rows else None, "reasons": sorted(reasons),
+                "samples": len(rows), "in_timed_region": inside}
 
 
 # ----------------------------------------------------------------------------------------
@@ -438,12 +459,14 @@ def run_ours(args, rank, world, local_rank):
     with Clocks(local_rank) as clk:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.nvtx.range_push("timed")
+        w0 = time.time()
         e0.record(stream)
         for _ in range(args.steps):
             wl.step()
         e1.record(stream)
         torch.cuda.nvtx.range_pop()
         e1.synchronize()
+        clk.mark(w0, time.time())
     barrier()
     ms = e0.elapsed_time(e1) / args.steps
     dom_ms = [a.elapsed_time(z) for a, z in wl.timers[dominant]]
