@@ -74,10 +74,15 @@ def test_host_argument_validation_without_device_work(L):
     assert L.dit_hadamard_quant_int8(fake_misaligned, 1, 4, 128, 48, fake_misaligned, 2, fake_misaligned, nul) == 3
     assert L.dit_hadamard_quant_int8(fake_misaligned, 1, 4, 128, 64, fake_misaligned, 2, fake_misaligned, nul) == 2
     assert L.dit_hadamard_quant_int8(ws, 1, 4, 128, 64, ws, 0, ws, nul) == 1       # fp32 is no code container
+    assert L.dit_hadamard_quant_int8(ws, 1, 4, 16448, 64, ws, 2, ws, nul) == 3     # a row wider than 16384
     assert L.dit_hadamard_quant_nvfp4(ws, 1, 4, 128, 64, nul, nul, nul, nul, ws, wsb, nul) == 1
     f = ctypes.c_float * 17
     assert L.dit_gamma_route(fake_misaligned, fake_misaligned, 1, 10, f(), f(), f(), 17, ws, ws, ws, wsb, nul) == 1
     assert L.dit_gamma_route(fake_misaligned, fake_misaligned, 1, 10, f(), f(), f(), 1, ws, ws, ws, wsb, nul) == 2
+    # the workspace-free Gamma/route: null input, too many layers, misaligned input
+    assert L.dit_gamma_route_noalloc(nul, ws, 1, 10, f(), f(), f(), 1, ws, ws, nul) == 1
+    assert L.dit_gamma_route_noalloc(ws, ws, 1, 10, f(), f(), f(), 17, ws, ws, nul) == 1
+    assert L.dit_gamma_route_noalloc(fake_misaligned, fake_misaligned, 1, 10, f(), f(), f(), 1, ws, ws, nul) == 2
     assert L.dit_qgemm_int8(fake_misaligned, ws, fake_misaligned, ws, 2, 4, 8, 100, nul, 0, ws, 1, nul, ws, wsb, nul) == 3
     assert L.dit_qgemm_int8(ws, ws, ws, ws, 0, 4, 8, 128, nul, 0, ws, 1, nul, ws, wsb, nul) == 1
     assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 96, nul, 0, ws, 1, ws, wsb, nul) == 3

@@ -50,6 +50,7 @@ def _status_clean(ws):
     (1, 12288, "bf16", 64),
     (5003, 1920, "bf16", 64),     # thousands of row groups, ragged tail
     (1203, 12288, "bf16", 16),
+    (3, 16384, "bf16", 64),       # the widest row the quantiser takes (256 units, one CTA)
 ])
 @pytest.mark.parametrize("container", [torch.int8, torch.bfloat16])
 def test_int8_quant_parity(rows, k, dtype, hb, container):
