@@ -568,7 +568,10 @@ def run_ours(args, rank, world, local_rank):
             continue
         if k.startswith("gemm"):
             a = units[k] / (t * 1e-3) / 1e12
-            p = pk["bf16_tflops_sustained"] * (6.0 if k == "gemm_nvfp4" else 1.0)
+            if k == "gemm_int8" and wl.int8_code_bytes == 1:   # int8-held codes run on IMMA
+                p = peak if dominant == "gemm_int8" else int8_ceiling(torch, dev)
+            else:
+                p = pk["bf16_tflops_sustained"] * (6.0 if k == "gemm_nvfp4" else 1.0)
             kern_roof[k] = {"bound": "tensor", "achieved": round(a, 1), "peak": round(p, 1), "unit": "TFLOP/s",
                             "frac": round(a / p, 4)}
         else:
