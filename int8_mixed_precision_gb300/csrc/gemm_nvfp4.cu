@@ -1858,16 +1858,22 @@ static dit_status launch_pair_cp(const CUtensorMap& ta, const CUtensorMap& tb, c
 
 using namespace dit6;
 
-// Tile configuration.  The default (10) is the persistent 128 x 128 kernel with two CTAs per
+// Tile configuration.  The base default (10) is the persistent 128 x 128 kernel with two CTAs per
 // SM whose scale atoms are written into tensor memory by four dedicated warps (tcgen05.st, one
 // wide store per stage): scale copies on the tensor-core unit (tcgen05.cp) cost ~110 cycles of
 // tensor time each, and two independent MMA streams per SM hide the pipeline latency (and each
 // other's epilogue) best.  The CTA-pair kernels (15: scale writers, 18: tcgen05.cp with early
 // accumulator release) are exact but slower on every CogVideoX shape and at 8192^3 (measured on
 // GB300).  DIT6_NVFP4_TILE selects another configuration for experiments and tests.
-static int nvfp4_tile_cfg() {
+// Without DIT6_NVFP4_TILE the shape picks: one CTA per SM on 128 x 256 tiles (11) when K >= 3072
+// and N is a multiple of 256 -- four deeper stages then beat two CTAs per SM (CogVideoX-5B /
+// 1080p shapes: QKV 4.08 vs 3.99, FFN-down 5.39 vs 4.92, 104746 x 3072 x 12288 5.53 vs 4.90,
+// 8192^3 4.87 vs 4.66 PFLOP/s) -- else 10 (CogVideoX-2B: QKV 3.13 vs 3.08, FFN-down with
+// N = 1920 4.39 vs 4.24).
+static int nvfp4_tile_cfg(int64_t n, int64_t k) {
   const char* e = getenv("DIT6_NVFP4_TILE");
-  return e ? atoi(e) : 10;
+  if (e) return atoi(e);
+  return (k >= 3072 && n % 256 == 0) ? 11 : 10;
 }
 
 extern "C" dit_status dit_qgemm_nvfp4_fused_quant(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
@@ -1920,7 +1926,7 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
   if (!aligned32(a) || !aligned32(b) || !aligned32(a_sf) || !aligned32(b_sf) || !aligned32(y) ||
       !aligned32(ws))
     return DIT_ERR_ALIGNMENT;
-  const int cfg = nvfp4_tile_cfg();
+  const int cfg = nvfp4_tile_cfg(n, k);
   const uint32_t bn_box = (cfg == 1 || cfg == 2 || cfg == 5 || cfg == 6 || cfg == 8 || cfg == 11) ? 256 : 128;
   CUtensorMap ta, tb;
   if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(k / 2),
