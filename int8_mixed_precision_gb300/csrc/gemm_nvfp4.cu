@@ -1058,6 +1058,60 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC>::THREADS, CTAS)
       tc_fence_after();
       const int row = m0 + q * 32 + lane;
       const uint32_t tacc = tmem + buf * BN;
+      if constexpr (QHB == 0 && CTAS == 1) {
+        if (epi & EPI_BF16) {
+          // one CTA per SM: convert the thread's 128 columns to packed bf16 in registers, release
+          // the accumulator, then store -- the next tile's MMAs overlap the stores
+          uint32_t pk[4][16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tc_ld32(tacc + ((uint32_t)(q * 32) << 16) + half * 128 + c * 32, r);
+            const int col0 = n0 + half * 128 + c * 32;
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
+              if (bias) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
+            }
+            if (epi & EPI_GELU) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float2 g = gelu_erf2(make_float2(v[2 * i], v[2 * i + 1]));
+                v[2 * i] = g.x;
+                v[2 * i + 1] = g.y;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[c][i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(aempty(buf));
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int col0 = n0 + half * 128 + c * 32;
+            if (row >= M || col0 >= N) continue;
+            const int64_t off = (int64_t)row * N + col0;
+            uint16_t* yp = reinterpret_cast<uint16_t*>(y) + off;
+            if (col0 + 32 <= N && (N % 16) == 0) {
+              U8x32 o0, o1;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                o0.w[i] = pk[c][i];
+                o1.w[i] = pk[c][8 + i];
+              }
+              st256(yp, o0);
+              st256(yp + 16, o1);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col0 + i < N) yp[i] = (uint16_t)(pk[c][i >> 1] >> (16 * (i & 1)));
+            }
+          }
+          continue;  // the accumulator is already released
+        }
+      }
       if constexpr (QHB == 0) {
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -1858,21 +1912,27 @@ static dit_status launch_pair_cp(const CUtensorMap& ta, const CUtensorMap& tb, c
 
 using namespace dit6;
 
-// Tile configuration.  The base default (10) is the persistent 128 x 128 kernel with two CTAs per
-// SM whose scale atoms are written into tensor memory by four dedicated warps (tcgen05.st, one
-// wide store per stage): scale copies on the tensor-core unit (tcgen05.cp) cost ~110 cycles of
-// tensor time each, and two independent MMA streams per SM hide the pipeline latency (and each
-// other's epilogue) best.  The CTA-pair kernels (15: scale writers, 18: tcgen05.cp with early
-// accumulator release) are exact but slower on every CogVideoX shape and at 8192^3 (measured on
-// GB300).  DIT6_NVFP4_TILE selects another configuration for experiments and tests.
-// Without DIT6_NVFP4_TILE the shape picks: one CTA per SM on 128 x 256 tiles (11) when K >= 3072
-// and N is a multiple of 256 -- four deeper stages then beat two CTAs per SM (CogVideoX-5B /
-// 1080p shapes: QKV 4.08 vs 3.99, FFN-down 5.39 vs 4.92, 104746 x 3072 x 12288 5.53 vs 4.90,
-// 8192^3 4.87 vs 4.66 PFLOP/s) -- else 10 (CogVideoX-2B: QKV 3.13 vs 3.08, FFN-down with
-// N = 1920 4.39 vs 4.24).
-static int nvfp4_tile_cfg(int64_t n, int64_t k) {
+// Tile configurations.  10: the persistent 128 x 128 kernel with two CTAs per SM whose scale
+// atoms are written into tensor memory by four dedicated warps (tcgen05.st, one wide store per
+// stage) -- scale copies on the tensor-core unit (tcgen05.cp) cost ~110 cycles of tensor time
+// each -- and whose two independent MMA streams per SM hide each other's epilogue.  11: the same
+// kernel on 128 x 256 tiles, one CTA per SM, four stages.  The CTA-pair kernels (15: scale
+// writers, 18: tcgen05.cp with early accumulator release) are exact but slower on every
+// CogVideoX shape and at 8192^3 (measured on GB300).  DIT6_NVFP4_TILE selects a configuration
+// for experiments and tests.
+// Without DIT6_NVFP4_TILE the call picks.  One CTA per SM on 128 x 256 tiles (11) drains its
+// accumulator into packed bf16 registers and releases it before storing, so with bf16 output
+// and no GELU it beats two CTAs per SM (10) on nearly every shape (CogVideoX-2B QKV 3.53 vs
+// 3.13, out 2.87 vs 2.74; 5B QKV 4.38 vs 3.95, FFN-down 5.38 vs 4.88; 1080p FFN-up 4.54 vs
+// 4.13; 8192^3 4.96 vs 4.58 PFLOP/s) -- except with N off the 256 grid and a long K (2B
+// FFN-down 4.32 vs 4.39).  The GELU epilogue runs before the release and keeps 10 ahead (2B
+// FFN-up 2.71 vs 2.50).  fp32 output keeps the accumulator until stored: 11 only when K >= 3072
+// and N is a multiple of 256.
+static int nvfp4_tile_cfg(int64_t n, int64_t k, int epi) {
   const char* e = getenv("DIT6_NVFP4_TILE");
   if (e) return atoi(e);
+  if (epi & EPI_GELU) return 10;
+  if (epi & EPI_BF16) return (n % 256 != 0 && k >= 4096) ? 10 : 11;
   return (k >= 3072 && n % 256 == 0) ? 11 : 10;
 }
 
@@ -1926,7 +1986,7 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
   if (!aligned32(a) || !aligned32(b) || !aligned32(a_sf) || !aligned32(b_sf) || !aligned32(y) ||
       !aligned32(ws))
     return DIT_ERR_ALIGNMENT;
-  const int cfg = nvfp4_tile_cfg(n, k);
+  const int cfg = nvfp4_tile_cfg(n, k, (y_dt == DIT_BF16 ? EPI_BF16 : 0) | (act == DIT_ACT_GELU_ERF ? EPI_GELU : 0));
   const uint32_t bn_box = (cfg == 1 || cfg == 2 || cfg == 5 || cfg == 6 || cfg == 8 || cfg == 11) ? 256 : 128;
   CUtensorMap ta, tb;
   if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(k / 2),
