@@ -822,7 +822,7 @@ static dit_status launch_r(const CUtensorMap& ta, const CUtensorMap& tb, const u
 // ---------------------------------------------------------------------------------------
 // ACC: tensor-memory accumulator buffers (2: the MMAs of tile t+1 run while the epilogue
 // drains tile t)
-template <int BN, int STAGES, int CTAS, int ACC = 1>
+template <int BN, int STAGES, int CTAS, int ACC = 1, int EPW = 0>
 struct SCfg {
   static_assert(ACC == 1 || ACC == 2, "accumulator buffers");
   static constexpr int NB = BN / 128;
@@ -835,12 +835,71 @@ struct SCfg {
   static constexpr int SF_BASE = BN * ACC;
   static constexpr int TMEM_USED = SF_BASE + STAGES * 4 * SF_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
-  static constexpr int EPI_WARPS = BN / 32;
+  static constexpr int EPI_WARPS = EPW ? EPW : BN / 32;   // 16 with BN = 256: 64 columns per warp
   static constexpr int SF_WARP0 = 2 + EPI_WARPS;
   static constexpr int THREADS = (2 + EPI_WARPS + 4) * 32;
   static_assert(TMEM_USED <= 512 / CTAS, "tensor memory");
   static_assert(SMEM_BYTES * CTAS <= 232448, "shared memory");
 };
+
+// Epilogue of 32 accumulator columns of one output row: Y = acc * (s_gA s_gB) (+ bias), then
+// GELU when asked, stored as bf16 or fp32 (256-bit stores when the chunk is whole and aligned).
+__device__ __forceinline__ void epi_store32(const uint32_t (&r)[32], float alpha, int row, int col0, int M, int N,
+                                            const float* __restrict__ bias, void* __restrict__ y, int epi) {
+  if (row >= M || col0 >= N) return;
+  float v[32];
+  const float2 al = make_float2(alpha, alpha);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 p = mul2(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), al);
+    v[2 * i] = p.x;
+    v[2 * i + 1] = p.y;
+  }
+  if (bias) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
+  }
+  if (epi & EPI_GELU) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 g = gelu_erf2(make_float2(v[2 * i], v[2 * i + 1]));
+      v[2 * i] = g.x;
+      v[2 * i + 1] = g.y;
+    }
+  }
+  const int64_t off = (int64_t)row * N + col0;
+  if (col0 + 32 <= N && (N % 16) == 0) {
+    if (epi & EPI_BF16) {
+      U8x32 o0, o1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        o0.w[i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
+        o1.w[i] = f2_to_bf16x2(v[16 + 2 * i], v[16 + 2 * i + 1]);
+      }
+      uint16_t* yp = reinterpret_cast<uint16_t*>(y) + off;
+      st256(yp, o0);
+      st256(yp + 16, o1);
+    } else {
+      float* yp = reinterpret_cast<float*>(y) + off;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        U8x32 o;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o.w[i] = __float_as_uint(v[8 * b + i]);
+        st256(yp + 8 * b, o);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (col0 + i >= N) continue;
+      if (epi & EPI_BF16)
+        reinterpret_cast<__nv_bfloat16*>(y)[off + i] = __float2bfloat16_rn(v[i]);
+      else
+        reinterpret_cast<float*>(y)[off + i] = v[i];
+    }
+  }
+}
 
 __device__ __forceinline__ void tc_st4(uint32_t taddr, const uint4& v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
@@ -873,8 +932,8 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t* r) {
 // written only when non-null.  max|H Z| over the whole output is reduced through the workspace
 // and the last CTA writes *q_sg_next = max / (6 * 448), the tensor scale the unfused quantiser
 // would derive from this Z.  Needs BN == 128 and N % 64 == 0.
-template <int BN, int STAGES, int CTAS, int QHB = 0, int ACC = 1>
-__global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC>::THREADS, CTAS)
+template <int BN, int STAGES, int CTAS, int QHB = 0, int ACC = 1, int EPW = 0>
+__global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC, EPW>::THREADS, CTAS)
     k_gemm_nvfp4_s(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
                    const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
@@ -882,7 +941,8 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC>::THREADS, CTAS)
                    void* ws, int stall, const float* __restrict__ q_sg, float q_isb,
                    uint8_t* __restrict__ q_codes, uint8_t* __restrict__ q_sf, float* __restrict__ q_sg_next) {
   static_assert(QHB == 0 || BN == 128, "fused quantisation works on 128-column tiles");
-  using C = SCfg<BN, STAGES, CTAS, ACC>;
+  static_assert(EPW == 0 || (QHB == 0 && CTAS == 1 && EPW == BN / 16), "sixteen epilogue warps: BN = 256 only");
+  using C = SCfg<BN, STAGES, CTAS, ACC, EPW>;
   constexpr int S = STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1058,6 +1118,22 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC>::THREADS, CTAS)
       tc_fence_after();
       const int row = m0 + q * 32 + lane;
       const uint32_t tacc = tmem + buf * BN;
+      if constexpr (EPW != 0) {
+        // sixteen epilogue warps, 64 columns each: load the raw accumulator words, release the
+        // accumulator, then scale, add the bias, apply the activation and store -- all of the
+        // epilogue's arithmetic overlaps the next tile's MMAs
+        const int part = e >> 2;  // 64-column quarter of the 256-column tile
+        uint32_t r0[32], r1[32];
+        tc_ld32_nowait(tacc + ((uint32_t)(q * 32) << 16) + part * 64, r0);
+        tc_ld32_nowait(tacc + ((uint32_t)(q * 32) << 16) + part * 64 + 32, r1);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(aempty(buf));
+        epi_store32(r0, alpha, row, n0 + part * 64, M, N, bias, y, epi);
+        epi_store32(r1, alpha, row, n0 + part * 64 + 32, M, N, bias, y, epi);
+        continue;  // the accumulator is already released
+      }
       if constexpr (QHB == 0 && CTAS == 1) {
         if (epi & EPI_BF16) {
           // one CTA per SM: convert the thread's 128 columns to packed bf16 in registers, release
@@ -1248,14 +1324,14 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC>::THREADS, CTAS)
   }
 }
 
-template <int BN, int STAGES, int CTAS, int QHB = 0, int ACC = 1>
+template <int BN, int STAGES, int CTAS, int QHB = 0, int ACC = 1, int EPW = 0>
 static dit_status launch_s(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf, const uint8_t* b_sf,
                            const float* a_gs, const float* b_gs, int M, int N, int K, const float* bias, void* y,
                            int epi, void* ws, cudaStream_t st, const float* q_sg = nullptr, float q_isb = 0.f,
                            uint8_t* q_codes = nullptr, uint8_t* q_sf = nullptr, float* q_sg_next = nullptr) {
-  using C = SCfg<BN, STAGES, CTAS, ACC>;
+  using C = SCfg<BN, STAGES, CTAS, ACC, EPW>;
   static bool attr_done = false;
-  auto kern = k_gemm_nvfp4_s<BN, STAGES, CTAS, QHB, ACC>;
+  auto kern = k_gemm_nvfp4_s<BN, STAGES, CTAS, QHB, ACC, EPW>;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
       return DIT_ERR_CUDA;
@@ -1313,65 +1389,6 @@ static dit_status launch(const CUtensorMap& ta, const CUtensorMap& tb, const uin
   return DIT_OK;
 }
 
-
-// Epilogue of 32 accumulator columns of one output row: Y = acc * (s_gA s_gB) (+ bias), then
-// GELU when asked, stored as bf16 or fp32 (256-bit stores when the chunk is whole and aligned).
-__device__ __forceinline__ void epi_store32(const uint32_t (&r)[32], float alpha, int row, int col0, int M, int N,
-                                            const float* __restrict__ bias, void* __restrict__ y, int epi) {
-  if (row >= M || col0 >= N) return;
-  float v[32];
-  const float2 al = make_float2(alpha, alpha);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float2 p = mul2(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), al);
-    v[2 * i] = p.x;
-    v[2 * i + 1] = p.y;
-  }
-  if (bias) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(v[i], bias[col0 + i < N ? col0 + i : N - 1]);
-  }
-  if (epi & EPI_GELU) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float2 g = gelu_erf2(make_float2(v[2 * i], v[2 * i + 1]));
-      v[2 * i] = g.x;
-      v[2 * i + 1] = g.y;
-    }
-  }
-  const int64_t off = (int64_t)row * N + col0;
-  if (col0 + 32 <= N && (N % 16) == 0) {
-    if (epi & EPI_BF16) {
-      U8x32 o0, o1;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        o0.w[i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
-        o1.w[i] = f2_to_bf16x2(v[16 + 2 * i], v[16 + 2 * i + 1]);
-      }
-      uint16_t* yp = reinterpret_cast<uint16_t*>(y) + off;
-      st256(yp, o0);
-      st256(yp + 16, o1);
-    } else {
-      float* yp = reinterpret_cast<float*>(y) + off;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        U8x32 o;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) o.w[i] = __float_as_uint(v[8 * b + i]);
-        st256(yp + 8 * b, o);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (col0 + i >= N) continue;
-      if (epi & EPI_BF16)
-        reinterpret_cast<__nv_bfloat16*>(y)[off + i] = __float2bfloat16_rn(v[i]);
-      else
-        reinterpret_cast<float*>(y)[off + i] = v[i];
-    }
-  }
-}
 
 // ---------------------------------------------------------------------------------------
 // CTA-pair variant: tcgen05.mma.cta_group::2 ... block_scale on 256 x 256 output tiles over
@@ -1916,22 +1933,23 @@ using namespace dit6;
 // atoms are written into tensor memory by four dedicated warps (tcgen05.st, one wide store per
 // stage) -- scale copies on the tensor-core unit (tcgen05.cp) cost ~110 cycles of tensor time
 // each -- and whose two independent MMA streams per SM hide each other's epilogue.  11: the same
-// kernel on 128 x 256 tiles, one CTA per SM, four stages.  The CTA-pair kernels (15: scale
-// writers, 18: tcgen05.cp with early accumulator release) are exact but slower on every
-// CogVideoX shape and at 8192^3 (measured on GB300).  DIT6_NVFP4_TILE selects a configuration
-// for experiments and tests.
-// Without DIT6_NVFP4_TILE the call picks.  One CTA per SM on 128 x 256 tiles (11) drains its
-// accumulator into packed bf16 registers and releases it before storing, so with bf16 output
-// and no GELU it beats two CTAs per SM (10) on nearly every shape (CogVideoX-2B QKV 3.53 vs
-// 3.13, out 2.87 vs 2.74; 5B QKV 4.38 vs 3.95, FFN-down 5.38 vs 4.88; 1080p FFN-up 4.54 vs
-// 4.13; 8192^3 4.96 vs 4.58 PFLOP/s) -- except with N off the 256 grid and a long K (2B
-// FFN-down 4.32 vs 4.39).  The GELU epilogue runs before the release and keeps 10 ahead (2B
-// FFN-up 2.71 vs 2.50).  fp32 output keeps the accumulator until stored: 11 only when K >= 3072
-// and N is a multiple of 256.
+// kernel on 128 x 256 tiles, one CTA per SM, four stages; with bf16 output its eight epilogue
+// warps convert their 128 columns to packed bf16 registers and release the accumulator before
+// storing.  23: 11 with sixteen epilogue warps of 64 columns that release the accumulator right
+// after loading it, so bias, activation and stores all overlap the next tile's MMAs.  The
+// CTA-pair kernels (15: scale writers, 18: tcgen05.cp with early accumulator release) are exact
+// but slower on every CogVideoX shape and at 8192^3 (measured on GB300).  DIT6_NVFP4_TILE selects
+// a configuration for experiments and tests.
+// Without DIT6_NVFP4_TILE the call picks (PFLOP/s, GB300).  With the GELU epilogue 23 leads
+// everywhere: CogVideoX-2B FFN-up 3.27 (10: 2.69, 11: 2.48), 5B FFN-up 4.11 (3.46), 1080p
+// FFN-up 4.26 (3.55), 8192^3 4.84 (4.34).  Without it, for bf16 output 11 leads or ties (2B QKV
+// 3.50 vs 3.08 / 3.42 for 23; 5B QKV 4.39 / 4.45; 1080p FFN-up 4.54 / 4.63) except with N off
+// the 256 grid and a long K, where 10 does (2B FFN-down 4.39 vs 4.32).  fp32 output keeps the
+// accumulator until stored in 10 and 11: 11 only when K >= 3072 and N is a multiple of 256.
 static int nvfp4_tile_cfg(int64_t n, int64_t k, int epi) {
   const char* e = getenv("DIT6_NVFP4_TILE");
   if (e) return atoi(e);
-  if (epi & EPI_GELU) return 10;
+  if (epi & EPI_GELU) return 23;
   if (epi & EPI_BF16) return (n % 256 != 0 && k >= 4096) ? 10 : 11;
   return (k >= 3072 && n % 256 == 0) ? 11 : 10;
 }
@@ -1987,7 +2005,7 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
       !aligned32(ws))
     return DIT_ERR_ALIGNMENT;
   const int cfg = nvfp4_tile_cfg(n, k, (y_dt == DIT_BF16 ? EPI_BF16 : 0) | (act == DIT_ACT_GELU_ERF ? EPI_GELU : 0));
-  const uint32_t bn_box = (cfg == 1 || cfg == 2 || cfg == 5 || cfg == 6 || cfg == 8 || cfg == 11) ? 256 : 128;
+  const uint32_t bn_box = (cfg == 1 || cfg == 2 || cfg == 5 || cfg == 6 || cfg == 8 || cfg == 11 || cfg == 23) ? 256 : 128;
   CUtensorMap ta, tb;
   if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(k / 2),
                       (uint64_t)m, (uint64_t)(k / 2), f4::BK / 2, f4::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -2010,6 +2028,7 @@ extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, con
       return f4::launch_p<256, 4, 1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 9: return f4::launch_p<128, 3, 1, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     default: return f4::launch_s<128, 3, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
+    case 23: return f4::launch_s<256, 4, 1, 0, 1, 16>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 11: return f4::launch_s<256, 4, 1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 12: return f4::launch_s<128, 6, 1>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);
     case 13: return f4::launch_s<128, 6, 1, 0, 2>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, yb, ws, st);

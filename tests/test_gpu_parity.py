@@ -394,7 +394,7 @@ def _nvfp4_operands(m, n, k, seed):
     return qa, qb, out[0], out[1]
 
 
-@pytest.mark.parametrize("cfg", ["0", "1", "2", "3", "4", "5", "6", "7", "8", "9", "10", "11", "12", "13", "14", "15", "18"])
+@pytest.mark.parametrize("cfg", ["0", "1", "2", "3", "4", "5", "6", "7", "8", "9", "10", "11", "12", "13", "14", "15", "18", "23"])
 @pytest.mark.parametrize("m,n,k", [(256, 512, 128), (300, 384, 1920), (129, 256, 7680), (128, 128, 64),
                                    (77, 136, 320)])
 def test_nvfp4_gemm_parity(m, n, k, cfg, ws, monkeypatch):
