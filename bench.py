@@ -7,8 +7,10 @@ block to INT8 (Gamma > 0.05) or NVFP4.  Synthetic, seeded inputs (no trained wei
 
 One step = one pass over the 30 blocks: for each block its four routed linears (online
 block Hadamard + activation quantisation + quantised GEMM; GELU (erf form) fused into the
-FFN-up epilogue, whose output is the FFN-down input) and the delta-cache commit
-(residual delta, Gamma_t for the next step's routing, similarity of the last two deltas).
+FFN-up epilogue, whose output is the FFN-down input; when both FFN linears route NVFP4 the
+FFN-up epilogue also yields its output's NVFP4 tensor scale, so FFN-down's quantisation is
+one pass) and the delta-cache commit (residual delta, Gamma_t for the next step's routing,
+similarity of the last two deltas).
 value = algorithmic GEMM FLOPs of the step / step time (TFLOP/s).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -189,6 +191,7 @@ class Workload:
                                 "has_delta": False})
         self.y = {name: torch.empty(M, n, dtype=torch.bfloat16, device=dev) for name, _, n in LINEARS}
         self.gamma = torch.empty(NBLOCKS, dtype=torch.float32, device=dev)
+        self.up_scale = torch.empty(1, dtype=torch.float32, device=dev)   # FFN-up output's NVFP4 tensor scale
         self.sim = torch.empty(NBLOCKS, dtype=torch.float32, device=dev)
         # routing from the predictor (one Gamma per block; the commit of every step
         # recomputes it, and with fixed pairs the routes stay the same)
@@ -205,9 +208,12 @@ class Workload:
 
     def launches_per_step(self):
         n = 0
+        nv = self.dit.ROUTE_NVFP4
         for b in range(NBLOCKS):
-            for r in self.routes[b]:
-                n += 2 if r == self.dit.ROUTE_INT8 else 3
+            rr = self.routes[b]
+            chained = rr[2] == nv and rr[3] == nv   # FFN-down's quantisation is one pass
+            for li, r in enumerate(rr):
+                n += 2 if r == self.dit.ROUTE_INT8 or (chained and li == 3) else 3
             n += 1
         return n
 
@@ -245,11 +251,20 @@ class Workload:
                     self._timed("gemm_int8", lambda: dit.qgemm_int8(lin.a8["q"], lin.a8["scale"], w8["q"],
                                                                     w8["scale"], y, self.ws, act=act))
                 else:
+                    # FFN-up -> FFN-down both on NVFP4: the FFN-up GEMM's epilogue also yields its
+                    # output's tensor scale, and FFN-down's quantisation is then one pass
+                    chained = self.routes[b][2] == dit.ROUTE_NVFP4 and self.routes[b][3] == dit.ROUTE_NVFP4
+                    ts_in = self.up_scale if (chained and name == "ffn_down") else None
                     self._timed("quant_nvfp4", lambda: dit.hadamard_quant_nvfp4(
-                        x, HBLOCK, lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], self.ws))
-                    self._timed("gemm_nvfp4", lambda: dit.qgemm_nvfp4(
-                        lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], lin.w.nvfp4["codes"], lin.w.nvfp4["sf"],
-                        lin.w.nvfp4["gs"], y, self.ws, act=act))
+                        x, HBLOCK, lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], self.ws, tensor_scale_in=ts_in))
+                    if chained and name == "ffn_up":
+                        self._timed("gemm_nvfp4", lambda: dit.qgemm_nvfp4_amax(
+                            lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], lin.w.nvfp4["codes"], lin.w.nvfp4["sf"],
+                            lin.w.nvfp4["gs"], y, self.ws, HBLOCK, self.up_scale, act=act))
+                    else:
+                        self._timed("gemm_nvfp4", lambda: dit.qgemm_nvfp4(
+                            lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], lin.w.nvfp4["codes"], lin.w.nvfp4["sf"],
+                            lin.w.nvfp4["gs"], y, self.ws, act=act))
             d_new, d_old = blk["d"][0], blk["d"][1]
             self._timed("tdc_commit", lambda: dit.tdc_step(
                 dit.TDC_COMMIT, self.x_in, self.ws, x_out=self.x_out[b], d1=d_old if blk["has_delta"] else None,

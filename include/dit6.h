@@ -221,6 +221,28 @@ dit_status dit_qgemm_nvfp4_fused_quant(const uint8_t* a, const uint8_t* a_sf, co
                                        void* ws, size_t ws_bytes, dit_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * NVFP4 GEMM whose epilogue also produces the tensor scale of its own output for the next
+ * NVFP4 layer (FFN up -> down): the two-phase form of fusing the next layer's quantisation.
+ * [EN] 2.A Mechanism 2-3 (online block Hadamard before NVFP4 quantisation): the dynamic
+ * tensor scale of the next layer's input is max|H Z| / (6 * 448) over the whole tensor, so it
+ * can only be applied once every output tile is known; this call computes it on the fly and
+ * the next layer's dit_hadamard_quant_nvfp4(tensor_scale_in = *tensor_scale_out) is then one
+ * pass instead of two, with the same codes and scales byte for byte.
+ *
+ * y = act(dit_qgemm_nvfp4 product (+ bias)) in bf16 -- the same bytes dit_qgemm_nvfp4 writes;
+ * *tensor_scale_out (device float) = max over y of |block Hadamard (blocks of hblock along n,
+ * orthonormal) of y as stored| / (6 * 448), exactly the tensor scale
+ * dit_hadamard_quant_nvfp4(y, hblock, ...) derives.  hblock in {16, 32, 64}; n % 64 == 0;
+ * k % 64 == 0; y device bf16 [m x n], 32-byte aligned.  The workspace's amax word and
+ * completion ticket are used and left reset.
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_qgemm_nvfp4_amax(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
+                                const uint8_t* b, const uint8_t* b_sf, const float* b_gs,
+                                int64_t m, int64_t n, int64_t k, const float* bias, dit_act act,
+                                void* y, int hblock, float* tensor_scale_out, void* ws,
+                                size_t ws_bytes, dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * PDR outlier ratio and the BF16 route.  [EN] 2.C first bullet, [ZH] 2.C: a layer whose
  * input has a high outlier ratio runs in full precision.  The pages do not define the
  * ratio; reading: the fraction of elements with |x| > k_sigma * RMS(x) over the whole block

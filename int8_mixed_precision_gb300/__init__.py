@@ -156,6 +156,16 @@ def qgemm_nvfp4_fused_quant(a, a_sf, a_gs, b, b_sf, b_gs, ws, hblock, q_scale_in
     _check(st, "dit_qgemm_nvfp4_fused_quant")
 
 
+def qgemm_nvfp4_amax(a, a_sf, a_gs, b, b_sf, b_gs, y, ws, hblock, tensor_scale_out, bias=None, act=ACT_NONE,
+                     stream=None):
+    """NVFP4 GEMM into bf16 y whose epilogue also writes y's NVFP4 tensor scale (the one
+    hadamard_quant_nvfp4(y, hblock, ...) would derive) to tensor_scale_out (device float [1])."""
+    m, n, k = a.shape[0], b.shape[0], a.shape[1] * 2
+    st = lib().dit_qgemm_nvfp4_amax(_p(a), _p(a_sf), _p(a_gs), _p(b), _p(b_sf), _p(b_gs), m, n, k, _p(bias), act,
+                                    _p(y), hblock, _p(tensor_scale_out), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dit_qgemm_nvfp4_amax")
+
+
 def qgemm_int8(a, a_scale, b, b_scale, y, ws, bias=None, acc_debug=None, act=ACT_NONE, stream=None):
     """a, b: int8 codes (IMMA path) or bf16-held integer codes (tcgen05 bf16 path)."""
     if a.dtype != b.dtype:

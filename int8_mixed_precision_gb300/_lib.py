@@ -31,6 +31,8 @@ SIGNATURES = {
     "dit_hadamard_quant_int8": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _i32, _vp, _vp]),
     "dit_qgemm_nvfp4": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _sz,
                                 _vp]),
+    "dit_qgemm_nvfp4_amax": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp,
+                                     _sz, _vp]),
     "dit_qgemm_nvfp4_fused_quant": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32,
                                             _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dit_nvfp4_to_int8": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp, _i32, _vp, _vp]),

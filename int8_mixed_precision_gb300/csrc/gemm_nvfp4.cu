@@ -843,11 +843,10 @@ struct SCfg {
 };
 
 // Epilogue of 32 accumulator columns of one output row: Y = acc * (s_gA s_gB) (+ bias), then
-// GELU when asked, stored as bf16 or fp32 (256-bit stores when the chunk is whole and aligned).
-__device__ __forceinline__ void epi_store32(const uint32_t (&r)[32], float alpha, int row, int col0, int M, int N,
-                                            const float* __restrict__ bias, void* __restrict__ y, int epi) {
-  if (row >= M || col0 >= N) return;
-  float v[32];
+// GELU when asked (epi_values32); stored as bf16 or fp32, with 256-bit stores when the chunk is
+// whole and aligned (epi_write32).
+__device__ __forceinline__ void epi_values32(const uint32_t (&r)[32], float alpha, int col0, int N,
+                                             const float* __restrict__ bias, int epi, float (&v)[32]) {
   const float2 al = make_float2(alpha, alpha);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -867,6 +866,10 @@ __device__ __forceinline__ void epi_store32(const uint32_t (&r)[32], float alpha
       v[2 * i + 1] = g.y;
     }
   }
+}
+__device__ __forceinline__ void epi_write32(const float (&v)[32], int row, int col0, int M, int N,
+                                            void* __restrict__ y, int epi) {
+  if (row >= M || col0 >= N) return;
   const int64_t off = (int64_t)row * N + col0;
   if (col0 + 32 <= N && (N % 16) == 0) {
     if (epi & EPI_BF16) {
@@ -900,6 +903,13 @@ __device__ __forceinline__ void epi_store32(const uint32_t (&r)[32], float alpha
     }
   }
 }
+__device__ __forceinline__ void epi_store32(const uint32_t (&r)[32], float alpha, int row, int col0, int M, int N,
+                                            const float* __restrict__ bias, void* __restrict__ y, int epi) {
+  if (row >= M || col0 >= N) return;
+  float v[32];
+  epi_values32(r, alpha, col0, N, bias, epi, v);
+  epi_write32(v, row, col0, M, N, y, epi);
+}
 
 __device__ __forceinline__ void tc_st4(uint32_t taddr, const uint4& v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
@@ -932,7 +942,11 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t* r) {
 // written only when non-null.  max|H Z| over the whole output is reduced through the workspace
 // and the last CTA writes *q_sg_next = max / (6 * 448), the tensor scale the unfused quantiser
 // would derive from this Z.  Needs BN == 128 and N % 64 == 0.
-template <int BN, int STAGES, int CTAS, int QHB = 0, int ACC = 1, int EPW = 0>
+// AHB > 0 (16, 32 or 64; with EPW = 16, bf16 output): the epilogue also reduces max|H Z| over
+// the output Z as stored in bf16 (block Hadamard along N in blocks of AHB, orthonormal) and the
+// last CTA writes *q_sg_next = max / (6 * 448) -- the tensor scale dit_hadamard_quant_nvfp4
+// derives from Z in its amax pass -- so the next NVFP4 layer's quantisation is one pass.
+template <int BN, int STAGES, int CTAS, int QHB = 0, int ACC = 1, int EPW = 0, int AHB = 0>
 __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC, EPW>::THREADS, CTAS)
     k_gemm_nvfp4_s(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const uint8_t* __restrict__ a_sf, const uint8_t* __restrict__ b_sf,
@@ -942,6 +956,8 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC, EPW>::THREADS, CTA
                    uint8_t* __restrict__ q_codes, uint8_t* __restrict__ q_sf, float* __restrict__ q_sg_next) {
   static_assert(QHB == 0 || BN == 128, "fused quantisation works on 128-column tiles");
   static_assert(EPW == 0 || (QHB == 0 && CTAS == 1 && EPW == BN / 16), "sixteen epilogue warps: BN = 256 only");
+  static_assert(AHB == 0 || EPW != 0, "the output's Hadamard amax needs the 64-column epilogue warps");
+  constexpr bool TRACK_AMAX = QHB > 0 || AHB > 0;
   using C = SCfg<BN, STAGES, CTAS, ACC, EPW>;
   constexpr int S = STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -1130,8 +1146,30 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC, EPW>::THREADS, CTA
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(aempty(buf));
-        epi_store32(r0, alpha, row, n0 + part * 64, M, N, bias, y, epi);
-        epi_store32(r1, alpha, row, n0 + part * 64 + 32, M, N, bias, y, epi);
+        const int col0 = n0 + part * 64;
+        if constexpr (AHB > 0) {
+          if (row < M && col0 < N) {  // N % 64 == 0: the 64 columns are one transform unit
+            float v0[32], v1[32];
+            epi_values32(r0, alpha, col0, N, bias, epi, v0);
+            epi_values32(r1, alpha, col0 + 32, N, bias, epi, v1);
+            epi_write32(v0, row, col0, M, N, y, epi);
+            epi_write32(v1, row, col0 + 32, M, N, y, epi);
+            float2 z[32];  // the values as stored (bf16), transformed
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              z[i] = bf16x2_to_f2(f2_to_bf16x2(v0[2 * i], v0[2 * i + 1]));
+              z[16 + i] = bf16x2_to_f2(f2_to_bf16x2(v1[2 * i], v1[2 * i + 1]));
+            }
+            fwht64<AHB>(z);
+            const float2 c = make_float2(q_isb, q_isb);
+#pragma unroll
+            for (int p = 0; p < 32; ++p) z[p] = mul2(z[p], c);
+            q_amax = fmaxf(q_amax, amax_range(z, 0, 32));
+          }
+        } else {
+          epi_store32(r0, alpha, row, col0, M, N, bias, y, epi);
+          epi_store32(r1, alpha, row, col0 + 32, M, N, bias, y, epi);
+        }
         continue;  // the accumulator is already released
       }
       if constexpr (QHB == 0 && CTAS == 1) {
@@ -1298,14 +1336,14 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC, EPW>::THREADS, CTA
       if (lane == 0) mbar_arrive(aempty(buf));
     }
     tc_fence_before();
-    if constexpr (QHB > 0) {
+    if constexpr (TRACK_AMAX) {
       const float m = warp_max_f(q_amax);
       if (lane == 0) atomicMax(ws_u32(ws, WS_AMAX), __float_as_uint(m));
     }
   }
 
   __syncthreads();
-  if constexpr (QHB > 0) {  // the last CTA turns the whole output's max|H Z| into its tensor scale
+  if constexpr (TRACK_AMAX) {  // the last CTA turns the whole output's max|H Z| into its tensor scale
     if (threadIdx.x == 0) {
       __threadfence();
       const uint32_t t = atomicAdd(ws_u32(ws, WS_TICKET), 1u);
@@ -1324,14 +1362,14 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, ACC, EPW>::THREADS, CTA
   }
 }
 
-template <int BN, int STAGES, int CTAS, int QHB = 0, int ACC = 1, int EPW = 0>
+template <int BN, int STAGES, int CTAS, int QHB = 0, int ACC = 1, int EPW = 0, int AHB = 0>
 static dit_status launch_s(const CUtensorMap& ta, const CUtensorMap& tb, const uint8_t* a_sf, const uint8_t* b_sf,
                            const float* a_gs, const float* b_gs, int M, int N, int K, const float* bias, void* y,
                            int epi, void* ws, cudaStream_t st, const float* q_sg = nullptr, float q_isb = 0.f,
                            uint8_t* q_codes = nullptr, uint8_t* q_sf = nullptr, float* q_sg_next = nullptr) {
   using C = SCfg<BN, STAGES, CTAS, ACC, EPW>;
   static bool attr_done = false;
-  auto kern = k_gemm_nvfp4_s<BN, STAGES, CTAS, QHB, ACC, EPW>;
+  auto kern = k_gemm_nvfp4_s<BN, STAGES, CTAS, QHB, ACC, EPW, AHB>;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
       return DIT_ERR_CUDA;
@@ -1987,6 +2025,38 @@ extern "C" dit_status dit_qgemm_nvfp4_fused_quant(const uint8_t* a, const uint8_
   if (hblock == 32) DIT6_FQ(32);
   DIT6_FQ(64);
 #undef DIT6_FQ
+}
+
+extern "C" dit_status dit_qgemm_nvfp4_amax(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
+                                           const uint8_t* b, const uint8_t* b_sf, const float* b_gs, int64_t m,
+                                           int64_t n, int64_t k, const float* bias, dit_act act, void* y,
+                                           int hblock, float* tensor_scale_out, void* ws, size_t ws_bytes,
+                                           dit_stream_t stream) {
+  if (!a || !a_sf || !a_gs || !b || !b_sf || !b_gs || !y || !tensor_scale_out || !ws || ws_bytes < WS_BYTES)
+    return DIT_ERR_INVALID_ARG;
+  if (m <= 0 || n <= 0 || k <= 0 || m > 0x7fffffff || n > 0x7fffffff || k > 0x7fffffff)
+    return DIT_ERR_INVALID_ARG;
+  if (act != DIT_ACT_NONE && act != DIT_ACT_GELU_ERF) return DIT_ERR_INVALID_ARG;
+  if (hblock != 16 && hblock != 32 && hblock != 64) return DIT_ERR_UNSUPPORTED;
+  if (k % 64 || n % 64) return DIT_ERR_UNSUPPORTED;
+  if (!aligned32(a) || !aligned32(b) || !aligned32(a_sf) || !aligned32(b_sf) || !aligned32(y) || !aligned32(ws))
+    return DIT_ERR_ALIGNMENT;
+  CUtensorMap ta, tb;
+  if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(a), (uint64_t)(k / 2),
+                      (uint64_t)m, (uint64_t)(k / 2), f4::BK / 2, f4::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<uint8_t*>(b), (uint64_t)(k / 2),
+                      (uint64_t)n, (uint64_t)(k / 2), f4::BK / 2, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+    return DIT_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int epi = EPI_BF16 | (act == DIT_ACT_GELU_ERF ? EPI_GELU : 0);
+  const float isb = (float)(1.0 / sqrt((double)hblock));
+#define DIT6_AM(HB_)                                                                                             \
+  return f4::launch_s<256, 4, 1, 0, 1, 16, HB_>(ta, tb, a_sf, b_sf, a_gs, b_gs, (int)m, (int)n, (int)k, bias, y, \
+                                                epi, ws, st, nullptr, isb, nullptr, nullptr, tensor_scale_out)
+  if (hblock == 16) DIT6_AM(16);
+  if (hblock == 32) DIT6_AM(32);
+  DIT6_AM(64);
+#undef DIT6_AM
 }
 
 extern "C" dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,

@@ -36,7 +36,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["dit_gamma_route", "dit_hadamard_quant_nvfp4", "dit_hadamard_quant_int8",
-              "dit_qgemm_nvfp4", "dit_qgemm_nvfp4_fused_quant", "dit_nvfp4_to_int8", "dit_qgemm_int8",
+              "dit_qgemm_nvfp4", "dit_qgemm_nvfp4_fused_quant", "dit_qgemm_nvfp4_amax", "dit_nvfp4_to_int8", "dit_qgemm_int8",
               "dit_outlier_ratio", "dit_gemm_bf16", "dit_route_host_pdr", "dit_tdc_step", "dit_sf_index", "dit_status_str"]:
         assert n in names
 
@@ -93,6 +93,12 @@ def test_host_argument_validation_without_device_work(L):
     assert F(ws, ws, ws, ws, ws, ws, 4, 128, 128, nul, 0, nul, 128, ws, ws, ws, ws, ws, wsb, nul) == 3
     assert F(ws, ws, ws, ws, ws, ws, 4, 96, 128, nul, 0, nul, 64, ws, ws, ws, ws, ws, wsb, nul) == 3
     assert F(ws, ws, ws, ws, ws, ws, 4, 128, 128, nul, 0, fake_misaligned, 64, ws, ws, ws, ws, ws, wsb, nul) == 2
+    # GEMM with its output's tensor scale: missing scale output, unsupported block, n % 64, misalignment
+    G = L.dit_qgemm_nvfp4_amax
+    assert G(ws, ws, ws, ws, ws, ws, 4, 128, 128, nul, 0, ws, 64, nul, ws, wsb, nul) == 1
+    assert G(ws, ws, ws, ws, ws, ws, 4, 128, 128, nul, 0, ws, 128, ws, ws, wsb, nul) == 3
+    assert G(ws, ws, ws, ws, ws, ws, 4, 96, 128, nul, 0, ws, 64, ws, ws, wsb, nul) == 3
+    assert G(ws, ws, ws, ws, ws, ws, 4, 128, 128, nul, 0, fake_misaligned, 64, ws, ws, wsb, nul) == 2
     # NVFP4 -> INT8 weights: missing pointer, k not a multiple of 64, misaligned codes
     assert L.dit_nvfp4_to_int8(nul, ws, ws, 4, 128, ws, 2, ws, nul) == 1
     assert L.dit_nvfp4_to_int8(ws, ws, ws, 4, 96, ws, 2, ws, nul) == 3

@@ -417,6 +417,52 @@ def test_nvfp4_gemm_parity(m, n, k, cfg, ws, monkeypatch):
     assert rel_fro(host(y), D.gelu_erf(ref + host(bias)[None, :])) <= GEMM_TOL
 
 
+@pytest.mark.parametrize("m,n,k,hb,act", [(300, 512, 320, 64, 1), (256, 384, 128, 32, 0), (129, 768, 1920, 16, 1),
+                                          (77, 128, 64, 64, 1), (1000, 1024, 640, 64, 0)])
+def test_nvfp4_gemm_output_tensor_scale(m, n, k, hb, act, ws):
+    """The GEMM that also returns its output's NVFP4 tensor scale: y is byte-identical to
+    dit_qgemm_nvfp4's, the scale equals the oracle's max|H y| / (6 * 448) over y as stored, and
+    the one-pass quantisation with it equals the two-pass one byte for byte."""
+    qa, qb, A, B = _nvfp4_operands(m, n, k, seed=5 * m + n + k)
+    bias = torch.linspace(-1, 1, n, device="cuda", dtype=torch.float32) if act else None
+    y_ref = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], y_ref, ws, bias=bias, act=act)
+    y = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    sc = torch.full((1,), -1.0, dtype=torch.float32, device="cuda")
+    for _ in range(2):  # twice: the workspace's amax word and ticket come back reset
+        dit.qgemm_nvfp4_amax(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], y, ws, hb, sc, bias=bias,
+                             act=act)
+        _status_clean(ws)
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+        ref_sg = D.nvfp4_tensor_scale(D.block_fwht_f32(F.bf16_bits_to_f32(host(y)), hb))
+        assert host(sc)[0] == np.float32(ref_sg)
+    two, one = dit.alloc_nvfp4(m, n), dit.alloc_nvfp4(m, n)
+    dit.hadamard_quant_nvfp4(y, hb, two["codes"], two["sf"], two["gs"], ws)
+    dit.hadamard_quant_nvfp4(y, hb, one["codes"], one["sf"], one["gs"], ws, tensor_scale_in=sc)
+    _status_clean(ws)
+    assert torch.equal(one["codes"], two["codes"]) and torch.equal(one["sf"], two["sf"])
+    assert one["gs"].view(torch.int32).item() == two["gs"].view(torch.int32).item()
+
+
+def test_nvfp4_gemm_output_tensor_scale_full_size(ws):
+    """CogVideoX-2B FFN-up at full size (17776 x 1920 -> 7680, GELU): the returned scale is the
+    one the two-pass quantiser derives from the same output, bit for bit."""
+    m, k, n, hb = synth.TOKENS_2B, 1920, 7680, 64
+    x, xd = make_x(m, k, "bf16", seed=71)
+    wq = dit.QuantizedWeight(dev_f32(synth.weights(n, k, seed=72)), hb, ws)
+    a4 = dit.alloc_nvfp4(m, k)
+    dit.hadamard_quant_nvfp4(xd, hb, a4["codes"], a4["sf"], a4["gs"], ws)
+    W = wq.nvfp4
+    y = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    sc = torch.empty(1, dtype=torch.float32, device="cuda")
+    dit.qgemm_nvfp4_amax(a4["codes"], a4["sf"], a4["gs"], W["codes"], W["sf"], W["gs"], y, ws, hb, sc,
+                         act=dit.ACT_GELU_ERF)
+    q = dit.alloc_nvfp4(m, n)
+    dit.hadamard_quant_nvfp4(y, hb, q["codes"], q["sf"], q["gs"], ws)
+    _status_clean(ws)
+    assert sc.view(torch.int32).item() == q["gs"].view(torch.int32).item()
+
+
 @pytest.mark.parametrize("m,n,k,hb,act,with_y", [(300, 512, 320, 64, 1, True), (256, 384, 128, 32, 0, False),
                                                  (129, 768, 1920, 16, 1, True), (77, 128, 64, 64, 1, False)])
 def test_nvfp4_fused_epilogue_quant(m, n, k, hb, act, with_y, ws):
