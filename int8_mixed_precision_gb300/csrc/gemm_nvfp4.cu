@@ -7,15 +7,21 @@
 // Y[m,n] = s_gA s_gB sum_k dec(A)[m,k] dec(sA)[m,k/16] dec(B)[n,k] dec(sB)[n,k/16]
 //
 // Design (sm_103a): tcgen05.mma kind::mxf4nvf4 block_scale scale_vec::4X (E2M1 operands,
-// UE4M3 scales per 16 elements, fp32 accumulator in tensor memory).  Warp-specialised CTA:
-//   warp 0  : TMA producer -- 2-D tiled loads (128-byte swizzle) of the packed A/B tiles and
-//             1-D bulk copies of the matching 512-byte scale atoms, into a STAGES-deep ring
-//             guarded by full/empty mbarriers;
-//   warp 1  : allocates tensor memory; one lane copies each K=64 step's scales from shared
-//             to tensor memory (tcgen05.cp 32x128b.warpx4) and issues the MMA; a
-//             tcgen05.commit per stage frees the ring slot;
-//   warps 2-5: epilogue -- tcgen05.ld of the accumulator (one TMEM lane quarter each),
-//             global scale (+bias), bf16/fp32 conversion, 256-bit stores.
+// UE4M3 scales per 16 elements, fp32 accumulator in tensor memory).  The default kernel
+// (k_gemm_nvfp4_s) is persistent and warp-specialised:
+//   warp 0    : TMA producer -- 2-D tiled loads (128-byte swizzle) of the packed A/B tiles and
+//               1-D bulk copies of the matching 512-byte scale atoms, into a STAGES-deep ring
+//               guarded by full/empty mbarriers;
+//   warp 1    : allocates tensor memory; one lane issues each stage's MMAs and a
+//               tcgen05.commit per stage that frees the ring slot;
+//   4 warps   : scale writers -- read each stage's scale atoms from shared memory and write
+//               them into the stage's tensor-memory slot with tcgen05.st (off the tensor
+//               pipe), then arrive on the stage's sf_ready barrier;
+//   the rest  : epilogue -- tcgen05.ld of the accumulator, global scale (+bias, GELU),
+//               bf16/fp32 conversion, 256-bit stores; optionally the output's Hadamard amax
+//               or the next layer's NVFP4 encoding.
+// The other tile configurations (tcgen05.cp scale copies, CTA pairs, resident scale bands)
+// are kept for tests and measurements; the host picks one per call.
 // Every mbarrier wait is bounded (%globaltimer); on expiry the CTA records
 // DIT_ERR_TIMEOUT in the workspace, lets in-flight copies and MMAs land, frees its tensor
 // memory and exits.
