@@ -44,7 +44,46 @@ def _dt(t) -> int:
 
 
 def _p(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device pointer of a buffer argument.  The kernels read every buffer as a dense array on
+    the current device, so a host tensor or a strided view is refused here, before any launch."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise DitError(f"buffers must be CUDA tensors (got one on {t.device})")
+    if not t.is_contiguous():
+        raise DitError("buffers must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, nbytes: int, what: str) -> None:
+    """Refuse a buffer smaller than the bytes the call will read or write."""
+    if t is not None and t.numel() * t.element_size() < nbytes:
+        raise DitError(f"{what}: {t.numel() * t.element_size()} bytes, the call needs {nbytes}")
+
+
+def _same_device(*ts) -> None:
+    devs = {t.device for t in ts if t is not None}
+    if len(devs) > 1:
+        raise DitError(f"buffers on different devices: {sorted(str(d) for d in devs)}")
+
+
+def _bias_ok(bias, n: int) -> None:
+    if bias is not None:
+        if bias.dtype != _torch().float32:
+            raise DitError("bias must be float32")
+        _need(bias, 4 * n, "bias")
+
+
+def _nvfp4_gemm_args(a, a_sf, a_gs, b, b_sf, b_gs, bias):
+    if a.dim() != 2 or b.dim() != 2 or b.shape[1] != a.shape[1]:
+        raise DitError("NVFP4 GEMM: a [m, k/2] and b [n, k/2] packed codes with the same k")
+    m, n, k = a.shape[0], b.shape[0], a.shape[1] * 2
+    _need(a_sf, sf_bytes(m, k), "a_sf")
+    _need(b_sf, sf_bytes(n, k), "b_sf")
+    _need(a_gs, 4, "a_gs")
+    _need(b_gs, 4, "b_gs")
+    _bias_ok(bias, n)
+    return m, n, k
 
 
 def _stream(stream=None):
@@ -100,10 +139,19 @@ def sf_index(row: int, kblock: int, rows: int, k: int) -> int:
 # ----------------------------------------------------------------------------------------
 
 
+def _gamma_args(x_in, x_out, n, gamma, routes):
+    if x_out.dtype != x_in.dtype or x_out.numel() != x_in.numel():
+        raise DitError("x_in and x_out must have the same dtype and size")
+    _need(gamma, 4, "gamma")
+    _need(routes, 4 * n, "routes")
+
+
 def gamma_route(x_in, x_out, alpha, beta, thr, gamma, routes, ws, stream=None):
     """Gamma = |x_out - x_in|_1 / |x_in|_1 and per-layer routes (device outputs)."""
     n = len(alpha)
     arr = ctypes.c_float * max(n, 1)
+    _gamma_args(x_in, x_out, n, gamma, routes)
+    _same_device(x_in, x_out, gamma, routes, ws)
     st = lib().dit_gamma_route(_p(x_in), _p(x_out), _dt(x_in), x_in.numel(), arr(*alpha),
                                arr(*beta), arr(*thr), n, _p(gamma), _p(routes), _p(ws),
                                ws.numel(), _stream(stream))
@@ -116,6 +164,8 @@ def gamma_route_noalloc(x_in, x_out, alpha, beta, thr, gamma, routes, stream=Non
     share that array, so calls running concurrently on different streams race."""
     n = len(alpha)
     arr = ctypes.c_float * max(n, 1)
+    _gamma_args(x_in, x_out, n, gamma, routes)
+    _same_device(x_in, x_out, gamma, routes)
     st = lib().dit_gamma_route_noalloc(_p(x_in), _p(x_out), _dt(x_in), x_in.numel(), arr(*alpha),
                                        arr(*beta), arr(*thr), n, _p(gamma), _p(routes), _stream(stream))
     _check(st, "dit_gamma_route_noalloc")
@@ -123,6 +173,11 @@ def gamma_route_noalloc(x_in, x_out, alpha, beta, thr, gamma, routes, stream=Non
 
 def hadamard_quant_nvfp4(x, hblock, codes, sf, tensor_scale, ws, tensor_scale_in=None, stream=None):
     rows, k = x.shape
+    _need(codes, rows * k // 2, "codes")
+    _need(sf, sf_bytes(rows, k), "sf")
+    _need(tensor_scale, 4, "tensor_scale")
+    _need(tensor_scale_in, 4, "tensor_scale_in")
+    _same_device(x, codes, sf, tensor_scale, tensor_scale_in, ws)
     st = lib().dit_hadamard_quant_nvfp4(_p(x), _dt(x), rows, k, hblock, _p(codes), _p(sf),
                                         _p(tensor_scale), _p(tensor_scale_in), _p(ws), ws.numel(),
                                         _stream(stream))
@@ -132,13 +187,20 @@ def hadamard_quant_nvfp4(x, hblock, codes, sf, tensor_scale, ws, tensor_scale_in
 def hadamard_quant_int8(x, hblock, q, row_scale, stream=None):
     """q: int8 codes, or the same integers in a bf16 tensor (operands of the bf16-pipe GEMM)."""
     rows, k = x.shape
+    if q.numel() < rows * k:
+        raise DitError(f"q: {q.numel()} codes, the call writes {rows * k}")
+    _need(row_scale, 4 * rows, "row_scale")
+    _same_device(x, q, row_scale)
     st = lib().dit_hadamard_quant_int8(_p(x), _dt(x), rows, k, hblock, _p(q), _dt(q), _p(row_scale),
                                        _stream(stream))
     _check(st, "dit_hadamard_quant_int8")
 
 
 def qgemm_nvfp4(a, a_sf, a_gs, b, b_sf, b_gs, y, ws, bias=None, act=ACT_NONE, stream=None):
-    m, n, k = a.shape[0], b.shape[0], a.shape[1] * 2
+    m, n, k = _nvfp4_gemm_args(a, a_sf, a_gs, b, b_sf, b_gs, bias)
+    if y.numel() < m * n:
+        raise DitError(f"y: {y.numel()} elements, the call writes {m * n}")
+    _same_device(a, a_sf, a_gs, b, b_sf, b_gs, bias, y, ws)
     st = lib().dit_qgemm_nvfp4(_p(a), _p(a_sf), _p(a_gs), _p(b), _p(b_sf), _p(b_gs), m, n, k,
                                _p(bias), act, _p(y), _dt(y), _p(ws), ws.numel(), _stream(stream))
     _check(st, "dit_qgemm_nvfp4")
@@ -149,7 +211,13 @@ def qgemm_nvfp4_fused_quant(a, a_sf, a_gs, b, b_sf, b_gs, ws, hblock, q_scale_in
     """NVFP4 GEMM whose epilogue also NVFP4-quantises the block-Hadamard transform of its bf16
     output with the supplied tensor scale q_scale_in (device float [1]) into q_codes / q_sf,
     and writes the output's own tensor scale to q_scale_next; y (bf16) is optional."""
-    m, n, k = a.shape[0], b.shape[0], a.shape[1] * 2
+    m, n, k = _nvfp4_gemm_args(a, a_sf, a_gs, b, b_sf, b_gs, bias)
+    _need(y, 2 * m * n, "y")
+    _need(q_codes, m * n // 2, "q_codes")
+    _need(q_sf, sf_bytes(m, n), "q_sf")
+    _need(q_scale_in, 4, "q_scale_in")
+    _need(q_scale_next, 4, "q_scale_next")
+    _same_device(a, a_sf, a_gs, b, b_sf, b_gs, bias, y, q_scale_in, q_codes, q_sf, q_scale_next, ws)
     st = lib().dit_qgemm_nvfp4_fused_quant(_p(a), _p(a_sf), _p(a_gs), _p(b), _p(b_sf), _p(b_gs), m, n, k, _p(bias),
                                            act, _p(y), hblock, _p(q_scale_in), _p(q_codes), _p(q_sf),
                                            _p(q_scale_next), _p(ws), ws.numel(), _stream(stream))
@@ -160,7 +228,10 @@ def qgemm_nvfp4_amax(a, a_sf, a_gs, b, b_sf, b_gs, y, ws, hblock, tensor_scale_o
                      stream=None):
     """NVFP4 GEMM into bf16 y whose epilogue also writes y's NVFP4 tensor scale (the one
     hadamard_quant_nvfp4(y, hblock, ...) would derive) to tensor_scale_out (device float [1])."""
-    m, n, k = a.shape[0], b.shape[0], a.shape[1] * 2
+    m, n, k = _nvfp4_gemm_args(a, a_sf, a_gs, b, b_sf, b_gs, bias)
+    _need(y, 2 * m * n, "y")
+    _need(tensor_scale_out, 4, "tensor_scale_out")
+    _same_device(a, a_sf, a_gs, b, b_sf, b_gs, bias, y, tensor_scale_out, ws)
     st = lib().dit_qgemm_nvfp4_amax(_p(a), _p(a_sf), _p(a_gs), _p(b), _p(b_sf), _p(b_gs), m, n, k, _p(bias), act,
                                     _p(y), hblock, _p(tensor_scale_out), _p(ws), ws.numel(), _stream(stream))
     _check(st, "dit_qgemm_nvfp4_amax")
@@ -170,7 +241,16 @@ def qgemm_int8(a, a_scale, b, b_scale, y, ws, bias=None, acc_debug=None, act=ACT
     """a, b: int8 codes (IMMA path) or bf16-held integer codes (tcgen05 bf16 path)."""
     if a.dtype != b.dtype:
         raise DitError("qgemm_int8: a and b must use the same code container")
+    if a.dim() != 2 or b.dim() != 2 or b.shape[1] != a.shape[1]:
+        raise DitError("qgemm_int8: a [m, k] and b [n, k] codes with the same k")
     m, n, k = a.shape[0], b.shape[0], a.shape[1]
+    _need(a_scale, 4 * m, "a_scale")
+    _need(b_scale, 4 * n, "b_scale")
+    _bias_ok(bias, n)
+    if y.numel() < m * n:
+        raise DitError(f"y: {y.numel()} elements, the call writes {m * n}")
+    _need(acc_debug, 4 * m * n, "acc_debug")
+    _same_device(a, a_scale, b, b_scale, bias, y, acc_debug, ws)
     st = lib().dit_qgemm_int8(_p(a), _p(a_scale), _p(b), _p(b_scale), _dt(a), m, n, k, _p(bias), act,
                               _p(y), _dt(y), _p(acc_debug), _p(ws), ws.numel(), _stream(stream))
     _check(st, "dit_qgemm_int8")
@@ -178,6 +258,12 @@ def qgemm_int8(a, a_scale, b, b_scale, y, ws, bias=None, acc_debug=None, act=ACT
 
 def tdc_step(mode, x_in, ws, x_out=None, x_out_skip=None, d1=None, d_new=None, gamma=None,
              sim=None, stream=None):
+    for name, t in (("x_out", x_out), ("x_out_skip", x_out_skip), ("d1", d1), ("d_new", d_new)):
+        if t is not None and (t.dtype != x_in.dtype or t.numel() != x_in.numel()):
+            raise DitError(f"tdc_step: {name} must have x_in's dtype and size")
+    _need(gamma, 4, "gamma")
+    _need(sim, 4, "sim")
+    _same_device(x_in, x_out, x_out_skip, d1, d_new, gamma, sim, ws)
     st = lib().dit_tdc_step(mode, _p(x_in), _p(x_out), _p(x_out_skip), _p(d1), _p(d_new),
                             _dt(x_in), x_in.numel(), _p(gamma), _p(sim), _p(ws), ws.numel(),
                             _stream(stream))
@@ -250,6 +336,9 @@ def alloc_int8(rows: int, k: int, device="cuda", container: str = "bf16") -> dic
 
 def outlier_ratio(x, ws, ratio, count=None, k_sigma: float = 6.0, stream=None):
     """ratio (device float [1]) = fraction of |x| > k_sigma * RMS(x); count (device int64 [1])."""
+    _need(ratio, 4, "ratio")
+    _need(count, 8, "count")
+    _same_device(x, ratio, count, ws)
     st = lib().dit_outlier_ratio(_p(x), _dt(x), x.numel(), float(k_sigma), _p(ratio), _p(count), _p(ws),
                                  ws.numel(), _stream(stream))
     _check(st, "dit_outlier_ratio")
@@ -259,6 +348,12 @@ def gemm_bf16(x, w, y, ws, bias=None, act=ACT_NONE, stream=None):
     """The BF16 route: y = act(x w^T (+ bias)) on untransformed bf16 operands."""
     m, k = x.shape
     n = w.shape[0]
+    if w.dim() != 2 or w.shape[1] != k:
+        raise DitError("gemm_bf16: x [m, k] and w [n, k] with the same k")
+    _bias_ok(bias, n)
+    if y.numel() < m * n:
+        raise DitError(f"y: {y.numel()} elements, the call writes {m * n}")
+    _same_device(x, w, bias, y, ws)
     st = lib().dit_gemm_bf16(_p(x), _p(w), m, n, k, _p(bias), act, _p(y), _dt(y), _p(ws), ws.numel(),
                              _stream(stream))
     _check(st, "dit_gemm_bf16")
@@ -267,6 +362,12 @@ def gemm_bf16(x, w, y, ws, bias=None, act=ACT_NONE, stream=None):
 def nvfp4_to_int8(codes, sf, tensor_scale, q, row_scale, stream=None):
     """Per-output-channel INT8 (int8 or bf16-held codes in q) of NVFP4 weights [rows x K]."""
     rows, k = codes.shape[0], codes.shape[1] * 2
+    _need(sf, sf_bytes(rows, k), "sf")
+    _need(tensor_scale, 4, "tensor_scale")
+    if q.numel() < rows * k:
+        raise DitError(f"q: {q.numel()} codes, the call writes {rows * k}")
+    _need(row_scale, 4 * rows, "row_scale")
+    _same_device(codes, sf, tensor_scale, q, row_scale)
     st = lib().dit_nvfp4_to_int8(_p(codes), _p(sf), _p(tensor_scale), rows, k, _p(q), _dt(q), _p(row_scale),
                                  _stream(stream))
     _check(st, "dit_nvfp4_to_int8")
