@@ -41,27 +41,46 @@ LINEARS = [("qkv", HIDDEN, 3 * HIDDEN), ("out", HIDDEN, HIDDEN), ("ffn_up", HIDD
            ("ffn_down", FFN, HIDDEN)]
 
 
+# The sources each kernel type is built from (its own file, the shared device helpers and the
+# host-side launch glue); a measured DRAM figure stands while these are unchanged.
+KERNEL_SOURCES = {
+    "gemm_int8": ["gemm_int8_tc.cu", "gemm_int8.cu"],
+    "gemm_nvfp4": ["gemm_nvfp4.cu"],
+    "quant_int8": ["quant.cu"],
+    "quant_nvfp4": ["quant.cu"],
+    "tdc_commit": ["reduce.cu"],
+}
+SHARED_SOURCES = ["common.cuh", "api.cu"]
+
+
+def kernel_sources_hash(kind: str) -> str:
+    """sha256 over the kernel type's source files and the shared ones, names and bytes."""
+    import hashlib
+    csrc = os.path.join(ROOT, "int8_mixed_precision_gb300", "csrc")
+    files = [os.path.join(csrc, f) for f in sorted(KERNEL_SOURCES[kind] + SHARED_SOURCES)]
+    files.append(os.path.join(ROOT, "include", "dit6.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def measured_traffic(kind: str):
     """DRAM bytes per launch of a kernel type from the committed ncu summary of this workload,
-    or None when the kernel sources have changed since that capture (their hash differs)."""
-    import glob
-    import hashlib
+    or None when that kernel type's sources have changed since the capture (their hash, listed
+    per kernel type in the summary, differs)."""
     import re
     path = os.path.join(ROOT, "profiles", "dram_traffic_cogvideox2b_step.md")
     try:
         text = open(path).read()
     except OSError:
         return None
-    csrc = os.path.join(ROOT, "int8_mixed_precision_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh")) +
-                   [os.path.join(ROOT, "include", "dit6.h")])
-    h = hashlib.sha256()
-    for f in files:
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
-    m = re.search(r"sources sha256: ([0-9a-f]{64})", text)
-    if not m or m.group(1) != h.hexdigest():
+    if kind not in KERNEL_SOURCES:
+        return None
+    m = re.search(r"^\| " + re.escape(kind) + r" sources \| ([0-9a-f]{64}) \|", text, re.M)
+    if not m or m.group(1) != kernel_sources_hash(kind):
         return None
     row = re.search(r"^\| " + re.escape(kind) + r" \| \d+ \| [\d.]+ \| [\d.]+ \| (\d+) \|", text, re.M)
     return int(row.group(1)) if row else None

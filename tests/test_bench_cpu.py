@@ -34,3 +34,23 @@ def test_clock_samples_fall_back_to_all_when_none_inside():
     s = c.summary()
     assert s["samples"] == 2 and not s["in_timed_region"]
     assert s["reasons"] == ["sw_thermal_slowdown"]
+
+
+def test_measured_traffic_follows_each_kernels_sources(tmp_path, monkeypatch):
+    """The committed DRAM figure of a kernel type is reported while that type's sources hash to
+    the listed value, and withdrawn once one of them changes; another type's edit leaves it."""
+    import shutil
+    root = tmp_path / "repo"
+    for d in ("profiles", "include", os.path.join("int8_mixed_precision_gb300", "csrc")):
+        shutil.copytree(os.path.join(bench.ROOT, d), root / d)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    before = {k: bench.measured_traffic(k) for k in bench.KERNEL_SOURCES}
+    assert all(v and v > 0 for v in before.values())
+    with open(root / "int8_mixed_precision_gb300" / "csrc" / "gemm_nvfp4.cu", "a") as f:
+        f.write("\n// edited\n")
+    assert bench.measured_traffic("gemm_nvfp4") is None
+    assert bench.measured_traffic("gemm_int8") == before["gemm_int8"]
+    with open(root / "int8_mixed_precision_gb300" / "csrc" / "common.cuh", "a") as f:
+        f.write("\n// edited\n")
+    assert all(bench.measured_traffic(k) is None for k in bench.KERNEL_SOURCES)
+    assert bench.measured_traffic("no_such_kernel") is None
