@@ -21,8 +21,8 @@ tdc      Temporal Delta Cache (commit / skip / decision) and Purified Delta Refr
 Parity status
 -------------
 Every function here is pinned by a ``-m "not gpu"`` test against something other than
-itself (closed forms, library routines, brute force, hand-worked fixtures) except:
-
-* the pages' own alpha, beta and tau values (not printed on the pages): parity unpinned;
-* the PDR "outlier ratio" BF16 override (undefined on the pages): not implemented.
-"""
+itself (closed forms, library routines, brute force, hand-worked fixtures under
+``tests/golden/``), including the rounding-boundary margins that decide which elements the
+GPU parity tests exempt (``tests/test_oracle_margins.py``).  Parity unpinned: the pages' own
+alpha, beta and tau values and their definition of the PDR "outlier ratio" (neither is
+printed on the pages); the oracle uses the readings listed in the design notes.
