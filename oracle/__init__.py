@@ -26,3 +26,4 @@ itself (closed forms, library routines, brute force, hand-worked fixtures under
 GPU parity tests exempt (``tests/test_oracle_margins.py``).  Parity unpinned: the pages' own
 alpha, beta and tau values and their definition of the PDR "outlier ratio" (neither is
 printed on the pages); the oracle uses the readings listed in the design notes.
+"""
