@@ -23,8 +23,10 @@
  *   run concurrently on the GPU must not share one workspace.
  * - Tensors are row-major and contiguous.  Activation and delta tensors are bf16 or fp32
  *   (dit_dtype).  Device pointers must be 32-byte aligned (256-bit vector loads).
- * - All entry points are thread-compatible (no global mutable state except a cached
- *   driver entry point).
+ * - All entry points are thread-compatible.  The library's only global mutable state is a
+ *   cached driver entry point, per-device caches of the SM count, and the fixed scratch
+ *   array of dit_gamma_route_noalloc (with its per-device address cache); calls of that entry
+ *   point share the array and race when they overlap on the GPU (see its comment).
  */
 #ifndef DIT6_H_
 #define DIT6_H_
@@ -111,10 +113,12 @@ dit_status dit_gamma_route(const void* x_in, const void* x_out, dit_dtype dt, in
  *
  * The first call on a device sets the scratch up (looks up its device address with
  * cudaGetSymbolAddress and zero-fills it once, synchronously, with that device current);
- * make that first call before any stream capture.  Every call then clears the status word
- * and counter asynchronously on `stream`.  All calls share the one array and it keeps the
- * last call's contents: calls whose kernels overlap on the GPU (different streams, no
- * ordering between them) race on it and give wrong results.
+ * make that first call before any stream capture.  The address is cached per device for
+ * the life of the process: do not use this entry point across a cudaDeviceReset (the
+ * module, and with it the array, may come back at another address).  Every call clears the
+ * status word and counter asynchronously on `stream`.  All calls share the one array and it
+ * keeps the last call's contents: calls whose kernels overlap on the GPU (different streams,
+ * no ordering between them) race on it and give wrong results.
  * ------------------------------------------------------------------------------------ */
 dit_status dit_gamma_route_noalloc(const void* x_in, const void* x_out, dit_dtype dt,
                                    int64_t n, const float* alpha, const float* beta,
@@ -197,28 +201,6 @@ dit_status dit_qgemm_nvfp4(const uint8_t* a, const uint8_t* a_sf, const float* a
                            int64_t m, int64_t n, int64_t k, const float* bias, dit_act act,
                            void* y, dit_dtype y_dt, void* ws, size_t ws_bytes,
                            dit_stream_t stream);
-
-/* ------------------------------------------------------------------------------------
- * NVFP4 GEMM with fused epilogue quantisation for the next NVFP4 layer (FFN up -> down).
- * [EN] 2.A Mechanism 2-3 (online block Hadamard before quantisation), applied to the
- * activation the GEMM produces instead of in a separate pass.
- *
- * Z = act(dit_qgemm_nvfp4 product (+ bias)) rounded to bf16 (the values y would hold);
- * q_codes / q_sf = the NVFP4 encoding of the block Hadamard transform of Z (blocks of
- * hblock along n) with the CALLER-SUPPLIED tensor scale *q_scale_in: byte for byte what
- * dit_hadamard_quant_nvfp4(Z, hblock, ..., tensor_scale_in = q_scale_in) writes, layouts
- * included, so they feed dit_qgemm_nvfp4 as its A operand with a_gs = q_scale_in.
- * *q_scale_next = max|H Z| / (6 * 448): the tensor scale the unfused quantiser would derive
- * from this Z (for the next call; a supplied scale below it saturates the largest values).
- * y : device bf16 [m x n] or NULL (Z not stored).  hblock in {16, 32, 64}; n % 64 == 0;
- * k % 64 == 0; q_codes [m x n/2] and q_sf (dit_sf_bytes(m, n)) device, 32-byte aligned.
- * ------------------------------------------------------------------------------------ */
-dit_status dit_qgemm_nvfp4_fused_quant(const uint8_t* a, const uint8_t* a_sf, const float* a_gs,
-                                       const uint8_t* b, const uint8_t* b_sf, const float* b_gs,
-                                       int64_t m, int64_t n, int64_t k, const float* bias,
-                                       dit_act act, void* y, int hblock, const float* q_scale_in,
-                                       uint8_t* q_codes, uint8_t* q_sf, float* q_scale_next,
-                                       void* ws, size_t ws_bytes, dit_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * NVFP4 GEMM whose epilogue also produces the tensor scale of its own output for the next
@@ -328,6 +310,47 @@ void dit_route_host(const dit_tdc_state* st, const float* alpha, const float* be
 void dit_route_host_pdr(const dit_tdc_state* st, const float* alpha, const float* beta,
                         const float* thr, int n_layers, double outlier_ratio, double rho,
                         int32_t* routes);
+
+/* ------------------------------------------------------------------------------------
+ * Token-sharded form (one block's tokens split across GPUs, one rank per GPU).
+ * The reductions of [EN] 2.A Mechanism 1 (Gamma), 2.B (the delta similarity) and of the NVFP4
+ * tensor scale ([IT] "Contributi Chiave" 4; one fp32 scale over the whole tensor) span all
+ * tokens, so a rank computes its shard's partials, the ranks all-reduce them (sum for the L1
+ * sums, max for the amax), and the finishing call applies the unsharded arithmetic.  Every
+ * other step of the path (quantisation with the finished tensor scale, the GEMMs against
+ * replicated weights, the delta-cache skip) works on a shard alone.  The library performs no
+ * collective itself: the caller all-reduces with its own communicator.
+ *
+ * dit_l1_partials (device): mode DIT_L1_GAMMA -> partials_dev[0..1] = sum|x_out - x_in|,
+ *   sum|x_in| over this shard's n elements; mode DIT_L1_TDC_COMMIT -> also writes
+ *   d_new = store(x_out - x_in) as dit_tdc_step COMMIT does and partials_dev[0..3] =
+ *   sum|x_out - x_in|, sum|x_in|, sum|d_new - d1|, sum|d1| (the last two 0 when d1 is NULL).
+ *   Fixed-order fp64 sums (bit-reproducible for a given shard).  partials_dev: device
+ *   double[2] or [4], 8-byte aligned.
+ * dit_nvfp4_amax (device): *amax_dev = max|block Hadamard (x)| over this shard [rows x k]
+ *   (arguments as dit_hadamard_quant_nvfp4).
+ * dit_shard_finish (device) / dit_shard_finish_host (host pointers, synchronous): from the
+ *   all-reduced partials, Gamma = p[0] / p[1] and sim = p[2] / p[3] (n_partials = 4) in fp64
+ *   with the 0/0 -> 0, x/0 -> +inf rule, routes as dit_gamma_route; from the all-reduced
+ *   amax, tensor_scale = amax / 2688 (one fp32 division, the value the unsharded quantiser
+ *   derives).  Any output may be NULL; partials may be NULL when only the tensor scale is
+ *   wanted, amax (with tensor_scale) when only the ratios are.
+ * ------------------------------------------------------------------------------------ */
+typedef enum { DIT_L1_GAMMA = 0, DIT_L1_TDC_COMMIT = 1 } dit_l1_mode;
+
+dit_status dit_l1_partials(int mode, const void* x_in, const void* x_out, const void* d1, void* d_new,
+                           dit_dtype dt, int64_t n, double* partials_dev, void* ws, size_t ws_bytes,
+                           dit_stream_t stream);
+dit_status dit_nvfp4_amax(const void* x, dit_dtype dt, int64_t rows, int64_t k, int hblock,
+                          float* amax_dev, void* ws, size_t ws_bytes, dit_stream_t stream);
+dit_status dit_shard_finish(const double* partials_dev, int n_partials, const float* amax_dev,
+                            const float* alpha, const float* beta, const float* thr, int n_layers,
+                            float* gamma_dev, float* sim_dev, int32_t* routes_dev,
+                            float* tensor_scale_dev, dit_stream_t stream);
+dit_status dit_shard_finish_host(const double* partials, int n_partials, const float* amax,
+                                 const float* alpha, const float* beta, const float* thr,
+                                 int n_layers, float* gamma, float* sim, int32_t* routes,
+                                 float* tensor_scale);
 
 /* ------------------------------------------------------------------------------------
  * Block-scale tile layout helpers (host).  The scales of a [rows x k] NVFP4 tensor are

@@ -206,24 +206,6 @@ def qgemm_nvfp4(a, a_sf, a_gs, b, b_sf, b_gs, y, ws, bias=None, act=ACT_NONE, st
     _check(st, "dit_qgemm_nvfp4")
 
 
-def qgemm_nvfp4_fused_quant(a, a_sf, a_gs, b, b_sf, b_gs, ws, hblock, q_scale_in, q_codes, q_sf, q_scale_next,
-                            y=None, bias=None, act=ACT_NONE, stream=None):
-    """NVFP4 GEMM whose epilogue also NVFP4-quantises the block-Hadamard transform of its bf16
-    output with the supplied tensor scale q_scale_in (device float [1]) into q_codes / q_sf,
-    and writes the output's own tensor scale to q_scale_next; y (bf16) is optional."""
-    m, n, k = _nvfp4_gemm_args(a, a_sf, a_gs, b, b_sf, b_gs, bias)
-    _need(y, 2 * m * n, "y")
-    _need(q_codes, m * n // 2, "q_codes")
-    _need(q_sf, sf_bytes(m, n), "q_sf")
-    _need(q_scale_in, 4, "q_scale_in")
-    _need(q_scale_next, 4, "q_scale_next")
-    _same_device(a, a_sf, a_gs, b, b_sf, b_gs, bias, y, q_scale_in, q_codes, q_sf, q_scale_next, ws)
-    st = lib().dit_qgemm_nvfp4_fused_quant(_p(a), _p(a_sf), _p(a_gs), _p(b), _p(b_sf), _p(b_gs), m, n, k, _p(bias),
-                                           act, _p(y), hblock, _p(q_scale_in), _p(q_codes), _p(q_sf),
-                                           _p(q_scale_next), _p(ws), ws.numel(), _stream(stream))
-    _check(st, "dit_qgemm_nvfp4_fused_quant")
-
-
 def qgemm_nvfp4_amax(a, a_sf, a_gs, b, b_sf, b_gs, y, ws, hblock, tensor_scale_out, bias=None, act=ACT_NONE,
                      stream=None):
     """NVFP4 GEMM into bf16 y whose epilogue also writes y's NVFP4 tensor scale (the one
@@ -268,6 +250,76 @@ def tdc_step(mode, x_in, ws, x_out=None, x_out_skip=None, d1=None, d_new=None, g
                             _dt(x_in), x_in.numel(), _p(gamma), _p(sim), _p(ws), ws.numel(),
                             _stream(stream))
     _check(st, "dit_tdc_step")
+
+
+# ----------------------------------------------------------------------------------------
+# token-sharded form: per-shard partials, all-reduced by the caller, then finished
+# ----------------------------------------------------------------------------------------
+
+L1_GAMMA = 0
+L1_TDC_COMMIT = 1
+
+
+def l1_partials(mode, x_in, x_out, partials, ws, d1=None, d_new=None, stream=None):
+    """This shard's L1 sums into partials (device float64): [sum|x_out - x_in|, sum|x_in|] for
+    L1_GAMMA; for L1_TDC_COMMIT also d_new = x_out - x_in (stored) and [sum|d_new - d1|,
+    sum|d1|] (zeros without d1)."""
+    for name, t in (("x_out", x_out), ("d1", d1), ("d_new", d_new)):
+        if t is not None and (t.dtype != x_in.dtype or t.numel() != x_in.numel()):
+            raise DitError(f"l1_partials: {name} must have x_in's dtype and size")
+    if partials.dtype != _torch().float64:
+        raise DitError("l1_partials: partials must be float64")
+    _need(partials, 8 * (4 if mode == L1_TDC_COMMIT else 2), "partials")
+    _same_device(x_in, x_out, d1, d_new, partials, ws)
+    st = lib().dit_l1_partials(mode, _p(x_in), _p(x_out), _p(d1), _p(d_new), _dt(x_in), x_in.numel(),
+                               _p(partials), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dit_l1_partials")
+
+
+def nvfp4_amax(x, hblock, amax, ws, stream=None):
+    """max|block Hadamard (x)| over this shard [rows x k] into amax (device float32 [1])."""
+    rows, k = x.shape
+    _need(amax, 4, "amax")
+    _same_device(x, amax, ws)
+    st = lib().dit_nvfp4_amax(_p(x), _dt(x), rows, k, hblock, _p(amax), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dit_nvfp4_amax")
+
+
+def shard_finish(partials=None, amax=None, alpha=(), beta=(), thr=(), gamma=None, sim=None, routes=None,
+                 tensor_scale=None, stream=None):
+    """From all-reduced partials / amax (device): Gamma, the delta similarity, the routes and the
+    NVFP4 tensor scale, with the arithmetic of the unsharded calls (device outputs)."""
+    n = len(alpha)
+    arr = ctypes.c_float * max(n, 1)
+    npart = 0 if partials is None else (4 if partials.numel() >= 4 else 2)
+    _same_device(partials, amax, gamma, sim, routes, tensor_scale)
+    st = lib().dit_shard_finish(_p(partials), npart, _p(amax), arr(*alpha), arr(*beta), arr(*thr), n, _p(gamma),
+                                _p(sim), _p(routes), _p(tensor_scale), _stream(stream))
+    _check(st, "dit_shard_finish")
+
+
+def shard_finish_host(partials=None, amax=None, alpha=(), beta=(), thr=()) -> dict:
+    """The finishing arithmetic on host values (a list of 2 or 4 sums, a float amax)."""
+    n = len(alpha)
+    arr = ctypes.c_float * max(n, 1)
+    p = None if partials is None else (ctypes.c_double * len(partials))(*[float(v) for v in partials])
+    npart = 0 if partials is None else len(partials)
+    am = None if amax is None else ctypes.byref(ctypes.c_float(float(amax)))
+    g, sm, ts = ctypes.c_float(), ctypes.c_float(), ctypes.c_float()
+    rt = (ctypes.c_int32 * max(n, 1))()
+    st = lib().dit_shard_finish_host(p, npart, am, arr(*alpha), arr(*beta), arr(*thr), n,
+                                     ctypes.byref(g) if p else None, ctypes.byref(sm) if npart == 4 else None,
+                                     rt if (p and n) else None, ctypes.byref(ts) if am else None)
+    _check(st, "dit_shard_finish_host")
+    out = {}
+    if p:
+        out["gamma"] = g.value
+        out["routes"] = list(rt)[:n]
+        if npart == 4:
+            out["sim"] = sm.value
+    if am:
+        out["tensor_scale"] = ts.value
+    return out
 
 
 # ----------------------------------------------------------------------------------------
@@ -418,15 +470,21 @@ class RoutedLinear:
     """Y = quant(X H) quant(W H)^T along a route chosen per call; the activation buffers for
     both routes are allocated once for a maximum token count."""
 
-    def __init__(self, weight: QuantizedWeight, max_tokens: int, ws, device="cuda", int8_scratch=None):
+    def __init__(self, weight: QuantizedWeight, max_tokens: int, ws, device="cuda", int8_scratch=None,
+                 act_buffers=None):
         """int8_scratch: for NVFP4-only weights, a buffer (alloc_int8 of at least N rows x K)
         the INT8 weights are derived into on each INT8-routed call; several layers may share
-        one.  Allocated here when not given."""
+        one.  Allocated here when not given.  act_buffers: (alloc_nvfp4, alloc_int8) buffers of
+        at least max_tokens x K for the quantised activations, shared by layers whose calls are
+        ordered on one stream; allocated here when not given."""
         self.w = weight
         self.ws = ws
-        self.a4 = alloc_nvfp4(max_tokens, weight.k, device)
         container = weight.int8_container
-        self.a8 = alloc_int8(max_tokens, weight.k, device, container)
+        if act_buffers is not None:
+            self.a4, self.a8 = act_buffers
+        else:
+            self.a4 = alloc_nvfp4(max_tokens, weight.k, device)
+            self.a8 = alloc_int8(max_tokens, weight.k, device, container)
         self.w8_scratch = None
         if weight.int8 is None:
             self.w8_scratch = int8_scratch if int8_scratch is not None else alloc_int8(weight.n, weight.k, device,

@@ -33,8 +33,6 @@ SIGNATURES = {
                                 _vp]),
     "dit_qgemm_nvfp4_amax": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp,
                                      _sz, _vp]),
-    "dit_qgemm_nvfp4_fused_quant": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32,
-                                            _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "dit_nvfp4_to_int8": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp, _i32, _vp, _vp]),
     "dit_qgemm_int8": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp, _sz,
                                _vp]),
@@ -47,6 +45,11 @@ SIGNATURES = {
                                   ctypes.POINTER(ctypes.c_int32)]),
     "dit_outlier_ratio": (_i32, [_vp, _i32, _i64, ctypes.c_float, _vp, _vp, _vp, _sz, _vp]),
     "dit_gemm_bf16": (_i32, [_vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _sz, _vp]),
+    "dit_l1_partials": (_i32, [_i32, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _sz, _vp]),
+    "dit_nvfp4_amax": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _sz, _vp]),
+    "dit_shard_finish": (_i32, [_vp, _i32, _vp, _f, _f, _f, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "dit_shard_finish_host": (_i32, [ctypes.POINTER(ctypes.c_double), _i32, _f, _f, _f, _f, _i32, _f, _f,
+                                     ctypes.POINTER(ctypes.c_int32), _f]),
     "dit_sf_index": (_i64, [_i64, _i64, _i64, _i64]),
     "dit_sf_bytes": (_sz, [_i64, _i64]),
 }

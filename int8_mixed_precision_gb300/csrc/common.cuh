@@ -20,15 +20,8 @@ constexpr size_t WS_AMAX = 8;        // uint32: float bits of a running amax (re
 constexpr size_t WS_SG = 12;         // float : tensor scale produced by the amax pass
 constexpr size_t WS_THR = 16;        // double: outlier threshold k * RMS from the first pass
 constexpr size_t WS_PARTIALS = 256;  // double[MAX_RED_CTAS][4]
-constexpr int MAX_RED_CTAS = 1024;
-// split-K tail of the INT8 GEMM: one uint32 arrival ticket per (split tile, epilogue warp),
-// reset by the last arrival, and the int32 partial accumulators of every split part
-constexpr size_t WS_SPLIT_TICKETS = 40960;   // uint32[WS_SPLIT_MAX_TICKETS]
-constexpr int WS_SPLIT_MAX_TICKETS = 4096;   // ends at 57344
-constexpr size_t WS_SPLIT_PARTIALS = 65536;  // int32 [slots][128 x 256]
-constexpr size_t WS_SPLIT_SLOT_BYTES = 128 * 256 * 4;
-constexpr int WS_SPLIT_SLOTS = 192;
-constexpr size_t WS_BYTES = WS_SPLIT_PARTIALS + WS_SPLIT_SLOTS * WS_SPLIT_SLOT_BYTES;  // 24.06 MiB
+constexpr int MAX_RED_CTAS = 1024;   // ends at 33024
+constexpr size_t WS_BYTES = 64 * 1024;
 
 // Device-side bounded waits give up after this many nanoseconds of %globaltimer.
 constexpr uint64_t WAIT_LIMIT_NS = 1000ull * 1000ull * 1000ull;  // 1 s

@@ -10,32 +10,19 @@
 // the additions.  Each finished chunk is drained from tensor memory, converted to int32
 // (exact) and added to int32 running sums in the epilogue warps' registers.
 //
-// Persistent CTAs (one per SM) walk output tiles of 128 x BN.  Warp 0: TMA producer (128-byte
-// swizzled A/B tiles, STAGES-deep ring).  Warp 1: tensor-memory allocation and the MMA issuer;
-// chunk accumulators alternate between two tensor-memory buffers, so the MMAs of chunk c+1
-// (also of the next tile) overlap the drain of chunk c.  Warps 2..: epilogue, two warps per
-// tensor-memory lane quarter when BN > 128.  Every wait is bounded.
+// Persistent CTA pairs (2-CTA clusters, cta_group::2) walk 256 x 256 output tiles.  Warp 0:
+// TMA producer (128-byte swizzled A/B tiles, STAGES-deep ring).  Warp 1: tensor-memory
+// allocation and, in the even CTA, the MMA issuer; chunk accumulators alternate between two
+// tensor-memory buffers, so the MMAs of chunk c+1 (also of the next tile) overlap the drain of
+// chunk c.  Warps 2..9: epilogue.  Every wait is bounded.
 #include "common.cuh"
 
 namespace dit6 {
 namespace i8tc {
 
-constexpr int BM = 128, BK = 64;  // BK bf16 elements = 128 bytes per row
+constexpr int BK = 64;             // BK bf16 elements = 128 bytes per row
 constexpr int KCHUNK_BLOCKS = 16;  // 16 x 64 = 1024 elements per exact chunk
-constexpr int A_BYTES = BM * BK * 2;
-
-template <int BN>
-struct Cfg {
-  static constexpr int STAGES = BN == 128 ? 3 : (BN == 192 ? 5 : 4);
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int EPI_WARPS = BN <= 128 ? 4 : 8;         // 4 lane quarters x (1 or 2)
-  static constexpr int CW = BN / (EPI_WARPS / 4);             // columns per epilogue thread
-  static constexpr int THREADS = (2 + EPI_WARPS) * 32;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-  static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
-  static_assert(CW % 16 == 0 && CW <= 128, "epilogue split");
-};
+constexpr int A_BYTES = 128 * BK * 2;
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   uint64_t d = 0;
@@ -52,26 +39,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
 }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
@@ -85,408 +52,18 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// TMA load of a box multicast into the same shared-memory offset of every CTA in `mask`
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
-                                               int32_t c1, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
-      "[%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
-      : "memory");
-}
-// MMA completion arrives on the barrier at the same offset in every CTA of `mask`
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(mask)
-               : "memory");
-}
-
-// MC = 1: independent CTAs.  MC = 2: clusters of two CTAs on adjacent 128-row M blocks and the
-// same N block; each loads half of the shared B tile and multicasts it to both, halving the
-// B traffic from L2; a stage is refilled only after both CTAs' MMAs have consumed it.
-// GELU selects the epilogue activation at compile time (erf GELU after the bias): the wide
-// accumulator drain already runs at the register cap, so the plain instantiation carries none
-// of the activation's code.
-// SPLIT selects the split-K tail instantiation (last partial wave split along K, see launch);
-// the whole-tile instantiation keeps its own loops, untouched by the split's bookkeeping,
-// because this kernel runs at the register cap and its speed follows the code layout.
-template <int BN, int MC, bool GELU, bool SPLIT>
-__global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
-    k_gemm_int8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N,
-                   int K, const float* __restrict__ bias, void* __restrict__ y, int epi,
-                   int32_t* __restrict__ acc_out, void* ws, int stall, int tail_base, int parts) {
-  using C = Cfg<BN>;
-  constexpr int S = C::STAGES;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
-  // bars: full[S], empty[S], chunk_full[2], chunk_empty[2], mma_done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const uint32_t sbase = smem_u32(smem);
-  auto full = [&](int s) { return smem_u32(bars + s); };
-  auto empty = [&](int s) { return smem_u32(bars + S + s); };
-  auto cfull = [&](int b) { return smem_u32(bars + 2 * S + b); };
-  auto cempty = [&](int b) { return smem_u32(bars + 2 * S + 2 + b); };
-  const uint32_t mma_done = smem_u32(bars + 2 * S + 4);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tiles_n = (N + BN - 1) / BN;
-  const int m_groups = ((M + BM - 1) / BM + MC - 1) / MC;     // groups of MC adjacent M blocks
-  const int n_tiles = m_groups * n_tiles_n;                    // work items (one per CTA group)
-  const int rank = MC > 1 ? (int)cluster_rank() : 0;
-  const int first_item = blockIdx.x / MC, item_step = gridDim.x / MC;
-  auto tile_m0 = [&](int item) { return ((item / n_tiles_n) * MC + rank) * BM; };
-  auto tile_n0 = [&](int item) { return (item % n_tiles_n) * BN; };
-  const int nkb = (K + BK - 1) / BK;
-  const int nchunks = (nkb + KCHUNK_BLOCKS - 1) / KCHUNK_BLOCKS;
-  // SPLIT work items: tiles [0, tail_base) whole; each tile from tail_base on split along K
-  // into `parts` items whose int32 partial sums the last part to finish adds (exactly)
-  const int n_items = tail_base + (n_tiles - tail_base) * parts;
-  struct Item {
-    int m0, n0, kb_lo, kb_hi, slot, part;  // part < 0: a whole tile
-  };
-  auto decode = [&](int item) {
-    Item it;
-    int tile = item;
-    it.slot = 0;
-    it.part = -1;
-    it.kb_lo = 0;
-    it.kb_hi = nkb;
-    if (item >= tail_base) {
-      const int j = item - tail_base;
-      it.slot = j / parts;
-      it.part = j % parts;
-      tile = tail_base + it.slot;
-      it.kb_lo = (int)((int64_t)it.part * nkb / parts);
-      it.kb_hi = (int)((int64_t)(it.part + 1) * nkb / parts);
-    }
-    it.m0 = tile_m0(tile);
-    it.n0 = tile_n0(tile);
-    return it;
-  };
-  constexpr uint16_t PEERS = MC > 1 ? (uint16_t)((1u << MC) - 1) : (uint16_t)1;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(empty(s), MC);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(cfull(b), 1);
-      mbar_init(cempty(b), C::EPI_WARPS);
-    }
-    mbar_init(mma_done, 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(C::TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    tc_fence_before();
-  }
-  __syncthreads();
-  if (MC > 1) cluster_sync();  // peers' barriers are initialised before any multicast
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {  // ------------------------------------------------------ TMA producer
-    if (lane == 0 && !stall) {  // stall: a test hook that issues no loads at all
-      prefetch_tmap(&tmA);
-      prefetch_tmap(&tmB);
-      uint32_t kc = 0;
-      bool ok = true;
-      if constexpr (!SPLIT) {
-        for (int item = first_item; item < n_tiles && ok; item += item_step) {
-          const int m0 = tile_m0(item), n0 = tile_n0(item);
-          for (int kb = 0; kb < nkb; ++kb, ++kc) {
-            const int s = kc % S;
-            if (!mbar_wait(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
-              ok = false;
-              break;
-            }
-            mbar_expect_tx(full(s), C::STAGE_BYTES);
-            tma_load_2d(sbase + s * C::STAGE_BYTES, &tmA, full(s), kb * BK, m0);
-            if (MC > 1)
-              tma_load_2d_mc(sbase + s * C::STAGE_BYTES + A_BYTES + rank * (C::B_BYTES / MC), &tmB, full(s), kb * BK,
-                             n0 + rank * (BN / MC), PEERS);
-            else
-              tma_load_2d(sbase + s * C::STAGE_BYTES + A_BYTES, &tmB, full(s), kb * BK, n0);
-          }
-        }
-      } else {
-        for (int item = first_item; item < n_items && ok; item += item_step) {
-          const Item it = decode(item);
-          const int m0 = it.m0, n0 = it.n0;
-          for (int kb = it.kb_lo; kb < it.kb_hi; ++kb, ++kc) {
-            const int s = kc % S;
-            if (!mbar_wait(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
-              ok = false;
-              break;
-            }
-            mbar_expect_tx(full(s), C::STAGE_BYTES);
-            tma_load_2d(sbase + s * C::STAGE_BYTES, &tmA, full(s), kb * BK, m0);
-            if (MC > 1)
-              tma_load_2d_mc(sbase + s * C::STAGE_BYTES + A_BYTES + rank * (C::B_BYTES / MC), &tmB, full(s), kb * BK,
-                             n0 + rank * (BN / MC), PEERS);
-            else
-              tma_load_2d(sbase + s * C::STAGE_BYTES + A_BYTES, &tmB, full(s), kb * BK, n0);
-          }
-        }
-      }
-      if (!ok) {  // let copies still in flight land before the CTA exits
-        volatile int no_abort = 0;
-        const uint32_t first = kc > (uint32_t)S ? kc - S : 0;
-        for (uint32_t c = first; c < kc; ++c) mbar_wait(full(c % S), (c / S) & 1, ws, &no_abort);
-      }
-    }
-  } else if (warp == 1) {  // --------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
-      uint32_t kc = 0, cc = 0;
-      bool ok = true;
-      for (int item = first_item; item < (SPLIT ? n_items : n_tiles) && ok; item += item_step) {
-        int kb_lo = 0, kb_hi = nkb, nch = nchunks;
-        if constexpr (SPLIT) {
-          const Item it = decode(item);
-          kb_lo = it.kb_lo;
-          kb_hi = it.kb_hi;
-          nch = (kb_hi - kb_lo + KCHUNK_BLOCKS - 1) / KCHUNK_BLOCKS;
-        }
-        for (int ch = 0; ch < nch && ok; ++ch, ++cc) {
-          const int buf = cc & 1;
-          if (!mbar_wait(cempty(buf), ((cc >> 1) & 1) ^ 1, ws, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d = tmem + buf * BN;
-          const int kb0 = kb_lo + ch * KCHUNK_BLOCKS;
-          const int kb1 = min(kb_hi, kb0 + KCHUNK_BLOCKS);
-          for (int kb = kb0; kb < kb1; ++kb, ++kc) {
-            const int s = kc % S;
-            if (!mbar_wait(full(s), (kc / S) & 1, ws, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a_s = sbase + s * C::STAGE_BYTES, b_s = a_s + A_BYTES;
-#pragma unroll
-            for (int j = 0; j < BK / 16; ++j)
-              tc_mma(d, desc_sw128(a_s + j * 32), desc_sw128(b_s + j * 32), idesc,
-                     (kb > kb0 || j > 0) ? 1u : 0u);
-            if (MC > 1)
-              tc_commit_mc(empty(s), PEERS);
-            else
-              tc_commit(empty(s));
-          }
-          if (ok) tc_commit(cfull(buf));
-        }
-      }
-      tc_commit(mma_done);
-      volatile int no_abort = 0;
-      mbar_wait(mma_done, 0, ws, &no_abort);  // every issued MMA has completed
-    }
-    __syncwarp();
-  } else {  // ------------------------------------------------------------- epilogue warps
-    const int e = warp - 2;
-    const int q = warp & 3;        // tensor-memory lane quarter of this warp
-    const int half = e >> 2;       // which CW-column part of the tile
-    uint32_t cc = 0;
-    bool ok = true;
-    for (int item = first_item; item < (SPLIT ? n_items : n_tiles) && (SPLIT || ok); item += item_step) {
-      int m0, n0, nch = nchunks;
-      Item it;
-      if constexpr (SPLIT) {
-        it = decode(item);
-        m0 = it.m0;
-        n0 = it.n0;
-        nch = (it.kb_hi - it.kb_lo + KCHUNK_BLOCKS - 1) / KCHUNK_BLOCKS;
-        if (!ok) {  // aborted: still arrive on split tickets so that every count returns to zero
-          if (it.part >= 0) {
-            __syncwarp();
-            uint32_t old = 0;
-            if (lane == 0) old = atomicAdd(ws_u32(ws, WS_SPLIT_TICKETS) + it.slot * C::EPI_WARPS + e, 1u);
-            old = __shfl_sync(0xffffffffu, old, 0);
-            if (lane == 0 && old == (uint32_t)(parts - 1)) ws_u32(ws, WS_SPLIT_TICKETS)[it.slot * C::EPI_WARPS + e] = 0;
-          }
-          continue;
-        }
-      } else {
-        m0 = tile_m0(item);
-        n0 = tile_n0(item);
-      }
-      constexpr int CW = C::CW;
-      int acc[CW];
-#pragma unroll
-      for (int i = 0; i < CW; ++i) acc[i] = 0;
-      for (int ch = 0; ch < nch; ++ch, ++cc) {
-        const int buf = cc & 1;
-        // SPLIT: a warp-uniform outcome, as the tickets below are warp-synchronous
-        const bool got = mbar_wait(cfull(buf), (cc >> 1) & 1, ws, abort_flag);
-        if (!(SPLIT ? __all_sync(0xffffffffu, got) : got)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + buf * BN + half * CW;
-#pragma unroll
-        for (int c = 0; c < CW / 16; ++c) {
-          uint32_t r[16];
-          tc_ld16(base + c * 16, r);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) acc[c * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cempty(buf));
-      }
-      if constexpr (SPLIT) {
-        if (it.part >= 0) {
-          // split part: publish this warp's 32 x CW int32 partial sums, then take a ticket;
-          // the last of the `parts` arrivals adds the others' sums (exact) and stores the
-          // tile.  Region layout [column group of 8][lane][8]: each warp-wide 256-bit access
-          // covers 1 KB of contiguous memory.
-          uint32_t* ticket = ws_u32(ws, WS_SPLIT_TICKETS) + it.slot * C::EPI_WARPS + e;
-          int32_t* partials = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(ws) + WS_SPLIT_PARTIALS);
-          auto region = [&](int part) {
-            return partials + ((size_t)(it.slot * parts + part) * C::EPI_WARPS + e) * 32 * CW + lane * 8;
-          };
-          if (ok) {
-            int32_t* mine = region(it.part);
-#pragma unroll
-            for (int c = 0; c < CW / 8; ++c) {
-              U8x32 o;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) o.w[i] = (uint32_t)acc[c * 8 + i];
-              st256(mine + c * 256, o);
-            }
-          }
-          __threadfence();
-          __syncwarp();
-          uint32_t old = 0;
-          if (lane == 0) old = atomicAdd(ticket, 1u);
-          old = __shfl_sync(0xffffffffu, old, 0);
-          if (old != (uint32_t)(parts - 1)) continue;  // another part finishes this region
-          if (lane == 0) *ticket = 0;
-          if (!ok) continue;
-          __threadfence();
-          for (int p = 0; p < parts; ++p) {
-            if (p == it.part) continue;
-            const int32_t* other = region(p);
-#pragma unroll
-            for (int c = 0; c < CW / 8; ++c) {
-              const int4 v0 = __ldcg(reinterpret_cast<const int4*>(other + c * 256));
-              const int4 v1 = __ldcg(reinterpret_cast<const int4*>(other + c * 256 + 4));
-              acc[8 * c] += v0.x;
-              acc[8 * c + 1] += v0.y;
-              acc[8 * c + 2] += v0.z;
-              acc[8 * c + 3] += v0.w;
-              acc[8 * c + 4] += v1.x;
-              acc[8 * c + 5] += v1.y;
-              acc[8 * c + 6] += v1.z;
-              acc[8 * c + 7] += v1.w;
-            }
-          }
-        }
-        if (!ok) continue;
-      } else {
-        if (!ok) break;
-      }
-      const int row = m0 + q * 32 + lane;
-      const int col0 = n0 + half * CW;
-      if (row < M && col0 < N) {
-        const float sa = a_scale[row];
-        const int64_t off = (int64_t)row * N + col0;
-#pragma unroll
-        for (int c = 0; c < CW / 16; ++c) {  // 16 columns per step
-          const int cb = col0 + c * 16;
-          if (cb >= N) break;
-          float v[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = cb + i < N ? cb + i : N - 1;
-            v[i] = __fmul_rn(__fmul_rn((float)acc[c * 16 + i], sa), b_scale[col]);
-            if (bias) v[i] = __fadd_rn(v[i], bias[col]);
-          }
-          if (GELU) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float2 g = gelu_erf2(make_float2(v[2 * i], v[2 * i + 1]));
-              v[2 * i] = g.x;
-              v[2 * i + 1] = g.y;
-            }
-          }
-          if (cb + 16 <= N && (N % 16) == 0) {
-            if (epi & EPI_BF16) {
-              uint32_t w[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) w[i] = f2_to_bf16x2(v[2 * i], v[2 * i + 1]);
-              U8x32 o;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) o.w[i] = w[i];
-              st256(reinterpret_cast<uint16_t*>(y) + off + c * 16, o);
-            } else {
-#pragma unroll
-              for (int b = 0; b < 2; ++b) {
-                U8x32 o;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) o.w[i] = __float_as_uint(v[8 * b + i]);
-                st256(reinterpret_cast<float*>(y) + off + c * 16 + 8 * b, o);
-              }
-            }
-            if (acc_out) {
-#pragma unroll
-              for (int b = 0; b < 2; ++b) {
-                U8x32 o;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) o.w[i] = (uint32_t)acc[c * 16 + 8 * b + i];
-                st256(acc_out + off + c * 16 + 8 * b, o);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              if (cb + i >= N) continue;
-              if (epi & EPI_BF16)
-                reinterpret_cast<__nv_bfloat16*>(y)[off + c * 16 + i] = __float2bfloat16_rn(v[i]);
-              else
-                reinterpret_cast<float*>(y)[off + c * 16 + i] = v[i];
-              if (acc_out) acc_out[off + c * 16 + i] = acc[c * 16 + i];
-            }
-          }
-        }
-      }
-    }
-    tc_fence_before();
-  }
-
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
-                 : "memory");
-  }
-  if (MC > 1) cluster_sync();  // no peer may still multicast into, or arrive on, this CTA
-}
-
 // ------------------------------------------------------------------------------------------
-// CTA-pair variant: tcgen05.mma.cta_group::2, 256 x 256 tiles over two SMs.
+// The CTA-pair kernel: tcgen05.mma.cta_group::2, 256 x 256 tiles over two SMs.
 //
 // Each CTA of a 2-CTA cluster stages its own 128 rows of A and its own 128-row half of the
 // tile's B (N split across the pair), so every SM moves 32 KB per 64-deep K step instead of
-// 48 KB for the same MMA work per SM as the single-CTA 128 x 256 tile.  The even CTA (leader)
+// the 48 KB a single-CTA 128 x 256 tile needs for the same MMA work per SM.  The even CTA (leader)
 // issues the pair's MMAs; they read both CTAs' shared memory at the same offsets and write each
 // CTA's 128 accumulator rows into that CTA's tensor memory.  Both producers signal the leader's
 // full barrier (TMA .cta_group::2), whose expected byte count covers the pair; MMA completion
 // is multicast to both CTAs' empty and chunk-full barriers; both epilogues release a drained
 // chunk buffer by arriving on the leader's chunk-empty barrier.  Tensor memory is allocated and
-// freed by one warp in each CTA together (cta_group::2).  Exactness and the chunked int32
-// accumulation are those of the single-CTA kernel.
+// freed by one warp in each CTA together (cta_group::2).
 // ------------------------------------------------------------------------------------------
 struct PairCfg {
   static constexpr int STAGES = 6;
@@ -817,135 +394,25 @@ dit_status launch_pair(const void* a, const float* a_scale, const void* b, const
   return DIT_OK;
 }
 
-// DIT6_INT8_TC_SPLIT=0 turns the split-K tail off (for comparisons and tests).
-static bool split_tail_enabled() {
-  const char* e = getenv("DIT6_INT8_TC_SPLIT");
-  return !(e && e[0] == '0');
-}
-
-template <int BN, int MC, bool GELU, bool SPLIT>
-dit_status launch_k(const CUtensorMap& ta, const CUtensorMap& tb, const float* a_scale, const float* b_scale,
-                    int64_t m, int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
-                    void* ws, cudaStream_t st, int tail_base, int parts, int64_t items);
-
-template <int BN, int MC, bool GELU>
-dit_status launch(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
-                  int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
-                  void* ws, size_t ws_bytes, cudaStream_t st) {
-  using C = Cfg<BN>;
-  CUtensorMap ta, tb;
-  if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(a), (uint64_t)k, (uint64_t)m,
-                      (uint64_t)k * 2, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(b), (uint64_t)k, (uint64_t)n,
-                      (uint64_t)k * 2, BK, BN / MC, CU_TENSOR_MAP_SWIZZLE_128B))
-    return DIT_ERR_CUDA;
-  const int64_t tiles = (((m + BM - 1) / BM + MC - 1) / MC) * ((n + BN - 1) / BN);
-  if (tiles > 0x7fffffff / 8) return DIT_ERR_UNSUPPORTED;
-  // Split-K tail: the R tiles of the last, partial wave become R x P items of nkb / P k-blocks
-  // each, so that the wave keeps more SMs busy.  Only for deep K (>= 4096): the partial-sum
-  // exchange and the final epilogue are not split, and on GB300 they cost more than the idle
-  // SMs of a short tile's last wave (measured on the CogVideoX-2B shapes).  Needs
-  // R <= SMs / 2 and room for the R x P partial-sum slots and tickets in the workspace.
-  int tail_base = (int)tiles, parts = 1;
-  if (BN == 256 && MC == 1 && k >= 4096 && split_tail_enabled()) {
-    const int64_t g = num_sms();
-    const int64_t r = tiles % g, nkb = (k + BK - 1) / BK;
-    const int64_t slot_bytes = (int64_t)BM * BN * 4;
-    int64_t p = r > 0 ? g / r : 1;
-    if (p > 4) p = 4;
-    if (p > nkb / 2) p = nkb / 2;
-    while (p > 1 && (r * p * slot_bytes > (int64_t)(ws_bytes - WS_SPLIT_PARTIALS) ||
-                     r * C::EPI_WARPS > WS_SPLIT_MAX_TICKETS))
-      --p;
-    if (p > 1) {
-      tail_base = (int)(tiles - r);
-      parts = (int)p;
-    }
-  }
-  const int64_t items = tail_base + (tiles - tail_base) * parts;
-  if constexpr (BN == 256 && MC == 1) {
-    if (parts > 1)
-      return launch_k<BN, MC, GELU, true>(ta, tb, a_scale, b_scale, m, n, k, bias, y, epi, acc_out, ws, st,
-                                          tail_base, parts, items);
-  }
-  return launch_k<BN, MC, GELU, false>(ta, tb, a_scale, b_scale, m, n, k, bias, y, epi, acc_out, ws, st,
-                                       tail_base, parts, items);
-}
-
-template <int BN, int MC, bool GELU, bool SPLIT>
-dit_status launch_k(const CUtensorMap& ta, const CUtensorMap& tb, const float* a_scale, const float* b_scale,
-                    int64_t m, int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
-                    void* ws, cudaStream_t st, int tail_base, int parts, int64_t items) {
-  using C = Cfg<BN>;
-  auto kern = k_gemm_int8_tc<BN, MC, GELU, SPLIT>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
-      return DIT_ERR_CUDA;
-    if (MC > 1 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess)
-      return DIT_ERR_CUDA;
-    attr_done = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = st;
-  int64_t grid = num_sms();
-  if (MC > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = MC;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cfg.gridDim = dim3((unsigned)(grid / MC * MC));
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return DIT_ERR_CUDA;
-    grid = (int64_t)clusters * MC;
-  }
-  if (grid > items * MC) grid = items * MC;
-  cfg.gridDim = dim3((unsigned)grid);
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, epi, acc_out,
-                         ws, MC > 1 ? 0 : test_stall(), tail_base, parts) != cudaSuccess)
-    return DIT_ERR_CUDA;
-  return DIT_OK;
-}
-
 }  // namespace i8tc
 
+// The CTA-pair kernel (256 x 256 tiles over two SMs).  When K spans at most two exact chunks
+// and no raw accumulators are requested, the chunk sums are added in fp32 (ACCM 1).
 dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
                         int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
                         void* ws, size_t ws_bytes, cudaStream_t st) {
-  const char* e = getenv("DIT6_INT8_TC_BN");
-  const char* c = getenv("DIT6_INT8_TC_CLUSTER");
-  const int bn = e ? atoi(e) : 256;
-  const int mc = c ? atoi(c) : 1;
+  (void)ws_bytes;
   const bool g = (epi & EPI_GELU) != 0;
-  // Default: the CTA-pair kernel (256 x 256 tiles over two SMs).  DIT6_INT8_TC_PAIR=0, or an
-  // explicit single-CTA tile (DIT6_INT8_TC_BN / DIT6_INT8_TC_CLUSTER), selects the single-CTA
-  // kernel, which also carries the split-K tail.
-  const char* pr = getenv("DIT6_INT8_TC_PAIR");
-  if (!(pr && pr[0] == '0') && !e && !c)
-  {
-    const bool f2 = !acc_out && (k + 1023) / 1024 <= 2;
-    if (f2)
-      return g ? i8tc::launch_pair<true, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
-               : i8tc::launch_pair<false, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
-    return g ? i8tc::launch_pair<true, 0>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
-             : i8tc::launch_pair<false, 0>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
-  }
-#define DIT6_I8TC(BN_, MC_)                                                                          \
-  return g ? i8tc::launch<BN_, MC_, true>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, ws_bytes, st) \
-           : i8tc::launch<BN_, MC_, false>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, ws_bytes, st)
-  if (bn == 128) DIT6_I8TC(128, 1);
-  if (bn == 192) DIT6_I8TC(192, 1);
-  if (mc == 2) DIT6_I8TC(256, 2);
-  DIT6_I8TC(256, 1);
-#undef DIT6_I8TC
+  const bool f2 = !acc_out && (k + 1023) / 1024 <= 2;
+  if (f2)
+    return g ? i8tc::launch_pair<true, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
+             : i8tc::launch_pair<false, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
+  return g ? i8tc::launch_pair<true, 0>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
+           : i8tc::launch_pair<false, 0>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
 }
 
 }  // namespace dit6
+
 
 // BF16 route of PDR ([EN] 2.C, [ZH] 2.C: full precision for a block whose input has a high
 // outlier ratio): Y = act(X W^T (+ bias)) on the untransformed bf16 operands, fp32 accumulation,

@@ -233,10 +233,12 @@ __global__ void __launch_bounds__(256) k_nvfp4_to_int8(const uint8_t* __restrict
 // ---------------------------------------------------------------------------------------
 // NVFP4 pass 1: amax of the transformed tensor -> s_g = amax / 2688 (workspace + output)
 // ---------------------------------------------------------------------------------------
+// raw_amax: write amax itself to tensor_scale_out (one shard of a token-sharded tensor, whose
+// tensor scale follows the all-reduce-max of every shard's amax), not s_g
 template <typename T, int HB>
 __global__ void __launch_bounds__(256) k_nvfp4_amax(const void* __restrict__ x, int64_t units,
                                                     float inv_sqrt_b, void* ws,
-                                                    float* __restrict__ tensor_scale_out) {
+                                                    float* __restrict__ tensor_scale_out, int raw_amax) {
   __shared__ float wmax[8];
   __shared__ bool last;
   float m = 0.f;
@@ -267,9 +269,13 @@ __global__ void __launch_bounds__(256) k_nvfp4_amax(const void* __restrict__ x, 
   if (last && threadIdx.x == 0) {
     __threadfence();
     const float amax = __uint_as_float(atomicExch(ws_u32(ws, WS_AMAX), 0u));
-    const float sg = __fdiv_rn(amax, 2688.0f);
-    *reinterpret_cast<float*>(ws_u32(ws, WS_SG)) = sg;
-    *tensor_scale_out = sg;
+    if (raw_amax) {
+      *tensor_scale_out = amax;
+    } else {
+      const float sg = __fdiv_rn(amax, 2688.0f);
+      *reinterpret_cast<float*>(ws_u32(ws, WS_SG)) = sg;
+      *tensor_scale_out = sg;
+    }
     *ws_u32(ws, WS_TICKET) = 0u;
   }
 }
@@ -349,7 +355,7 @@ static void launch_nvfp4_t(const void* x, int64_t rows, int upr, float isb, uint
     int64_t g1 = (units + 255) / 256;
     if (g1 > 6 * sms) g1 = 6 * sms;
     if (g1 < 1) g1 = 1;
-    k_nvfp4_amax<T, HB><<<(unsigned)g1, 256, 0, st>>>(x, units, isb, ws, ts_out);
+    k_nvfp4_amax<T, HB><<<(unsigned)g1, 256, 0, st>>>(x, units, isb, ws, ts_out, 0);
     sgp = reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws) + WS_SG);
   }
   int64_t g2 = (pad_units + 255) / 256;
@@ -433,6 +439,43 @@ extern "C" dit_status dit_nvfp4_to_int8(const uint8_t* codes, const uint8_t* sf,
     k_nvfp4_to_int8<true><<<(unsigned)grid, tr * upr, 0, st>>>(codes, sf, tensor_scale, rows, upr, tr, q, row_scale);
   else
     k_nvfp4_to_int8<false><<<(unsigned)grid, tr * upr, 0, st>>>(codes, sf, tensor_scale, rows, upr, tr, q, row_scale);
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
+// One shard of a token-sharded tensor: max|H x| over this shard's rows (the all-reduce-max of
+// every shard's value, turned into s_g = amax / (6 * 448) by dit_shard_finish, is the tensor
+// scale the unsharded quantiser derives from the whole tensor).
+template <typename T, int HB>
+static void launch_amax_shard(const void* x, int64_t rows, int upr, float isb, float* amax_out, void* ws,
+                              cudaStream_t st) {
+  const int64_t units = rows * upr;
+  int64_t g1 = (units + 255) / 256;
+  if (g1 > 6 * num_sms()) g1 = 6 * num_sms();
+  if (g1 < 1) g1 = 1;
+  k_nvfp4_amax<T, HB><<<(unsigned)g1, 256, 0, st>>>(x, units, isb, ws, amax_out, 1);
+}
+
+extern "C" dit_status dit_nvfp4_amax(const void* x, dit_dtype dt, int64_t rows, int64_t k, int hblock,
+                                     float* amax_dev, void* ws, size_t ws_bytes, dit_stream_t stream) {
+  dit_status s = check_quant_args(x, dt, rows, k, hblock);
+  if (s != DIT_OK) return s;
+  if (!amax_dev || !ws || ws_bytes < WS_BYTES) return DIT_ERR_INVALID_ARG;
+  if (!aligned32(ws)) return DIT_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int upr = (int)(k / UNIT);
+  const float isb = (float)(1.0 / sqrt((double)hblock));
+#define DIT_AS(T, HB) launch_amax_shard<T, HB>(x, rows, upr, isb, amax_dev, ws, st)
+  if (dt == DIT_BF16) {
+    if (hblock == 16) DIT_AS(__nv_bfloat16, 16);
+    else if (hblock == 32) DIT_AS(__nv_bfloat16, 32);
+    else DIT_AS(__nv_bfloat16, 64);
+  } else {
+    if (hblock == 16) DIT_AS(float, 16);
+    else if (hblock == 32) DIT_AS(float, 32);
+    else DIT_AS(float, 64);
+  }
+#undef DIT_AS
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }

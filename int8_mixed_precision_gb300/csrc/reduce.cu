@@ -140,7 +140,8 @@ __global__ void __launch_bounds__(RED_THREADS) k_gamma_route(const void* __restr
                                                              const void* __restrict__ xo,
                                                              int64_t n, RouteParams rp,
                                                              float* gamma_out,
-                                                             int32_t* routes, void* ws) {
+                                                             int32_t* routes, void* ws,
+                                                             double* partials_out) {
   constexpr int N = Vec<T>::N;
   constexpr int U = 4;  // vectors in flight per thread
   const int64_t nv = n / N;
@@ -183,6 +184,11 @@ __global__ void __launch_bounds__(RED_THREADS) k_gamma_route(const void* __restr
   }
   double r[2];
   if (!reduce_partials<2>(s, ws, r)) return;
+  if (partials_out) {  // one shard of a token-sharded tensor: the sums, for an all-reduce
+    partials_out[0] = r[0];
+    partials_out[1] = r[1];
+    return;
+  }
   const double g = ratio(r[0], r[1]);
   *gamma_out = (float)g;
   for (int l = 0; l < rp.n_layers; ++l) {
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(RED_THREADS) k_tdc_commit(const void* __restri
                                                             const void* __restrict__ d1,
                                                             void* __restrict__ dnew, int64_t n,
                                                             float* gamma_out, float* sim_out,
-                                                            void* ws) {
+                                                            void* ws, double* partials_out) {
   constexpr int N = Vec<T>::N;
   const int64_t nv = n / N;
   float s[4] = {0.f, 0.f, 0.f, 0.f};
@@ -286,6 +292,11 @@ __global__ void __launch_bounds__(RED_THREADS) k_tdc_commit(const void* __restri
   }
   double r[4];
   if (!reduce_partials<4>(s, ws, r)) return;
+  if (partials_out) {  // one shard: the four sums, for an all-reduce
+#pragma unroll
+    for (int i = 0; i < 4; ++i) partials_out[i] = r[i];
+    return;
+  }
   *gamma_out = (float)ratio(r[0], r[1]);
   *sim_out = d1 ? (float)ratio(r[2], r[3]) : __int_as_float(0x7f800000);
 }
@@ -363,10 +374,10 @@ extern "C" dit_status dit_gamma_route(const void* x_in, const void* x_out, dit_d
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (dt == DIT_BF16)
     k_gamma_route<__nv_bfloat16><<<red_grid(n, 16), RED_THREADS, 0, st>>>(x_in, x_out, n, rp,
-                                                                         gamma_dev, routes_dev, ws);
+                                                                         gamma_dev, routes_dev, ws, nullptr);
   else
     k_gamma_route<float><<<red_grid(n, 8), RED_THREADS, 0, st>>>(x_in, x_out, n, rp, gamma_dev,
-                                                               routes_dev, ws);
+                                                               routes_dev, ws, nullptr);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -402,10 +413,10 @@ extern "C" dit_status dit_tdc_step(int mode, const void* x_in, const void* x_out
     return DIT_ERR_ALIGNMENT;
   if (dt == DIT_BF16)
     k_tdc_commit<__nv_bfloat16><<<red_grid(n, 16), RED_THREADS, 0, st>>>(
-        x_in, x_out, d1, d_new, n, gamma_dev, sim_dev, ws);
+        x_in, x_out, d1, d_new, n, gamma_dev, sim_dev, ws, nullptr);
   else
     k_tdc_commit<float><<<red_grid(n, 8), RED_THREADS, 0, st>>>(x_in, x_out, d1, d_new, n,
-                                                              gamma_dev, sim_dev, ws);
+                                                              gamma_dev, sim_dev, ws, nullptr);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -435,6 +446,8 @@ static std::mutex g_noalloc_mu;
 
 // Device address of the scratch array on the current device.  The first call on a device
 // looks the address up (cudaGetSymbolAddress) and zero-fills the array once, synchronously.
+// The address stays cached for the life of the process, so the entry point must not be used
+// across a cudaDeviceReset, after which the module may be loaded at another address.
 static dit_status noalloc_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return DIT_ERR_CUDA;
@@ -478,10 +491,10 @@ extern "C" dit_status dit_gamma_route_noalloc(const void* x_in, const void* x_ou
   if (cudaMemsetAsync(scratch, 0, 8, st) != cudaSuccess) return DIT_ERR_CUDA;
   if (dt == DIT_BF16)
     k_gamma_route<__nv_bfloat16><<<grid, RED_THREADS, 0, st>>>(x_in, x_out, n, rp, gamma_dev,
-                                                               routes_dev, scratch);
+                                                               routes_dev, scratch, nullptr);
   else
     k_gamma_route<float><<<grid, RED_THREADS, 0, st>>>(x_in, x_out, n, rp, gamma_dev,
-                                                       routes_dev, scratch);
+                                                       routes_dev, scratch, nullptr);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -502,5 +515,128 @@ extern "C" dit_status dit_outlier_ratio(const void* x, dit_dtype dt, int64_t n, 
     k_count_over<float><<<g, RED_THREADS, 0, st>>>(x, n, ws, ratio_dev, count_dev);
   }
   DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+// Token-sharded form.  When one block's tokens are split across GPUs, every reduction of the
+// path becomes a per-shard partial plus one all-reduce: the two (Gamma) or four (TDC commit)
+// L1 sums add, and the NVFP4 tensor amax takes the maximum.  These calls produce a shard's
+// partials; dit_shard_finish (device) / dit_shard_finish_host turn the reduced values into
+// Gamma, the similarity, the routes and the tensor scale with the arithmetic of the
+// unsharded calls.
+// ---------------------------------------------------------------------------------------
+namespace dit6 {
+__global__ void k_shard_finish(const double* __restrict__ p, int n_partials, const float* __restrict__ amax,
+                               RouteParams rp, float* gamma_out, float* sim_out, int32_t* routes,
+                               float* tensor_scale_out) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  if (p) {
+    const double g = ratio(p[0], p[1]);
+    if (gamma_out) *gamma_out = (float)g;
+    if (sim_out) *sim_out = n_partials == 4 ? (float)ratio(p[2], p[3]) : __int_as_float(0x7f800000);
+    if (routes)
+      for (int l = 0; l < rp.n_layers; ++l) {
+        const double e = (double)rp.alpha[l] * g + (double)rp.beta[l];
+        routes[l] = e > (double)rp.thr[l] ? DIT_ROUTE_INT8 : DIT_ROUTE_NVFP4;
+      }
+  }
+  if (amax && tensor_scale_out) *tensor_scale_out = __fdiv_rn(*amax, 2688.0f);
+}
+}  // namespace dit6
+
+extern "C" dit_status dit_l1_partials(int mode, const void* x_in, const void* x_out, const void* d1, void* d_new,
+                                      dit_dtype dt, int64_t n, double* partials_dev, void* ws, size_t ws_bytes,
+                                      dit_stream_t stream) {
+  if (!x_in || !x_out || n <= 0 || !partials_dev || !ws || ws_bytes < WS_BYTES) return DIT_ERR_INVALID_ARG;
+  if (dt != DIT_F32 && dt != DIT_BF16) return DIT_ERR_INVALID_ARG;
+  if (mode != DIT_L1_GAMMA && mode != DIT_L1_TDC_COMMIT) return DIT_ERR_INVALID_ARG;
+  const bool commit = mode == DIT_L1_TDC_COMMIT;
+  if (commit && (!d_new || d1 == d_new)) return DIT_ERR_INVALID_ARG;
+  if (!aligned32(x_in) || !aligned32(x_out) || !aligned32(ws) || (commit && !aligned32(d_new)) ||
+      (commit && d1 && !aligned32(d1)) || (reinterpret_cast<uintptr_t>(partials_dev) & 7))
+    return DIT_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (commit) {
+    if (!d1 && cudaMemsetAsync(partials_dev + 2, 0, 2 * sizeof(double), st) != cudaSuccess) return DIT_ERR_CUDA;
+    if (dt == DIT_BF16)
+      k_tdc_commit<__nv_bfloat16><<<red_grid(n, 16), RED_THREADS, 0, st>>>(x_in, x_out, d1, d_new, n, nullptr,
+                                                                          nullptr, ws, partials_dev);
+    else
+      k_tdc_commit<float><<<red_grid(n, 8), RED_THREADS, 0, st>>>(x_in, x_out, d1, d_new, n, nullptr, nullptr, ws,
+                                                                partials_dev);
+  } else {
+    RouteParams rp;
+    rp.n_layers = 0;
+    if (dt == DIT_BF16)
+      k_gamma_route<__nv_bfloat16><<<red_grid(n, 16), RED_THREADS, 0, st>>>(x_in, x_out, n, rp, nullptr, nullptr,
+                                                                           ws, partials_dev);
+    else
+      k_gamma_route<float><<<red_grid(n, 8), RED_THREADS, 0, st>>>(x_in, x_out, n, rp, nullptr, nullptr, ws,
+                                                                 partials_dev);
+  }
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
+static dit_status route_params(const float* alpha, const float* beta, const float* thr, int n_layers,
+                               RouteParams* rp) {
+  if (n_layers < 0 || n_layers > DIT_MAX_LAYERS) return DIT_ERR_INVALID_ARG;
+  if (n_layers > 0 && (!alpha || !beta || !thr)) return DIT_ERR_INVALID_ARG;
+  rp->n_layers = n_layers;
+  for (int l = 0; l < n_layers; ++l) {
+    rp->alpha[l] = alpha[l];
+    rp->beta[l] = beta[l];
+    rp->thr[l] = thr[l];
+  }
+  return DIT_OK;
+}
+
+extern "C" dit_status dit_shard_finish(const double* partials_dev, int n_partials, const float* amax_dev,
+                                       const float* alpha, const float* beta, const float* thr, int n_layers,
+                                       float* gamma_dev, float* sim_dev, int32_t* routes_dev,
+                                       float* tensor_scale_dev, dit_stream_t stream) {
+  if (partials_dev && n_partials != 2 && n_partials != 4) return DIT_ERR_INVALID_ARG;
+  if (!partials_dev && (gamma_dev || sim_dev || routes_dev)) return DIT_ERR_INVALID_ARG;
+  if (sim_dev && n_partials != 4) return DIT_ERR_INVALID_ARG;
+  if ((amax_dev == nullptr) != (tensor_scale_dev == nullptr)) return DIT_ERR_INVALID_ARG;
+  if (!partials_dev && !amax_dev) return DIT_ERR_INVALID_ARG;
+  if (routes_dev && n_layers <= 0) return DIT_ERR_INVALID_ARG;
+  RouteParams rp;
+  dit_status s = route_params(alpha, beta, thr, routes_dev ? n_layers : 0, &rp);
+  if (s != DIT_OK) return s;
+  k_shard_finish<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(partials_dev, n_partials, amax_dev, rp,
+                                                                      gamma_dev, sim_dev, routes_dev,
+                                                                      tensor_scale_dev);
+  DIT_CHECK_LAUNCH();
+  return DIT_OK;
+}
+
+extern "C" dit_status dit_shard_finish_host(const double* partials, int n_partials, const float* amax,
+                                            const float* alpha, const float* beta, const float* thr, int n_layers,
+                                            float* gamma, float* sim, int32_t* routes, float* tensor_scale) {
+  if (partials && n_partials != 2 && n_partials != 4) return DIT_ERR_INVALID_ARG;
+  if (!partials && (gamma || sim || routes)) return DIT_ERR_INVALID_ARG;
+  if (sim && n_partials != 4) return DIT_ERR_INVALID_ARG;
+  if ((amax == nullptr) != (tensor_scale == nullptr)) return DIT_ERR_INVALID_ARG;
+  if (routes && (n_layers <= 0 || n_layers > DIT_MAX_LAYERS || !alpha || !beta || !thr)) return DIT_ERR_INVALID_ARG;
+  auto host_ratio = [](double num, double den) {
+    if (den == 0.0) return num == 0.0 ? 0.0 : (double)INFINITY;
+    return num / den;
+  };
+  if (partials) {
+    const double g = host_ratio(partials[0], partials[1]);
+    if (gamma) *gamma = (float)g;
+    if (sim) *sim = (float)host_ratio(partials[2], partials[3]);
+    if (routes)
+      for (int l = 0; l < n_layers; ++l) {
+        const double e = (double)alpha[l] * g + (double)beta[l];
+        routes[l] = e > (double)thr[l] ? DIT_ROUTE_INT8 : DIT_ROUTE_NVFP4;
+      }
+  }
+  if (amax) {
+    volatile float a = *amax;  // one correctly rounded fp32 division, as on the device
+    *tensor_scale = a / 2688.0f;
+  }
   return DIT_OK;
 }

@@ -3,12 +3,14 @@
   python -m int8_mixed_precision_gb300.kernel_bench --case gemm_nvfp4 --m 17776 --n 5760 --k 1920
 
 Cases: quant_int8, quant_nvfp4 (two passes), quant_nvfp4_given (one pass, tensor scale
-given), gamma, tdc_commit, tdc_skip, gemm_int8, gemm_nvfp4, ffn_nvfp4_fused / ffn_nvfp4_unfused
-(FFN up + GELU + quantisation for the next NVFP4 layer), outlier_ratio and gemm_bf16 (the
-PDR full-precision route).  Inputs are synthetic bf16
-activations (N(0,1), 1% outlier channels x50) and N(0,0.02) weights.  Prints one JSON line
-with the median time and the algorithmic rate (GB/s for streaming kernels, TFLOP/s for
-GEMMs).  Also the small cases used for ncu captures.
+given), gamma, tdc_commit, tdc_skip, gemm_int8, gemm_nvfp4, gemm_nvfp4_amax (the GEMM that
+also returns its output's NVFP4 tensor scale), outlier_ratio and gemm_bf16 (the PDR
+full-precision route).  Inputs are synthetic bf16 activations (N(0,1), 1% outlier channels
+x50) and N(0,0.02) weights.  Prints one JSON line with the median time and the algorithmic
+rate (GB/s for streaming kernels at the algorithmic bytes per element -- quantisers: 2 in
++ 1 out + 4 per row for INT8, 2 + 0.5 + 1/16 for NVFP4 -- and TFLOP/s for GEMMs); "moved"
+gives the bytes the kernel really reads and writes when they differ (bf16-held INT8 codes,
+the NVFP4 amax pass).  Also the small cases used for ncu captures.
 """
 from __future__ import annotations
 
@@ -46,19 +48,22 @@ def main(argv=None):
         return x.to(torch.bfloat16)
 
     case = a.case
+    moved = None
     if case in ("quant_int8", "quant_nvfp4", "quant_nvfp4_given"):
         x = act(m, k)
         if case == "quant_int8":
             q = torch.empty(m, k, dtype=torch.int8 if a.int8_container == "int8" else torch.bfloat16, device=dev)
             s = torch.empty(m, device=dev)
             fn = lambda: dit.hadamard_quant_int8(x, a.hblock, q, s)
-            units, unit = m * k * (2 + q.element_size()) + 4 * m, "GB/s"
+            units, unit = m * k * 3 + 4 * m, "GB/s"
+            moved = m * k * (2 + q.element_size()) + 4 * m
         else:
             b = dit.alloc_nvfp4(m, k, dev)
             dit.hadamard_quant_nvfp4(x, a.hblock, b["codes"], b["sf"], b["gs"], ws)
             sg = b["gs"].clone() if case == "quant_nvfp4_given" else None
             fn = lambda: dit.hadamard_quant_nvfp4(x, a.hblock, b["codes"], b["sf"], b["gs"], ws, tensor_scale_in=sg)
             units, unit = m * k * 2 + m * k // 2 + m * k // 16, "GB/s"
+            moved = units + (0 if sg is not None else m * k * 2)
     elif case in ("gamma", "tdc_commit", "tdc_skip"):
         xi = act(m, k)
         xo = (xi.float() * 1.05).to(torch.bfloat16)
@@ -77,28 +82,18 @@ def main(argv=None):
             fn = lambda: dit.tdc_step(dit.TDC_SKIP, xi, ws, x_out_skip=out, d1=d1)
             units = m * k * 6
         unit = "GB/s"
-    elif case in ("ffn_nvfp4_fused", "ffn_nvfp4_unfused"):
-        # FFN up with GELU whose output feeds an NVFP4 layer: the GEMM with the quantisation
-        # fused in its epilogue (supplied tensor scale), or the GEMM writing bf16 followed by
-        # the quantiser (two passes); the rate counts the GEMM FLOPs
+    elif case == "gemm_nvfp4_amax":
+        # FFN up with GELU whose output feeds an NVFP4 layer: the epilogue also reduces the
+        # output's NVFP4 tensor scale (the next quantisation is then one pass)
         x = act(m, k)
         w = torch.randn(n, k, device=dev, generator=g) * 0.02
         lin = dit.RoutedLinear(dit.QuantizedWeight(w, a.hblock, ws), m, ws, dev)
         y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
         lin(x, dit.ROUTE_NVFP4, y, act=dit.ACT_GELU_ERF)
-        q = dit.alloc_nvfp4(m, n, dev)
-        dit.hadamard_quant_nvfp4(y, a.hblock, q["codes"], q["sf"], q["gs"], ws)
         nxt = torch.empty(1, dtype=torch.float32, device=dev)
         A, W = lin.a4, lin.w.nvfp4
-        if case == "ffn_nvfp4_fused":
-            fn = lambda: dit.qgemm_nvfp4_fused_quant(A["codes"], A["sf"], A["gs"], W["codes"], W["sf"], W["gs"], ws,
-                                                     a.hblock, q["gs"], q["codes"], q["sf"], nxt,
-                                                     act=dit.ACT_GELU_ERF)
-        else:
-            def fn():
-                dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], W["codes"], W["sf"], W["gs"], y, ws,
-                                act=dit.ACT_GELU_ERF)
-                dit.hadamard_quant_nvfp4(y, a.hblock, q["codes"], q["sf"], q["gs"], ws)
+        fn = lambda: dit.qgemm_nvfp4_amax(A["codes"], A["sf"], A["gs"], W["codes"], W["sf"], W["gs"], y, ws,
+                                          a.hblock, nxt, act=dit.ACT_GELU_ERF)
         units, unit = 2 * m * n * k, "TFLOP/s"
     elif case == "outlier_ratio":
         x = act(m, k)
@@ -151,8 +146,11 @@ def main(argv=None):
     assert dit.device_status(ws) == 0, "device status raised"
     t = statistics.median(times)
     rate = units / (t * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
-    print(json.dumps({"case": case, "m": m, "n": n, "k": k, "median_us": round(t * 1e3, 2),
-                      "min_us": round(min(times) * 1e3, 2), "rate": round(rate, 2), "unit": unit}))
+    out = {"case": case, "m": m, "n": n, "k": k, "median_us": round(t * 1e3, 2),
+           "min_us": round(min(times) * 1e3, 2), "rate": round(rate, 2), "unit": unit}
+    if moved is not None and moved != units:
+        out["moved_gbs"] = round(moved / (t * 1e-3) / 1e9, 2)
+    print(json.dumps(out))
 
 
 if __name__ == "__main__":

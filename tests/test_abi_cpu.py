@@ -36,8 +36,9 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["dit_gamma_route", "dit_hadamard_quant_nvfp4", "dit_hadamard_quant_int8",
-              "dit_qgemm_nvfp4", "dit_qgemm_nvfp4_fused_quant", "dit_qgemm_nvfp4_amax", "dit_nvfp4_to_int8", "dit_qgemm_int8",
-              "dit_outlier_ratio", "dit_gemm_bf16", "dit_route_host_pdr", "dit_tdc_step", "dit_sf_index", "dit_status_str"]:
+              "dit_qgemm_nvfp4", "dit_qgemm_nvfp4_amax", "dit_nvfp4_to_int8", "dit_qgemm_int8",
+              "dit_outlier_ratio", "dit_gemm_bf16", "dit_route_host_pdr", "dit_tdc_step", "dit_sf_index", "dit_status_str",
+              "dit_l1_partials", "dit_nvfp4_amax", "dit_shard_finish", "dit_shard_finish_host"]:
         assert n in names
 
 
@@ -87,12 +88,6 @@ def test_host_argument_validation_without_device_work(L):
     assert L.dit_qgemm_int8(ws, ws, ws, ws, 0, 4, 8, 128, nul, 0, ws, 1, nul, ws, wsb, nul) == 1
     assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 96, nul, 0, ws, 1, ws, wsb, nul) == 3
     assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 128, nul, 0, ws, 1, ws, 100, nul) == 1
-    # fused quantisation: a missing output, an unsupported block size, n not a multiple of 64
-    F = L.dit_qgemm_nvfp4_fused_quant
-    assert F(ws, ws, ws, ws, ws, ws, 4, 128, 128, nul, 0, nul, 64, ws, ws, nul, ws, ws, wsb, nul) == 1
-    assert F(ws, ws, ws, ws, ws, ws, 4, 128, 128, nul, 0, nul, 128, ws, ws, ws, ws, ws, wsb, nul) == 3
-    assert F(ws, ws, ws, ws, ws, ws, 4, 96, 128, nul, 0, nul, 64, ws, ws, ws, ws, ws, wsb, nul) == 3
-    assert F(ws, ws, ws, ws, ws, ws, 4, 128, 128, nul, 0, fake_misaligned, 64, ws, ws, ws, ws, ws, wsb, nul) == 2
     # GEMM with its output's tensor scale: missing scale output, unsupported block, n % 64, misalignment
     G = L.dit_qgemm_nvfp4_amax
     assert G(ws, ws, ws, ws, ws, ws, 4, 128, 128, nul, 0, ws, 64, nul, ws, wsb, nul) == 1
@@ -112,6 +107,15 @@ def test_host_argument_validation_without_device_work(L):
     # an activation code outside dit_act
     assert L.dit_qgemm_int8(ws, ws, ws, ws, 2, 4, 8, 128, nul, 5, ws, 1, nul, ws, wsb, nul) == 1
     assert L.dit_qgemm_nvfp4(ws, ws, ws, ws, ws, ws, 4, 8, 128, nul, 2, ws, 1, ws, wsb, nul) == 1
+    # token-sharded form: bad mode, d1 == d_new, misaligned partials; finishing without inputs
+    assert L.dit_l1_partials(2, ws, ws, nul, nul, 1, 64, ws, ws, wsb, nul) == 1
+    assert L.dit_l1_partials(1, ws, ws, ws, ws, 1, 64, ws, ws, wsb, nul) == 1
+    assert L.dit_l1_partials(0, ws, ws, nul, nul, 1, 64, ctypes.c_void_p(0x2004), ws, wsb, nul) == 2
+    assert L.dit_nvfp4_amax(ws, 1, 4, 96, 64, ws, ws, wsb, nul) == 3
+    assert L.dit_shard_finish(nul, 0, nul, nul, nul, nul, 0, nul, nul, nul, nul, nul) == 1
+    assert L.dit_shard_finish(ws, 3, nul, nul, nul, nul, 0, ws, nul, nul, nul, nul) == 1
+    assert L.dit_shard_finish(ws, 2, nul, nul, nul, nul, 0, nul, ws, nul, nul, nul) == 1   # sim needs 4 sums
+    assert L.dit_shard_finish(nul, 0, ws, nul, nul, nul, 0, nul, nul, nul, nul, nul) == 1  # amax without output
     ws2 = ctypes.c_void_p(0x4000)
     assert L.dit_tdc_step(0, fake_misaligned, fake_misaligned, nul, ws, ws2, 1, 64, ws, ws, ws, wsb, nul) == 2
     assert L.dit_tdc_step(0, ws, ws, nul, ws, ws, 1, 64, ws, ws, ws, wsb, nul) == 1   # d1 == d_new
@@ -208,3 +212,20 @@ def test_host_pdr_routes_match_oracle(L):
         f32 = lambda v: np.float32(v).astype(np.float64)      # the C interface takes float parameters
         want = D.route_layers_pdr(gamma, f32(alpha), f32(beta), f32(thr), ratio, rho)
         assert st.routes(alpha, beta, thr, ratio, rho) == want
+
+
+def test_shard_finish_host_rules():
+    """The finishing arithmetic of the token-sharded form on host values: Gamma and the
+    similarity are fp64 ratios with the 0/0 -> 0 and x/0 -> +inf rule of the unsharded calls,
+    routes follow E_rel > thr, and the tensor scale is amax / 2688 in one fp32 division."""
+    import int8_mixed_precision_gb300 as dit
+    r = dit.shard_finish_host([3.0, 60.0, 1.0, 8.0], 448.0, [1.0, 1.0], [0.0, 0.0], [0.05, 0.049])
+    assert r["gamma"] == np.float32(0.05) and r["sim"] == 0.125
+    assert r["routes"] == [D.ROUTE_NVFP4, D.ROUTE_INT8]      # 0.05 > 0.05 is false; > 0.049 true
+    assert np.float32(r["tensor_scale"]) == np.float32(np.float32(448.0) / np.float32(2688.0))
+    assert dit.shard_finish_host([0.0, 0.0, 5.0, 0.0])["gamma"] == 0.0
+    assert math.isinf(dit.shard_finish_host([0.0, 0.0, 5.0, 0.0])["sim"])
+    assert math.isinf(dit.shard_finish_host([1.0, 0.0])["gamma"])
+    for amax in (0.0, 1e-30, 3.0e38, 6.0 * 448.0 * 1.7):
+        assert np.float32(dit.shard_finish_host(amax=amax)["tensor_scale"]) == \
+            D.nvfp4_tensor_scale(np.array([amax], np.float32))

@@ -257,17 +257,12 @@ def _int8_dev(a, container):
     return t if container == torch.int8 else t.to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("container,bn", [(torch.int8, None), (torch.bfloat16, "192"), (torch.bfloat16, "128"),
-                                          (torch.bfloat16, "256"), (torch.bfloat16, "256c2"), (torch.bfloat16, "pair")])
+@pytest.mark.parametrize("container", [torch.int8, torch.bfloat16])
 @pytest.mark.parametrize("m,n,k", [(256, 512, 128), (300, 384, 1920), (129, 256, 7680), (1, 8, 16),
                                    (200, 136, 208), (700, 5760 // 10, 2112)])
-def test_int8_gemm_exact_accumulators(m, n, k, container, bn, ws, monkeypatch):
-    if bn == "pair":
-        monkeypatch.setenv("DIT6_INT8_TC_PAIR", "1")
-    elif bn:
-        monkeypatch.setenv("DIT6_INT8_TC_PAIR", "0")
-        monkeypatch.setenv("DIT6_INT8_TC_BN", bn[:3])
-        monkeypatch.setenv("DIT6_INT8_TC_CLUSTER", "2" if bn.endswith("c2") else "1")
+def test_int8_gemm_exact_accumulators(m, n, k, container, ws):
+    """int8-held codes run on IMMA, bf16-held codes on the CTA-pair tcgen05 kernel: both give the
+    int64 oracle's accumulators bit for bit."""
     g = synth.rng(m * n + k)
     a = g.integers(-127, 128, (m, k)).astype(np.int8)
     b = g.integers(-127, 128, (n, k)).astype(np.int8)
@@ -315,34 +310,26 @@ def test_gelu_epilogue_elementwise_error_bound(container, ws):
 
 
 @pytest.mark.parametrize("m,n,k", [(2560, 1920, 4096), (17776, 1920, 7680), (640, 1920, 12288), (300, 384, 4160)])
-def test_int8_gemm_split_tail_bit_exact(m, n, k, ws, monkeypatch):
-    """The split-K tail (K >= 4096: last partial wave of 128 x 256 tiles spread over idle SMs, int32
-    partial sums added by the last part) gives the same accumulators and outputs, bit for bit,
-    as whole tiles; sampled rows also match the int64 oracle."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    tiles = -(-m // 128) * -(-n // 256)
-    if not 0 < tiles % sms <= sms // 2:
-        pytest.skip(f"{tiles} tiles on {sms} SMs: no split tail for this shape")
+def test_int8_gemm_many_tiles_per_pair_bit_exact(m, n, k, ws):
+    """Shapes with more 256 x 256 tiles than CTA pairs (each pair walks several tiles, the chunk
+    buffers alternate across tile boundaries) and deep K: sampled rows of the accumulators equal
+    the int64 oracle, and the GELU output equals the epilogue's arithmetic on those integers."""
     g = synth.rng(m + n + k + 1)
     a = g.integers(-127, 128, (m, k)).astype(np.int8)
     b = g.integers(-127, 128, (n, k)).astype(np.int8)
     sa = (g.random(m) * 0.01).astype(np.float32)
     sb = (g.random(n) * 0.01).astype(np.float32)
     ta, tb = _int8_dev(a, torch.bfloat16), _int8_dev(b, torch.bfloat16)
-    outs = {}
-    monkeypatch.setenv("DIT6_INT8_TC_PAIR", "0")   # the single-CTA kernel carries the split
-    for split in ("0", "1"):
-        monkeypatch.setenv("DIT6_INT8_TC_SPLIT", split)
-        acc = torch.empty(m, n, dtype=torch.int32, device="cuda")
-        y = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
-        dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws, acc_debug=acc, act=dit.ACT_GELU_ERF)
-        _status_clean(ws)
-        outs[split] = (acc, y)
-    assert torch.equal(outs["0"][0], outs["1"][0])
-    assert torch.equal(outs["0"][1].view(torch.int16), outs["1"][1].view(torch.int16))
-    rows = np.unique(np.concatenate([synth.rng(m).choice(m, 24, replace=False), [m - 1]]))
+    acc = torch.empty(m, n, dtype=torch.int32, device="cuda")
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws, acc_debug=acc, act=dit.ACT_GELU_ERF)
+    _status_clean(ws)
+    rows = np.unique(np.concatenate([synth.rng(m).choice(m, 24, replace=False), [0, m - 1]]))
     ref = D.gemm_int8_acc(a[rows], b)
-    assert np.array_equal(host(outs["1"][0][torch.from_numpy(rows).cuda()]).astype(np.int64), ref)
+    assert np.array_equal(host(acc[torch.from_numpy(rows).cuda()]).astype(np.int64), ref)
+    x = (ref.astype(np.float32) * sa[rows, None]).astype(np.float32) * sb[None, :]
+    err = np.abs(host(y[torch.from_numpy(rows).cuda()]).astype(np.float64) - D.gelu_erf(x.astype(np.float32)))
+    assert (err <= 2.5e-6 * np.abs(x) + 1e-37).all()
 
 
 def _adversarial_int8(m, n, k, seed):
@@ -360,14 +347,8 @@ def _adversarial_int8(m, n, k, seed):
     return a, b
 
 
-@pytest.mark.parametrize("cluster", ["1", "2", "pair"])
 @pytest.mark.parametrize("k", [1024, 1040, 2048, 7680, 12288])
-def test_int8_gemm_bf16_pipe_exact_at_the_bound(k, cluster, ws, monkeypatch):
-    if cluster == "pair":
-        monkeypatch.setenv("DIT6_INT8_TC_PAIR", "1")
-    else:
-        monkeypatch.setenv("DIT6_INT8_TC_PAIR", "0")
-        monkeypatch.setenv("DIT6_INT8_TC_CLUSTER", cluster)
+def test_int8_gemm_bf16_pipe_exact_at_the_bound(k, ws):
     """Extreme codes (+-127 everywhere, totals up to 12288 * 127^2 ~ 2^27.6): the chunked fp32
     accumulation on the bf16 tensor pipe still gives the exact int32 accumulators."""
     m, n = 200, 392
@@ -394,11 +375,16 @@ def _nvfp4_operands(m, n, k, seed):
     return qa, qb, out[0], out[1]
 
 
-@pytest.mark.parametrize("cfg", ["0", "1", "2", "3", "4", "5", "6", "7", "8", "9", "10", "11", "12", "13", "14", "15", "18", "23"])
 @pytest.mark.parametrize("m,n,k", [(256, 512, 128), (300, 384, 1920), (129, 256, 7680), (128, 128, 64),
-                                   (77, 136, 320)])
-def test_nvfp4_gemm_parity(m, n, k, cfg, ws, monkeypatch):
-    monkeypatch.setenv("DIT6_NVFP4_TILE", cfg)
+                                   (77, 136, 320), (129, 384, 4096), (4096, 2688, 1024), (8192, 2048, 256)])
+def test_nvfp4_gemm_parity(m, n, k, ws):
+    """Each shape runs three outputs (fp32; bf16 with bias; fp32 with bias and GELU), which between
+    them reach every tile configuration the call picks: 128 x 128 tiles (fp32 with K < 3072 or N
+    off the 256 grid; bf16 with N off the 256 grid and K >= 4096), 128 x 256 tiles with eight
+    epilogue warps (bf16; fp32 with K >= 3072 and N on the 256 grid) and with sixteen (GELU).
+    The last N tile of N = 384, 136 and 2688 holds at most 128 columns (half-tile MMAs); the two
+    large shapes give every CTA several tiles, so the accumulator halves change hands across tile
+    boundaries, with one K stage (K = 256) and with four (K = 1024)."""
     qa, qb, A, B = _nvfp4_operands(m, n, k, seed=m + n + k)
     y = torch.empty(m, n, dtype=torch.float32, device="cuda")
     dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], y, ws)
@@ -461,66 +447,6 @@ def test_nvfp4_gemm_output_tensor_scale_full_size(ws):
     dit.hadamard_quant_nvfp4(y, hb, q["codes"], q["sf"], q["gs"], ws)
     _status_clean(ws)
     assert sc.view(torch.int32).item() == q["gs"].view(torch.int32).item()
-
-
-@pytest.mark.parametrize("m,n,k,hb,act,with_y", [(300, 512, 320, 64, 1, True), (256, 384, 128, 32, 0, False),
-                                                 (129, 768, 1920, 16, 1, True), (77, 128, 64, 64, 1, False)])
-def test_nvfp4_fused_epilogue_quant(m, n, k, hb, act, with_y, ws):
-    """GEMM + GELU + bf16 rounding + block Hadamard + NVFP4 encoding in one epilogue: with the
-    tensor scale the unfused quantiser derives, codes, scales and the returned scale equal the
-    unfused GEMM -> dit_hadamard_quant_nvfp4 path byte for byte, and match the oracle's
-    encoding of the GPU's bf16 output; a stale (halved) scale saturates exactly as the
-    quantiser with a supplied scale does."""
-    qa, qb, A, B = _nvfp4_operands(m, n, k, seed=m * 7 + n + k)
-    bias = torch.linspace(-0.5, 0.5, n, device="cuda", dtype=torch.float32)
-    z = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
-    dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], z, ws, bias=bias, act=act)
-    ref = dit.alloc_nvfp4(m, n)
-    dit.hadamard_quant_nvfp4(z, hb, ref["codes"], ref["sf"], ref["gs"], ws)
-    for scale in (ref["gs"], ref["gs"] * 0.5):
-        codes = torch.full_like(ref["codes"], 0x77)
-        sf = torch.full_like(ref["sf"], 0x77)
-        nxt = torch.zeros(1, dtype=torch.float32, device="cuda")
-        y = torch.zeros(m, n, dtype=torch.bfloat16, device="cuda") if with_y else None
-        dit.qgemm_nvfp4_fused_quant(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], ws, hb, scale,
-                                    codes, sf, nxt, y=y, bias=bias, act=act)
-        _status_clean(ws)
-        unf = dit.alloc_nvfp4(m, n)
-        dit.hadamard_quant_nvfp4(z, hb, unf["codes"], unf["sf"], unf["gs"], ws, tensor_scale_in=scale)
-        torch.cuda.synchronize()
-        assert torch.equal(codes, unf["codes"]) and torch.equal(sf, unf["sf"])
-        assert nxt.view(torch.int32).item() == ref["gs"].view(torch.int32).item()
-        if with_y:
-            assert torch.equal(y.view(torch.int16), z.view(torch.int16))
-        check_nvfp4(host(codes), host(sf), host(scale)[0], host(z), "bf16", hb, m, n, s_g=host(scale)[0])
-
-
-def test_nvfp4_fused_epilogue_quant_full_size_sampled(ws):
-    """CogVideoX-2B FFN-up at full size (17776 x 1920 -> 7680, GELU) quantised for FFN-down in
-    the epilogue: equal to the unfused path byte for byte; sampled rows against the oracle."""
-    m, k, n, hb = synth.TOKENS_2B, 1920, 7680, 64
-    x, xd = make_x(m, k, "bf16", seed=61)
-    wq = dit.QuantizedWeight(dev_f32(synth.weights(n, k, seed=62)), hb, ws)
-    a4 = dit.alloc_nvfp4(m, k)
-    dit.hadamard_quant_nvfp4(xd, hb, a4["codes"], a4["sf"], a4["gs"], ws)
-    z = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
-    W = wq.nvfp4
-    dit.qgemm_nvfp4(a4["codes"], a4["sf"], a4["gs"], W["codes"], W["sf"], W["gs"], z, ws, act=dit.ACT_GELU_ERF)
-    ref = dit.alloc_nvfp4(m, n)
-    dit.hadamard_quant_nvfp4(z, hb, ref["codes"], ref["sf"], ref["gs"], ws)
-    codes, sf = torch.empty_like(ref["codes"]), torch.empty_like(ref["sf"])
-    nxt = torch.empty(1, dtype=torch.float32, device="cuda")
-    dit.qgemm_nvfp4_fused_quant(a4["codes"], a4["sf"], a4["gs"], W["codes"], W["sf"], W["gs"], ws, hb, ref["gs"],
-                                codes, sf, nxt, act=dit.ACT_GELU_ERF)
-    _status_clean(ws)
-    assert torch.equal(codes, ref["codes"]) and torch.equal(sf, ref["sf"])
-    assert nxt.view(torch.int32).item() == ref["gs"].view(torch.int32).item()
-    rows = np.unique(np.concatenate([synth.rng(63).choice(m, 24, replace=False), np.arange(m - 4, m)]))
-    zr = F.bf16_bits_to_f32(host(z[torch.from_numpy(rows).cuda()]))
-    r = D.quant_nvfp4(D.block_fwht_f32(zr, hb), s_g=np.float32(host(ref["gs"])[0]))
-    got = D.unpack_e2m1(host(codes[torch.from_numpy(rows).cuda()]))
-    ex = (F.e2m1_rounding_margin(r["v"]) <= 1e-5) | (F.e4m3_rounding_margin(r["sbf"]) <= 1e-5).repeat(16, axis=1)
-    assert not ((got != r["codes"]) & ~ex).any()
 
 
 # ------------------------------------------------------------------------------ NVFP4-only weights
@@ -713,21 +639,30 @@ def test_tdc_chained_blocks_full_size(ws):
     _status_clean(ws)
 
 
-@pytest.mark.parametrize("route", ["nvfp4", "int8", "int8_split", "int8_pair"])
+@pytest.mark.parametrize("route", ["nvfp4", "nvfp4_gelu", "nvfp4_fp32", "int8"])
 def test_gemm_bounded_wait_reports_timeout_and_recovers(route, monkeypatch):
     """A GEMM whose producer issues no loads (test hook): the consumers' bounded waits run out
     after ~1 s, the kernel records DIT_ERR_TIMEOUT in the workspace status word, frees its
     tensor memory and exits; the next normal call on the same context is correct."""
     import time
     ws2 = dit.workspace()
-    # int8_split: 2 tiles over 4096-deep K, split into 4 parts each; the aborted parts still
-    # arrive on their tickets, so the next call's split finds them at zero
-    m, n, k = (256, 256, 4096) if route == "int8_split" else (256, 256, 128)
+    # the NVFP4 routes reach the three tile configurations: bf16 output (128 x 256, eight epilogue
+    # warps), GELU (sixteen), fp32 output with K < 3072 (128 x 128, two CTAs per SM)
+    m, n, k = 256, 256, 128
     g = synth.rng(55)
-    if route == "nvfp4":
+    if route.startswith("nvfp4"):
         qa, qb, A, B = _nvfp4_operands(m, n, k, seed=56)
         ref = D.gemm_nvfp4(qa["codes"], qa["sf"], qa["s_g"], qb["codes"], qb["sf"], qb["s_g"])
-        call = lambda y: dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], y, ws2)
+        act = dit.ACT_GELU_ERF if route == "nvfp4_gelu" else dit.ACT_NONE
+        if act:
+            ref = D.gelu_erf(ref)
+        if route == "nvfp4":   # bf16 output: compare with the oracle as bf16 would store it
+            ref = F.bf16_bits_to_f32(F.f32_to_bf16_bits(ref.astype(np.float32))).astype(np.float64)
+        ybuf = torch.zeros(m, n, dtype=torch.bfloat16 if route == "nvfp4" else torch.float32, device="cuda")
+
+        def call(y):
+            dit.qgemm_nvfp4(A["codes"], A["sf"], A["gs"], B["codes"], B["sf"], B["gs"], ybuf, ws2, act=act)
+            y.copy_(ybuf.float())
     else:
         a = g.integers(-127, 128, (m, k)).astype(np.int8)
         b = g.integers(-127, 128, (n, k)).astype(np.int8)
@@ -735,7 +670,6 @@ def test_gemm_bounded_wait_reports_timeout_and_recovers(route, monkeypatch):
         ref = D.gemm_int8(a, sa, b, sb)
         ta, tb = _int8_dev(a, torch.bfloat16), _int8_dev(b, torch.bfloat16)
         call = lambda y: dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws2)
-    monkeypatch.setenv("DIT6_INT8_TC_PAIR", "1" if route == "int8_pair" else "0")
     y = torch.zeros(m, n, dtype=torch.float32, device="cuda")
     monkeypatch.setenv("DIT6_TEST_STALL_PRODUCER", "1")
     t0 = time.time()
