@@ -1,21 +1,27 @@
 """Benchmark of the routed NVFP4/INT8 linear layer + Temporal Delta Cache on GB300.
 
-Workload (default): CogVideoX-2B-shaped DiT block linears, bf16, hidden 1920, 17776 tokens
-(13x30x45 video + 226 text), QKV 1920->5760, out 1920->1920, FFN 1920->7680->1920,
-Hadamard block 64, 1% outlier channels x50, 30 blocks whose Gamma ~ U(0, 0.2) routes each
-block to INT8 (Gamma > 0.05) or NVFP4.  Synthetic, seeded inputs (no trained weights exist).
+Workload (default): CogVideoX-5B-shaped DiT block linears, bf16, hidden 3072, 17776 tokens
+(13x30x45 video + 226 text), QKV 3072->9216, out 3072->3072, FFN 3072->12288->3072 (GELU),
+Hadamard block 64, Laplace(0,1) activations with 0.5% outlier channels x100, 42 blocks whose
+Gamma ~ U(0, 0.2) routes each block to INT8 (Gamma > 0.05) or NVFP4.  Synthetic, seeded
+inputs (no trained weights exist); weights N(0, 0.02), resident in both formats.
 
-One step = one pass over the 30 blocks: for each block its four routed linears (online
+One step = one pass over the 42 blocks: for each block its four routed linears (online
 block Hadamard + activation quantisation + quantised GEMM; GELU (erf form) fused into the
 FFN-up epilogue, whose output is the FFN-down input; when both FFN linears route NVFP4 the
 FFN-up epilogue also yields its output's NVFP4 tensor scale, so FFN-down's quantisation is
-one pass) and the delta-cache commit (residual delta, Gamma_t for the next step's routing,
-similarity of the last two deltas).
+one pass) and the delta-cache commit of the block's own input/output pair (residual delta,
+Gamma_t for the next step's routing, similarity of the last two deltas).
 value = algorithmic GEMM FLOPs of the step / step time (TFLOP/s).
+
+Further keys of the JSON line: the CogVideoX-2B step (hidden 1920, 30 blocks), the whole
+1080p-shaped path (104746 tokens: Gamma, both quantisers, both FFN GEMMs per route, delta
+commit and skip), the NVFP4-only-weights variant, the full TDC/PDR loop (50 steps x 30 2B
+blocks, its decisions replayed by the CPU oracle) and the CPU oracle baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Under torchrun each rank runs its own 30-block replica (independent problems, no data-path
+Under torchrun each rank runs its own replica (independent problems, no data-path
 collective: weak scaling); value = FLOPs of all ranks / max time over ranks.
 """
 from __future__ import annotations
@@ -33,12 +39,35 @@ sys.path.insert(0, ROOT)
 
 METRIC = "quantized-linear TFLOPS (NVFP4 / INT8) & HBM GB/s of quant+TDC, 1 GB300"
 UNIT = "TFLOP/s"
-WORKLOAD = "cogvideox_2b_block_linears"
-TOKENS = 13 * 30 * 45 + 226
-HIDDEN, FFN, HBLOCK, NBLOCKS = 1920, 7680, 64, 30
+HBLOCK = 64
 THR, ALPHA, BETA = 0.05, 1.0, 0.0
-LINEARS = [("qkv", HIDDEN, 3 * HIDDEN), ("out", HIDDEN, HIDDEN), ("ffn_up", HIDDEN, FFN),
-           ("ffn_down", FFN, HIDDEN)]
+TOKENS = 13 * 30 * 45 + 226
+TOKENS_1080P = 13 * 67 * 120 + 226
+
+WORKLOADS = {
+    "cogvideox_5b_block_linears": {"tokens": TOKENS, "hidden": 3072, "ffn": 12288, "blocks": 42,
+                                   "dist": "laplace", "outlier_frac": 0.005, "outlier_mult": 100.0,
+                                   "activations": "Laplace(0,1), 0.5% outlier channels x100"},
+    "cogvideox_2b_block_linears": {"tokens": TOKENS, "hidden": 1920, "ffn": 7680, "blocks": 30,
+                                   "dist": "normal", "outlier_frac": 0.01, "outlier_mult": 50.0,
+                                   "activations": "N(0,1), 1% outlier channels x50"},
+}
+DEFAULT_WORKLOAD = "cogvideox_5b_block_linears"
+KINDS = ("gemm_int8", "gemm_nvfp4", "quant_int8", "quant_nvfp4", "tdc_commit")
+
+
+def linears(spec):
+    h, f = spec["hidden"], spec["ffn"]
+    return [("qkv", h, 3 * h), ("out", h, h), ("ffn_up", h, f), ("ffn_down", f, h)]
+
+
+# Algorithmic bytes of the streaming kernels (bf16 input), per call
+def bytes_quant_int8(m, k):       # 2 in + 1 out per element + one fp32 scale per row
+    return m * k * 3 + 4 * m
+
+
+def bytes_quant_nvfp4(m, k):      # 2 in + 0.5 codes + 1/16 block scales per element
+    return m * k * 2 + m * k // 2 + m * k // 16
 
 
 # The sources each kernel type is built from (its own file, the shared device helpers and the
@@ -51,6 +80,7 @@ KERNEL_SOURCES = {
     "tdc_commit": ["reduce.cu"],
 }
 SHARED_SOURCES = ["common.cuh", "api.cu"]
+TRAFFIC_PROFILE = os.path.join("profiles", "dram_traffic_cogvideox5b_layers.md")
 
 
 def kernel_sources_hash(kind: str) -> str:
@@ -68,13 +98,13 @@ def kernel_sources_hash(kind: str) -> str:
 
 
 def measured_traffic(kind: str):
-    """DRAM bytes per launch of a kernel type from the committed ncu summary of this workload,
-    or None when that kernel type's sources have changed since the capture (their hash, listed
-    per kernel type in the summary, differs)."""
+    """DRAM bytes per launch of a kernel type in the default step, from the committed ncu
+    summary: the mean of the per-shape captures listed for that type (every block that routes
+    a kernel type runs it once per listed layer shape), or None when the type has no capture or
+    its sources have changed since (their hash, listed per type, differs)."""
     import re
-    path = os.path.join(ROOT, "profiles", "dram_traffic_cogvideox2b_step.md")
     try:
-        text = open(path).read()
+        text = open(os.path.join(ROOT, TRAFFIC_PROFILE)).read()
     except OSError:
         return None
     if kind not in KERNEL_SOURCES:
@@ -82,8 +112,8 @@ def measured_traffic(kind: str):
     m = re.search(r"^\| " + re.escape(kind) + r" sources \| ([0-9a-f]{64}) \|", text, re.M)
     if not m or m.group(1) != kernel_sources_hash(kind):
         return None
-    row = re.search(r"^\| " + re.escape(kind) + r" \| \d+ \| [\d.]+ \| [\d.]+ \| (\d+) \|", text, re.M)
-    return int(row.group(1)) if row else None
+    rows = re.findall(r"^\| " + re.escape(kind) + r" \| [^|]+ \| \d+ \| [\d.]+ \| [\d.]+ \| (\d+) \|", text, re.M)
+    return int(round(sum(int(r) for r in rows) / len(rows))) if rows else None
 
 
 def peaks():
@@ -168,71 +198,96 @@ class Clocks:
 # ----------------------------------------------------------------------------------------
 
 
-class Workload:
-    """Device-resident synthetic workload: 30 blocks of routed linears + delta-cache state."""
+def device_activations(torch, g, dev, m, k, spec, seed):
+    """[m x k] bf16 activations of the workload's law on the device (seeded torch generator):
+    N(0,1) or Laplace(0,1) (inverse CDF of a uniform draw), floor(frac * k) outlier channels
+    scaled by the multiplier."""
+    g.manual_seed(seed)
+    if spec["dist"] == "laplace":
+        u = torch.rand(m, k, device=dev, generator=g).clamp_(min=2.0 ** -24) - 0.5
+        x = -torch.sign(u) * torch.log1p(-2.0 * u.abs())
+        del u
+    else:
+        x = torch.randn(m, k, device=dev, generator=g)
+    ch = torch.randperm(k, device=dev, generator=g)[: max(1, int(k * spec["outlier_frac"]))]
+    x[:, ch] *= spec["outlier_mult"]
+    return x.to(torch.bfloat16)
 
-    def __init__(self, dev, seed: int):
+
+class Workload:
+    """Device-resident synthetic workload: the blocks of routed linears + delta-cache state."""
+
+    def __init__(self, dev, seed: int, name: str = DEFAULT_WORKLOAD):
         import torch
         import int8_mixed_precision_gb300 as dit
         self.dit, self.torch, self.dev = dit, torch, dev
+        self.name, self.spec = name, WORKLOADS[name]
+        self.lin_shapes = linears(self.spec)
+        self.nblocks = self.spec["blocks"]
         g = torch.Generator(device=dev)
-        g.manual_seed(seed)
         self.ws = dit.workspace(dev)
-        M = TOKENS
-
-        def act(k, s):
-            g.manual_seed(seed * 1000 + s)
-            x = torch.randn(M, k, device=dev, generator=g)
-            ch = torch.randperm(k, device=dev, generator=g)[: max(1, k // 100)]
-            x[:, ch] *= 50.0
-            return x.to(torch.bfloat16)
-
-        # two alternating activation sets (consecutive blocks never share an input tensor); the
-        # FFN-down input is not among them: it is GELU(FFN-up output), produced in the step
-        self.inputs = [{name: act(k, 10 * s + i) for i, (name, k, _) in enumerate(LINEARS) if name != "ffn_down"}
-                       for s in range(2)]
-        self.x_in = act(HIDDEN, 99)
-        # per-block Gamma pairs: X_out = X_in + gamma_b * S * X_in, gamma_b ~ U(0, 0.2)
+        M, H = self.spec["tokens"], self.spec["hidden"]
+        act = lambda k, s: device_activations(torch, g, dev, M, k, self.spec, seed * 1000 + s)
+        # two alternating sets of linear inputs (consecutive blocks never share an input
+        # tensor); the FFN-down input is GELU(FFN-up output), produced in the step
+        self.inputs = [{name: act(k, 10 * s + i) for i, (name, k, _) in enumerate(self.lin_shapes)
+                        if name != "ffn_down"} for s in range(2)]
+        # per-block Gamma pairs: X_out = X_in + gamma_b * S * X_in, gamma_b ~ U(0, 0.2); every
+        # block commits its own pair
         g.manual_seed(seed + 7)
-        self.gammas_true = (torch.rand(NBLOCKS, generator=g, device=dev) * 0.2).tolist()
-        self.x_out, self.blocks = [], []
-        for b in range(NBLOCKS):
+        self.gammas_true = (torch.rand(self.nblocks, generator=g, device=dev) * 0.2).tolist()
+        # quantised-activation buffers shared by all blocks (one stream orders their uses)
+        self.act_bufs = {}
+        for _, k, _ in self.lin_shapes:
+            if k not in self.act_bufs:
+                self.act_bufs[k] = (dit.alloc_nvfp4(M, k, dev), dit.alloc_int8(M, k, dev))
+        self.x_in, self.x_out, self.blocks = [], [], []
+        for b in range(self.nblocks):
+            xi = act(H, 500 + b)
             g.manual_seed(seed * 31 + b)
-            sgn = torch.randint(0, 2, self.x_in.shape, generator=g, device=dev).to(torch.float32) * 2 - 1
-            self.x_out.append((self.x_in.float() * (1 + self.gammas_true[b] * sgn)).to(torch.bfloat16))
+            sgn = torch.randint(0, 2, xi.shape, generator=g, device=dev).to(torch.float32) * 2 - 1
+            self.x_in.append(xi)
+            self.x_out.append((xi.float() * (1 + self.gammas_true[b] * sgn)).to(torch.bfloat16))
+            del sgn
             lins = {}
-            for name, k, n in LINEARS:
+            for name, k, n in self.lin_shapes:
                 g.manual_seed(seed * 7919 + b * 17 + n + k)
                 w = torch.randn(n, k, device=dev, generator=g) * 0.02
-                lins[name] = dit.RoutedLinear(dit.QuantizedWeight(w, HBLOCK, self.ws), M, self.ws, dev)
+                lins[name] = dit.RoutedLinear(dit.QuantizedWeight(w, HBLOCK, self.ws), M, self.ws, dev,
+                                              act_buffers=self.act_bufs[k])
                 del w
-            self.blocks.append({"lin": lins, "d": [torch.empty_like(self.x_in), torch.empty_like(self.x_in)],
+            self.blocks.append({"lin": lins, "d": [torch.empty_like(xi), torch.empty_like(xi)],
                                 "has_delta": False})
-        self.y = {name: torch.empty(M, n, dtype=torch.bfloat16, device=dev) for name, _, n in LINEARS}
-        self.gamma = torch.empty(NBLOCKS, dtype=torch.float32, device=dev)
+        self.y = {name: torch.empty(M, n, dtype=torch.bfloat16, device=dev) for name, _, n in self.lin_shapes}
+        self.gamma = torch.empty(self.nblocks, dtype=torch.float32, device=dev)
         self.up_scale = torch.empty(1, dtype=torch.float32, device=dev)   # FFN-up output's NVFP4 tensor scale
-        self.sim = torch.empty(NBLOCKS, dtype=torch.float32, device=dev)
+        self.sim = torch.empty(self.nblocks, dtype=torch.float32, device=dev)
         # routing from the predictor (one Gamma per block; the commit of every step
         # recomputes it, and with fixed pairs the routes stay the same)
         r = torch.empty(4, dtype=torch.int32, device=dev)
         self.routes = []
-        for b in range(NBLOCKS):
-            dit.gamma_route(self.x_in, self.x_out[b], [ALPHA] * 4, [BETA] * 4, [THR] * 4,
+        for b in range(self.nblocks):
+            dit.gamma_route(self.x_in[b], self.x_out[b], [ALPHA] * 4, [BETA] * 4, [THR] * 4,
                             self.gamma[b:b + 1], r, self.ws)
             self.routes.append(r.tolist())
         torch.cuda.synchronize()
-        self.flops_step = NBLOCKS * sum(2 * M * n * k for _, k, n in LINEARS)
-        self.int8_code_bytes = self.blocks[0]["lin"]["qkv"].a8["q"].element_size()
+        self.flops_step = self.nblocks * sum(2 * M * n * k for _, k, n in self.lin_shapes)
+        self.int8_code_bytes = self.act_bufs[H][1]["q"].element_size()
         self.timers = None   # {kernel type: [event pairs]} when per-kernel timing is on
+
+    def free(self):
+        self.inputs = self.x_in = self.x_out = self.blocks = self.y = self.act_bufs = None
+        self.torch.cuda.empty_cache()
+
+    def chained(self, b):
+        nv = self.dit.ROUTE_NVFP4
+        return self.routes[b][2] == nv and self.routes[b][3] == nv
 
     def launches_per_step(self):
         n = 0
-        nv = self.dit.ROUTE_NVFP4
-        for b in range(NBLOCKS):
-            rr = self.routes[b]
-            chained = rr[2] == nv and rr[3] == nv   # FFN-down's quantisation is one pass
-            for li, r in enumerate(rr):
-                n += 2 if r == self.dit.ROUTE_INT8 or (chained and li == 3) else 3
+        for b in range(self.nblocks):
+            for li, r in enumerate(self.routes[b]):
+                n += 2 if r == self.dit.ROUTE_INT8 or (self.chained(b) and li == 3) else 3
             n += 1
         return n
 
@@ -256,7 +311,8 @@ class Workload:
             if before_block is not None:
                 before_block(b)
             xs = self.inputs[b % 2]
-            for li, (name, k, n) in enumerate(LINEARS):
+            chained = self.chained(b)
+            for li, (name, k, n) in enumerate(self.lin_shapes):
                 lin = blk["lin"][name]
                 route = self.routes[b][li]
                 x = self.y["ffn_up"] if name == "ffn_down" else xs[name]
@@ -272,7 +328,6 @@ class Workload:
                 else:
                     # FFN-up -> FFN-down both on NVFP4: the FFN-up GEMM's epilogue also yields its
                     # output's tensor scale, and FFN-down's quantisation is then one pass
-                    chained = self.routes[b][2] == dit.ROUTE_NVFP4 and self.routes[b][3] == dit.ROUTE_NVFP4
                     ts_in = self.up_scale if (chained and name == "ffn_down") else None
                     self._timed("quant_nvfp4", lambda: dit.hadamard_quant_nvfp4(
                         x, HBLOCK, lin.a4["codes"], lin.a4["sf"], lin.a4["gs"], self.ws, tensor_scale_in=ts_in))
@@ -286,92 +341,157 @@ class Workload:
                             lin.w.nvfp4["gs"], y, self.ws, act=act))
             d_new, d_old = blk["d"][0], blk["d"][1]
             self._timed("tdc_commit", lambda: dit.tdc_step(
-                dit.TDC_COMMIT, self.x_in, self.ws, x_out=self.x_out[b], d1=d_old if blk["has_delta"] else None,
+                dit.TDC_COMMIT, self.x_in[b], self.ws, x_out=self.x_out[b], d1=d_old if blk["has_delta"] else None,
                 d_new=d_new, gamma=self.gamma[b:b + 1], sim=self.sim[b:b + 1]))
             blk["d"].reverse()
             blk["has_delta"] = True
 
-    # algorithmic units per kernel launch type (FLOPs for GEMMs, bytes otherwise)
     def kernel_units(self):
-        M = TOKENS
-        u = {"gemm_int8": 0, "gemm_nvfp4": 0, "quant_int8": 0, "quant_nvfp4": 0, "tdc_commit": 0}
-        for b in range(NBLOCKS):
-            for li, (name, k, n) in enumerate(LINEARS):
+        """Algorithmic units per kernel type and step: FLOPs (2 M N K) for the GEMMs, the bytes of
+        the survey's per-element accounting otherwise (INT8 quantiser 3 B/elem + 4 B/row, NVFP4
+        quantiser 2.5625 B/elem, delta commit 8 B/elem).  The second dict holds the bytes the
+        quantisers really move (bf16-held INT8 codes, the NVFP4 amax pass)."""
+        M, H = self.spec["tokens"], self.spec["hidden"]
+        u = {k: 0 for k in KINDS}
+        moved = {"quant_int8": 0, "quant_nvfp4": 0}
+        for b in range(self.nblocks):
+            for li, (name, k, n) in enumerate(self.lin_shapes):
                 if self.routes[b][li] == self.dit.ROUTE_INT8:
                     u["gemm_int8"] += 2 * M * n * k
-                    u["quant_int8"] += M * k * (2 + self.int8_code_bytes) + 4 * M
+                    u["quant_int8"] += bytes_quant_int8(M, k)
+                    moved["quant_int8"] += M * k * (2 + self.int8_code_bytes) + 4 * M
                 else:
                     u["gemm_nvfp4"] += 2 * M * n * k
-                    u["quant_nvfp4"] += M * k * 2 + M * k // 2 + M * k // 16
-            u["tdc_commit"] += M * HIDDEN * 8
-        return u
+                    u["quant_nvfp4"] += bytes_quant_nvfp4(M, k)
+                    one_pass = self.chained(b) and name == "ffn_down"
+                    moved["quant_nvfp4"] += bytes_quant_nvfp4(M, k) + (0 if one_pass else 2 * M * k)
+            u["tdc_commit"] += M * H * 8
+        return u, moved
 
 
-def run_large_shapes(dev, reps: int = 5):
-    """The two quantised GEMMs alone on the 1080p-shaped long sequence (104746 tokens, FFN 3072 ->
-    12288 -> 3072, Laplace activations with 0.5 % outlier channels x100): median CUDA-event time
-    of `reps` launches, L2 flushed by a 640 MB read before each, against the measured burst peaks
-    (a kernel timed alone)."""
+def _median_us(torch, fn, reps, flush):
+    fn()
+    times = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.max()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(times)
+
+
+def run_long_1080p(dev, reps: int = 5):
+    """The whole hot path on the 1080p-shaped long sequence (104746 tokens, hidden 3072, FFN
+    3072 -> 12288 -> 3072, Laplace activations with 0.5 % outlier channels x100): Gamma and
+    routing, both quantisers on the FFN-up input (3072) and the FFN-down input (12288), the FFN
+    GEMMs on both routes (GELU in the FFN-up epilogue; on the NVFP4 route it also yields the
+    FFN-down input's tensor scale, so that quantisation is one pass), the delta-cache commit and
+    skip.  Each kernel: median CUDA-event time of `reps` launches, L2 flushed before each (a
+    640 MB read), against the measured burst peaks (kernels timed alone).  The per-route path
+    adds the kernels one FFN pass of that route runs."""
     import torch
     import int8_mixed_precision_gb300 as dit
-    pk, _ = peaks()
+    pk, src = peaks()
+    spec = WORKLOADS["cogvideox_5b_block_linears"]
+    m, h, f = TOKENS_1080P, 3072, 12288
     g = torch.Generator(device=dev)
-    g.manual_seed(4242)
     ws = dit.workspace(dev)
     flush = torch.ones(640 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    m, out = 104746, {}
-    for name, k, n in (("ffn_up", 3072, 12288), ("ffn_down", 12288, 3072)):
-        u = torch.rand(m, k, device=dev, generator=g).clamp_(min=2.0 ** -24) - 0.5   # Laplace(0, 1), inverse CDF
-        x = -torch.sign(u) * torch.log1p(-2.0 * u.abs())
-        del u
-        x[:, torch.randperm(k, device=dev, generator=g)[: max(1, k * 5 // 1000)]] *= 100.0
-        x = x.to(torch.bfloat16)
-        w = torch.randn(n, k, device=dev, generator=g) * 0.02
-        lin = dit.RoutedLinear(dit.QuantizedWeight(w, HBLOCK, ws), m, ws, dev)
-        del w
-        y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
-        lin(x, dit.ROUTE_NVFP4, y)
-        lin(x, dit.ROUTE_INT8, y)
-        del x
-        A4, W4, A8, W8 = lin.a4, lin.w.nvfp4, lin.a8, lin.w.int8
-        calls = {"nvfp4": lambda: dit.qgemm_nvfp4(A4["codes"], A4["sf"], A4["gs"], W4["codes"], W4["sf"], W4["gs"],
-                                                  y, ws),
-                 "int8": lambda: dit.qgemm_int8(A8["q"], A8["scale"], W8["q"], W8["scale"], y, ws)}
-        for route, fn in calls.items():
-            fn()
-            times = []
-            for _ in range(reps):
-                flush.max()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                fn()
-                e1.record()
-                e1.synchronize()
-                times.append(e0.elapsed_time(e1))
-            t = statistics.median(times)
-            tf = 2.0 * m * n * k / (t * 1e-3) / 1e12
-            peak = pk["bf16_tflops"] * (6.0 if route == "nvfp4" else 1.0)
-            out[f"{name}_{route}"] = {"m": m, "n": n, "k": k, "us": round(t * 1e3, 1), "tflops": round(tf, 1),
-                                      "peak": round(peak, 1), "frac": round(tf / peak, 4)}
-        del lin, y
-        torch.cuda.empty_cache()
+    x = device_activations(torch, g, dev, m, h, spec, 9001)
+    g.manual_seed(9002)
+    sgn = torch.randint(0, 2, x.shape, generator=g, device=dev).to(torch.float32) * 2 - 1
+    x_out = (x.float() * (1 + 0.1 * sgn)).to(torch.bfloat16)
+    del sgn
+    d1 = (x_out.float() - x.float()).mul_(1.01).to(torch.bfloat16)
+    d_new, skip_out = torch.empty_like(x), torch.empty_like(x)
+    g.manual_seed(9003)
+    w_up = torch.randn(f, h, device=dev, generator=g) * 0.02
+    w_dn = torch.randn(h, f, device=dev, generator=g) * 0.02
+    up = dit.RoutedLinear(dit.QuantizedWeight(w_up, HBLOCK, ws), m, ws, dev)
+    dn = dit.RoutedLinear(dit.QuantizedWeight(w_dn, HBLOCK, ws), m, ws, dev)
+    del w_up, w_dn
+    y_up = torch.empty(m, f, dtype=torch.bfloat16, device=dev)
+    y_dn = torch.empty(m, h, dtype=torch.bfloat16, device=dev)
+    gam = torch.empty(1, device=dev)
+    sim = torch.empty(1, device=dev)
+    routes = torch.empty(4, dtype=torch.int32, device=dev)
+    up_scale = torch.empty(1, device=dev)
+    up(x, dit.ROUTE_NVFP4, y_up, act=dit.ACT_GELU_ERF)      # a GELU output as the FFN-down input
+    A, W = up.a4, up.w.nvfp4
+    calls = {
+        "gamma_route": (lambda: dit.gamma_route(x, x_out, [ALPHA] * 4, [BETA] * 4, [THR] * 4, gam, routes, ws),
+                        "hbm", 4 * m * h),
+        "quant_nvfp4_k3072": (lambda: dit.hadamard_quant_nvfp4(x, HBLOCK, up.a4["codes"], up.a4["sf"], up.a4["gs"],
+                                                               ws), "hbm", bytes_quant_nvfp4(m, h)),
+        "quant_int8_k3072": (lambda: dit.hadamard_quant_int8(x, HBLOCK, up.a8["q"], up.a8["scale"]), "hbm",
+                             bytes_quant_int8(m, h)),
+        "gemm_nvfp4_ffn_up_gelu_amax": (lambda: dit.qgemm_nvfp4_amax(A["codes"], A["sf"], A["gs"], W["codes"],
+                                                                     W["sf"], W["gs"], y_up, ws, HBLOCK, up_scale,
+                                                                     act=dit.ACT_GELU_ERF), "tensor_fp4", 2 * m * f * h),
+        "gemm_int8_ffn_up_gelu": (lambda: dit.qgemm_int8(up.a8["q"], up.a8["scale"], up.w.int8["q"],
+                                                         up.w.int8["scale"], y_up, ws, act=dit.ACT_GELU_ERF),
+                                  "tensor_bf16", 2 * m * f * h),
+        "quant_nvfp4_k12288_one_pass": (lambda: dit.hadamard_quant_nvfp4(y_up, HBLOCK, dn.a4["codes"], dn.a4["sf"],
+                                                                         dn.a4["gs"], ws, tensor_scale_in=up_scale),
+                                        "hbm", bytes_quant_nvfp4(m, f)),
+        "quant_nvfp4_k12288_two_pass": (lambda: dit.hadamard_quant_nvfp4(y_up, HBLOCK, dn.a4["codes"], dn.a4["sf"],
+                                                                         dn.a4["gs"], ws), "hbm", bytes_quant_nvfp4(m, f)),
+        "quant_int8_k12288": (lambda: dit.hadamard_quant_int8(y_up, HBLOCK, dn.a8["q"], dn.a8["scale"]), "hbm",
+                              bytes_quant_int8(m, f)),
+        "gemm_nvfp4_ffn_down": (lambda: dit.qgemm_nvfp4(dn.a4["codes"], dn.a4["sf"], dn.a4["gs"], dn.w.nvfp4["codes"],
+                                                        dn.w.nvfp4["sf"], dn.w.nvfp4["gs"], y_dn, ws),
+                                "tensor_fp4", 2 * m * h * f),
+        "gemm_int8_ffn_down": (lambda: dit.qgemm_int8(dn.a8["q"], dn.a8["scale"], dn.w.int8["q"], dn.w.int8["scale"],
+                                                      y_dn, ws), "tensor_bf16", 2 * m * h * f),
+        "tdc_commit": (lambda: dit.tdc_step(dit.TDC_COMMIT, x, ws, x_out=x_out, d1=d1, d_new=d_new, gamma=gam,
+                                            sim=sim), "hbm", 8 * m * h),
+        "tdc_skip": (lambda: dit.tdc_step(dit.TDC_SKIP, x, ws, x_out_skip=skip_out, d1=d1), "hbm", 6 * m * h),
+    }
+    out = {}
+    for name, (fn, bound, units) in calls.items():
+        us = _median_us(torch, fn, reps, flush)
+        if bound == "hbm":
+            a = units / (us * 1e-6) / 1e9
+            out[name] = {"us": round(us, 1), "achieved": round(a, 1), "unit": "GB/s", "peak": pk["hbm_gbs"],
+                         "frac": round(a / pk["hbm_gbs"], 4)}
+        else:
+            a = units / (us * 1e-6) / 1e12
+            p = pk["bf16_tflops"] * (6.0 if bound == "tensor_fp4" else 1.0)
+            out[name] = {"us": round(us, 1), "achieved": round(a, 1), "unit": "TFLOP/s", "peak": round(p, 1),
+                         "frac": round(a / p, 4)}
     torch.cuda.synchronize()
     assert dit.device_status(ws) == 0
-    out["peak_source"] = ("measured bf16 burst (INT8 codes on the bf16 tensor pipe) and bf16 burst x 6 (NVFP4, "
-                          "nominal dense fp4/bf16 ratio)")
+    flops = 2 * 2 * m * h * f
+    paths = {"nvfp4": ["gamma_route", "quant_nvfp4_k3072", "gemm_nvfp4_ffn_up_gelu_amax",
+                       "quant_nvfp4_k12288_one_pass", "gemm_nvfp4_ffn_down", "tdc_commit"],
+             "int8": ["gamma_route", "quant_int8_k3072", "gemm_int8_ffn_up_gelu", "quant_int8_k12288",
+                      "gemm_int8_ffn_down", "tdc_commit"]}
+    for route, names in paths.items():
+        us = sum(out[n]["us"] for n in names)
+        out[f"path_{route}"] = {"us": round(us, 1), "tflops": round(flops / (us * 1e-6) / 1e12, 1),
+                                "kernels": names}
+    out["workload"] = {"tokens": m, "hidden": h, "ffn": f, "activations": spec["activations"],
+                       "peak_source": f"{src} HBM copy; bf16 burst (INT8 codes on the bf16 tensor pipe); "
+                                      "bf16 burst x 6 (NVFP4, nominal dense fp4/bf16 ratio)"}
+    del up, dn, x, x_out, d1, d_new, skip_out, y_up, y_dn, flush
+    torch.cuda.empty_cache()
     return out
 
 
-def run_nvfp4_only_weights(wl, steps: int = 5):
+def run_nvfp4_only_weights(wl, steps: int = 3):
     """The same step with every weight resident in NVFP4 only ([ZH] 2.A weight handling): each
     INT8-routed layer derives its INT8 weights per call into one scratch buffer per K."""
     import torch
     import int8_mixed_precision_gb300 as dit
     dev = wl.dev
-    scratch = {k: dit.alloc_int8(max(n for _, kk, n in LINEARS if kk == k), k, dev) for _, k, _ in LINEARS}
+    scratch = {k: dit.alloc_int8(max(n for _, kk, n in wl.lin_shapes if kk == k), k, dev) for _, k, _ in wl.lin_shapes}
     saved = []
     for blk in wl.blocks:
-        for name, k, n in LINEARS:
+        for name, k, n in wl.lin_shapes:
             lin = blk["lin"][name]
             saved.append((lin, lin.w, lin.w8_scratch))
             lin.w = lin.w.without_int8()
@@ -392,48 +512,58 @@ def run_nvfp4_only_weights(wl, steps: int = 5):
     wl.timers = None
     for lin, w, sc in saved:
         lin.w, lin.w8_scratch = w, sc
-    return {"ms_per_step": round(ms, 3), "value": round(wl.flops_step / (ms * 1e-3) / 1e12, 3), "unit": UNIT,
-            "weight_conversion_ms_per_step": round(conv_ms, 3),
+    return {"workload": wl.name, "ms_per_step": round(ms, 3), "value": round(wl.flops_step / (ms * 1e-3) / 1e12, 3),
+            "unit": UNIT, "weight_conversion_ms_per_step": round(conv_ms, 3),
             "resident_weight_bytes": int(only), "resident_weight_bytes_nvfp4_and_int8": int(both),
             "note": "weights resident in NVFP4 only; INT8-routed layers convert theirs per call (dit_nvfp4_to_int8)"}
 
 
-def run_tdc_loop(wl, steps: int = 50, tau: float = 0.05, seed: int = 77):
-    """The full TDC/PDR loop on the same 30 CogVideoX-2B blocks: per denoising step and block,
-    skip (X_out = X_in + cached delta) or compute (four routed linears + delta commit), with
-    the block chain X_in(b+1) = X_out(b).  The synthetic "true" block delta follows
-    Delta_t = Delta_{t-1} (1 + eps), eps ~ N(0, 0.01) elementwise, N(0, 0.5) on jump steps
-    (Bernoulli(1/8) per block-step), Delta_0 ~ N(0, sigma_b), sigma_b ~ U(0.02, 0.15); it is
-    generated on the device between our kernels and is not part of the timed segments."""
+def run_tdc_loop(wl, steps: int = 50, tau: float = 0.05, seed: int = 77, replay_blocks: int = 2):
+    """The full TDC/PDR loop on CogVideoX-2B blocks: per denoising step and block, skip (X_out =
+    X_in + cached delta) or compute (four routed linears + delta commit), with the block chain
+    X_in(b+1) = X_out(b).  The synthetic "true" block delta follows Delta_t = Delta_{t-1}
+    (1 + eps), eps ~ N(0, 0.01) elementwise, N(0, 0.5) on jump steps (Bernoulli(1/8) per
+    block-step), Delta_0 ~ N(0, sigma_b), sigma_b ~ U(0.02, 0.15), held in bf16; it is generated
+    on the device between our kernels and is not part of the timed segments.  The first
+    `replay_blocks` blocks of the chain are replayed by the CPU oracle step by step on host
+    copies of their inputs and true deltas: skip decisions and routes must be identical (a
+    decision or route within 1e-5 relative of its threshold is counted, not compared)."""
     import torch
     import int8_mixed_precision_gb300 as dit
-    dev, M = wl.dev, TOKENS
+    from oracle import dmpq as D
+    from oracle import tdc as T
+    dev, M, H = wl.dev, wl.spec["tokens"], wl.spec["hidden"]
+    nb = wl.nblocks
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
-    gam = torch.zeros(NBLOCKS, dtype=torch.float32, device=dev)
-    sim = torch.zeros(NBLOCKS, dtype=torch.float32, device=dev)
-    blocks = [dit.DeltaCachedBlock(M * HIDDEN, torch.bfloat16, tau, [ALPHA] * 4, [BETA] * 4, [THR] * 4, wl.ws,
-                                   gam[b:b + 1], sim[b:b + 1], dev) for b in range(NBLOCKS)]
-    sig = (torch.rand(NBLOCKS, generator=g, device=dev) * 0.13 + 0.02).tolist()
-    deltas = [torch.randn(M, HIDDEN, generator=g, device=dev) * sig[b] for b in range(NBLOCKS)]
-    x0 = wl.x_in
+    gam = torch.zeros(nb, dtype=torch.float32, device=dev)
+    sim = torch.zeros(nb, dtype=torch.float32, device=dev)
+    blocks = [dit.DeltaCachedBlock(M * H, torch.bfloat16, tau, [ALPHA] * 4, [BETA] * 4, [THR] * 4, wl.ws,
+                                   gam[b:b + 1], sim[b:b + 1], dev) for b in range(nb)]
+    sig = (torch.rand(nb, generator=g, device=dev) * 0.13 + 0.02).tolist()
+    deltas = [(torch.randn(M, H, generator=g, device=dev) * sig[b]).to(torch.bfloat16) for b in range(nb)]
+    x0 = wl.x_in[0]
     xb = [torch.empty_like(x0), torch.empty_like(x0)]
     y = wl.y
+    oracle = [T.BlockLoop(tau, [ALPHA] * 4, [BETA] * 4, [THR] * 4, "bf16") for _ in range(replay_blocks)]
+    bits = lambda t: t.contiguous().view(torch.int16).cpu().numpy().view("uint16")
+    mismatch, borderline, compared = 0, 0, 0
     segs, n_skip, n_comp, route_count, launches = [], 0, 0, [0, 0], 0
-    skip_bytes = commit_bytes = 0.0
-    skip_ms = commit_ms = 0.0
     ev = lambda: torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
+    oracle_s = 0.0
     for t in range(steps):
         x = x0
         for b, blk in enumerate(blocks):
             if t > 0:  # advance the true trajectory
                 jump = bool(torch.rand(1, generator=g, device=dev).item() < 1.0 / 8.0)
-                eps = torch.randn(M, HIDDEN, generator=g, device=dev) * (0.5 if jump else 0.01)
-                deltas[b].mul_(1.0 + eps)
+                eps = torch.randn(M, H, generator=g, device=dev) * (0.5 if jump else 0.01)
+                deltas[b] = (deltas[b].float() * (1.0 + eps)).to(torch.bfloat16)
+                del eps
             x_next = xb[1] if x is xb[0] else xb[0]
             mode = blk.decide()
+            routes = None
             a, z = ev(), ev()
             if mode == dit.TDC_SKIP:
                 a.record()
@@ -446,7 +576,7 @@ def run_tdc_loop(wl, steps: int = 50, tau: float = 0.05, seed: int = 77):
                 routes = blk.routes()
                 lins = wl.blocks[b]["lin"]
                 a.record()
-                for li, (name, k, n) in enumerate(LINEARS):
+                for li, (name, k, n) in enumerate(wl.lin_shapes):
                     xin = y["ffn_up"] if name == "ffn_down" else x
                     lins[name](xin, routes[li], y[name],
                                act=dit.ACT_GELU_ERF if name == "ffn_up" else dit.ACT_NONE)
@@ -454,7 +584,7 @@ def run_tdc_loop(wl, steps: int = 50, tau: float = 0.05, seed: int = 77):
                     route_count[routes[li]] += 1
                 z.record()
                 segs.append(("linears", a, z))
-                x_next.copy_((x.float() + deltas[b]).to(torch.bfloat16))
+                x_next.copy_((x.float() + deltas[b].float()).to(torch.bfloat16))
                 a2, z2 = ev(), ev()
                 a2.record()
                 blk.commit(x, x_next)
@@ -462,6 +592,23 @@ def run_tdc_loop(wl, steps: int = 50, tau: float = 0.05, seed: int = 77):
                 segs.append(("commit", a2, z2))
                 n_comp += 1
                 launches += 1
+            if b < replay_blocks:   # the oracle takes the same step on host copies
+                t0 = time.perf_counter()
+                r = oracle[b].step(bits(x).reshape(M, H), bits(deltas[b]).reshape(M, H), want_skip_output=False)
+                got = "skip" if mode == dit.TDC_SKIP else "compute"
+                if r["margin"] <= 1e-5:
+                    borderline += 1
+                else:
+                    compared += 1
+                    if r["decision"] != got:
+                        mismatch += 1
+                    elif routes is not None:
+                        g_ref = r["gamma"]
+                        if g_ref is not None and D.route_margin(g_ref, ALPHA, BETA, THR) <= 1e-5:
+                            borderline += 1
+                        elif routes != r["routes"]:
+                            mismatch += 1
+                oracle_s += time.perf_counter() - t0
             x = x_next
         h = torch.stack([gam, sim]).cpu()      # one device-to-host copy per denoising step
         for b, blk in enumerate(blocks):
@@ -472,18 +619,23 @@ def run_tdc_loop(wl, steps: int = 50, tau: float = 0.05, seed: int = 77):
     for kind, a, z in segs:
         tot[kind] += a.elapsed_time(z)
     kernel_ms = sum(tot.values())
-    n_elem = M * HIDDEN
+    n_elem = M * H
     total_bits = route_count[1] * 8 + route_count[0] * 4.5
+    del deltas, xb
+    torch.cuda.empty_cache()
     return {
-        "workload": "cogvideox_2b_tdc_loop", "denoising_steps": steps, "blocks": NBLOCKS, "tau": tau,
+        "workload": "cogvideox_2b_tdc_loop", "denoising_steps": steps, "blocks": nb, "tau": tau,
         "skip_fraction": round(n_skip / (n_skip + n_comp), 4), "computed_block_steps": n_comp,
         "skipped_block_steps": n_skip, "routes": {"int8": route_count[1], "nvfp4": route_count[0]},
         "avg_activation_bits": round(total_bits / max(1, sum(route_count)), 3),
         "kernel_ms_total": round(kernel_ms, 2), "kernel_ms_per_denoising_step": round(kernel_ms / steps, 3),
-        "wall_s_incl_synthetic_delta_generation": round(wall, 2),
+        "wall_s_incl_synthetic_delta_generation_and_oracle_replay": round(wall, 2),
         "tdc_skip_gbs": round(n_skip * n_elem * 6 / (tot["skip"] * 1e-3) / 1e9, 1) if n_skip else None,
         "tdc_commit_gbs": round(n_comp * n_elem * 8 / (tot["commit"] * 1e-3) / 1e9, 1) if n_comp else None,
         "gpu_launches": launches,
+        "oracle_replay": {"blocks": replay_blocks, "block_steps_compared": compared, "borderline": borderline,
+                          "mismatches": mismatch, "decisions_match_oracle": mismatch == 0,
+                          "cpu_seconds": round(oracle_s, 1)},
     }
 
 
@@ -503,85 +655,86 @@ def aggregate_value(units_per_rank: float, world: int, ms_max: float) -> float:
     return units_per_rank * world / (ms_max * 1e-3) / 1e12
 
 
-def int8_ceiling(torch, dev):
-    """cuBLASLt INT8 GEMM throughput (torch._int_mm, 8192^3) measured in this run."""
-    a = torch.randint(-127, 127, (8192, 8192), device=dev, dtype=torch.int8)
-    b = torch.randint(-127, 127, (8192, 8192), device=dev, dtype=torch.int8)
-    for _ in range(2):
-        torch._int_mm(a, b.t())
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(5):
-        torch._int_mm(a, b.t())
-    e1.record()
-    e1.synchronize()
-    return 5 * 2 * 8192 ** 3 / (e0.elapsed_time(e1) * 1e-3) / 1e12
-
-
-def run_ours(args, rank, world, local_rank):
-    import torch
-    import torch.distributed as tdist
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    wl = Workload(dev, seed=1234 + rank)
-    stream = torch.cuda.current_stream()
-
-    # one instrumented warm-up step: which kernel type dominates
-    wl.timers = {k: [] for k in ("gemm_int8", "gemm_nvfp4", "quant_int8", "quant_nvfp4", "tdc_commit")}
+def instrumented_kernels(wl, pk):
+    """One step with every launch event-timed: total ms per kernel type and each type against
+    its own bound (GEMMs: bf16 sustained, x 6 for NVFP4; streaming kernels: the HBM copy rate
+    at the algorithmic bytes, with the bytes the quantisers really move beside them)."""
+    torch = wl.torch
+    wl.timers = {k: [] for k in KINDS}
     wl.step()
     torch.cuda.synchronize()
     tot = {k: sum(a.elapsed_time(z) for a, z in v) for k, v in wl.timers.items()}
-    dominant = max(tot, key=tot.get)
+    n = {k: len(v) for k, v in wl.timers.items()}
     wl.timers = None
-    for _ in range(max(0, args.warmup - 1)):
+    units, moved = wl.kernel_units()
+    roof = {}
+    for k, t in tot.items():
+        if not t:
+            continue
+        if k.startswith("gemm"):
+            a = units[k] / (t * 1e-3) / 1e12
+            p = pk["bf16_tflops_sustained"] * (6.0 if k == "gemm_nvfp4" else 1.0)
+            roof[k] = {"bound": "tensor", "achieved": round(a, 1), "peak": round(p, 1), "unit": "TFLOP/s",
+                       "frac": round(a / p, 4), "launches": n[k], "ms": round(t, 3)}
+        else:
+            a = units[k] / (t * 1e-3) / 1e9
+            roof[k] = {"bound": "hbm", "achieved": round(a, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                       "frac": round(a / pk["hbm_gbs"], 4), "launches": n[k], "ms": round(t, 3)}
+            if k in moved:
+                roof[k]["moved_gbs"] = round(moved[k] / (t * 1e-3) / 1e9, 1)
+    return tot, roof
+
+
+def time_steps(wl, steps, warmup, world, barrier, dominant=None, clocks=None):
+    """Device-timed region (inputs resident in HBM): `steps` steps after `warmup` untimed ones,
+    CUDA events on the launching stream, max over ranks.  With `dominant`, that kernel type's
+    launches are event-timed inside the region as well."""
+    torch = wl.torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
         wl.step()
-
-    def barrier():
-        if world > 1:
-            tdist.barrier()
-        torch.cuda.synchronize()
-
-    # ---- device-timed region (inputs resident in HBM) ----
-    wl.timers = {dominant: []}
+    wl.timers = {dominant: []} if dominant else None
     barrier()
-    with Clocks(local_rank) as clk:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.nvtx.range_push("timed")
-        w0 = time.time()
-        e0.record(stream)
-        for _ in range(args.steps):
-            wl.step()
-        e1.record(stream)
-        torch.cuda.nvtx.range_pop()
-        e1.synchronize()
-        clk.mark(w0, time.time())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    e0.record(stream)
+    for _ in range(steps):
+        wl.step()
+    e1.record(stream)
+    e1.synchronize()
+    if clocks is not None:
+        clocks.mark(w0, time.time())
     barrier()
-    ms = e0.elapsed_time(e1) / args.steps
-    dom_ms = [a.elapsed_time(z) for a, z in wl.timers[dominant]]
+    ms = e0.elapsed_time(e1) / steps
+    dom_ms = [a.elapsed_time(z) for a, z in wl.timers[dominant]] if dominant else []
     wl.timers = None
-    ms = max_over_ranks(ms, world, dev)
+    return max_over_ranks(ms, world, wl.dev), dom_ms
 
-    # ---- end to end through the public API: host inputs in, results out ----
-    # Every step copies its inputs from pinned host memory and reads its result back.  The
-    # copies run on a second stream into one of two device buffer sets (ping-pong by step), in
-    # block order with one event per block: block b waits only for its own inputs, so the
-    # copies of later blocks (and of the next step) overlap the kernels of earlier ones.
-    host_in = {}
-    for s in range(2):
-        for name, t in wl.inputs[s].items():
-            host_in[(s, name)] = t.cpu().pin_memory()
-    host_pairs = [t.cpu().pin_memory() for t in wl.x_out] + [wl.x_in.cpu().pin_memory()]
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + \
-        sum(t.numel() * t.element_size() for t in host_pairs)
+
+def e2e_leg(wl, steps, world, barrier):
+    """The same metric end to end through the public API: every step copies its inputs from
+    pinned host memory (the linear inputs, every block's input/output pair) and reads its result
+    (the last FFN-down output, Gamma and the similarity of every block) back.  The copies run on
+    a second stream into one of two device buffer sets (ping-pong by step), in block order with
+    one event per block: block b waits only for its own inputs, so the copies of later blocks
+    (and of the next step) overlap the kernels of earlier ones."""
+    torch = wl.torch
+    dev = wl.dev
+    stream = torch.cuda.current_stream()
+    nb = wl.nblocks
+    host_in = {(s, name): t.cpu().pin_memory() for s in range(2) for name, t in wl.inputs[s].items()}
+    host_xi = [t.cpu().pin_memory() for t in wl.x_in]
+    host_xo = [t.cpu().pin_memory() for t in wl.x_out]
+    h2d = sum(t.numel() * t.element_size() for t in list(host_in.values()) + host_xi + host_xo)
     out_host = torch.empty_like(wl.y["ffn_down"], device="cpu").pin_memory()
-    g_host = torch.empty(2 * NBLOCKS, dtype=torch.float32).pin_memory()
+    g_host = torch.empty(2 * nb, dtype=torch.float32).pin_memory()
     d2h = out_host.numel() * out_host.element_size() + g_host.numel() * 4
-    slots = [{"inputs": wl.inputs, "x_out": wl.x_out, "x_in": wl.x_in},
+    orig = {"inputs": wl.inputs, "x_out": wl.x_out, "x_in": wl.x_in}
+    slots = [orig,
              {"inputs": [{k: torch.empty_like(v) for k, v in st.items()} for st in wl.inputs],
-              "x_out": [torch.empty_like(t) for t in wl.x_out], "x_in": torch.empty_like(wl.x_in)}]
+              "x_out": [torch.empty_like(t) for t in wl.x_out], "x_in": [torch.empty_like(t) for t in wl.x_in]}]
     copy_stream = torch.cuda.Stream(device=dev)
-    ready = [[torch.cuda.Event() for _ in range(NBLOCKS)] for _ in range(2)]
+    ready = [[torch.cuda.Event() for _ in range(nb)] for _ in range(2)]
     slot_free = [torch.cuda.Event() for _ in range(2)]
     for ev in slot_free:
         ev.record(stream)
@@ -592,46 +745,67 @@ def run_ours(args, rank, world, local_rank):
         sl = slots[k]
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(slot_free[k])      # the step that last read this slot is done
-            for b in range(NBLOCKS):
+            for b in range(nb):
                 if b < 2:
                     for name, t in sl["inputs"][b].items():
                         t.copy_(host_in[(b, name)], non_blocking=True)
-                if b == 0:
-                    sl["x_in"].copy_(host_pairs[-1], non_blocking=True)
-                sl["x_out"][b].copy_(host_pairs[b], non_blocking=True)
+                sl["x_in"][b].copy_(host_xi[b], non_blocking=True)
+                sl["x_out"][b].copy_(host_xo[b], non_blocking=True)
                 ready[k][b].record(copy_stream)
         wl.inputs, wl.x_out, wl.x_in = sl["inputs"], sl["x_out"], sl["x_in"]
         wl.step(before_block=lambda b: stream.wait_event(ready[k][b]))
         slot_free[k].record(stream)
         out_host.copy_(wl.y["ffn_down"], non_blocking=True)
-        g_host[:NBLOCKS].copy_(wl.gamma, non_blocking=True)
-        g_host[NBLOCKS:].copy_(wl.sim, non_blocking=True)
+        g_host[:nb].copy_(wl.gamma, non_blocking=True)
+        g_host[nb:].copy_(wl.sim, non_blocking=True)
         step_no[0] += 1
 
     e2e_step()
     barrier()
-    e_steps = max(1, min(args.steps, 3))
     t0 = time.perf_counter()
-    for _ in range(e_steps):
+    for _ in range(steps):
         e2e_step()
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / e_steps
-    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    ms = (time.perf_counter() - t0) * 1e3 / steps
+    wl.inputs, wl.x_out, wl.x_in = orig["inputs"], orig["x_out"], orig["x_in"]
+    del slots, host_in, host_xi, host_xo
+    torch.cuda.empty_cache()
+    return max_over_ranks(ms, world, dev), int(h2d), int(d2h)
 
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as tdist
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pk, src = peaks()
+
+    def barrier():
+        if world > 1:
+            tdist.barrier()
+        torch.cuda.synchronize()
+
+    wl = Workload(dev, seed=1234 + rank, name=args.workload)
+    wl.step()                                   # first warm-up step
+    tot, kern_roof = instrumented_kernels(wl, pk)   # second warm-up step, every launch timed
+    dominant = max(tot, key=tot.get)
+    with Clocks(local_rank) as clk:
+        ms, dom_ms = time_steps(wl, args.steps, max(0, args.warmup - 2), world, barrier, dominant, clk)
+    e2e_ms, h2d, d2h = e2e_leg(wl, max(1, min(args.steps, 3)), world, barrier)
+
+    extras = {}
+    if not args.no_nvfp4_only and rank == 0:
+        extras["nvfp4_only_weights"] = run_nvfp4_only_weights(wl)
     if rank != 0:
         return
-    pk, src = peaks()
-    units = wl.kernel_units()
+    units, moved = wl.kernel_units()
     avg_ms = sum(dom_ms) / len(dom_ms)
     n_launch_step = len(dom_ms) / args.steps
     unit_per_launch = units[dominant] / n_launch_step
     if dominant.startswith("gemm"):
         achieved = unit_per_launch / (avg_ms * 1e-3) / 1e12
-        if dominant == "gemm_int8" and wl.int8_code_bytes == 1:
-            peak = int8_ceiling(torch, dev)
-            peak_note = "measured cuBLASLt INT8 GEMM (torch._int_mm 8192^3) in this run"
-        elif dominant == "gemm_int8":
+        if dominant == "gemm_int8":
             peak = pk["bf16_tflops_sustained"]
             peak_note = (f"{src} bf16 sustained: the INT8 codes run exactly on the bf16 tensor pipe "
                          "(sm_103a has no tcgen05 integer MMA)")
@@ -643,60 +817,56 @@ def run_ours(args, rank, world, local_rank):
                 "peak_source": peak_note}
     else:
         achieved = unit_per_launch / (avg_ms * 1e-3) / 1e9
-        peak = pk["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": measured_traffic(dominant), "kernel": dominant,
-                "peak_source": f"{src} HBM copy"}
-    kern_times = {k: round(v, 3) for k, v in tot.items()}
-    hbm = {k: round(units[k] / (tot[k] * 1e-3) / 1e9, 1) for k in ("quant_int8", "quant_nvfp4", "tdc_commit")
-           if tot.get(k)}
-    # every kernel type against its own bound (event-timed launches of one instrumented step)
-    kern_roof = {}
-    for k, t in tot.items():
-        if not t:
-            continue
-        if k.startswith("gemm"):
-            a = units[k] / (t * 1e-3) / 1e12
-            if k == "gemm_int8" and wl.int8_code_bytes == 1:   # int8-held codes run on IMMA
-                p = peak if dominant == "gemm_int8" else int8_ceiling(torch, dev)
-            else:
-                p = pk["bf16_tflops_sustained"] * (6.0 if k == "gemm_nvfp4" else 1.0)
-            kern_roof[k] = {"bound": "tensor", "achieved": round(a, 1), "peak": round(p, 1), "unit": "TFLOP/s",
-                            "frac": round(a / p, 4)}
-        else:
-            a = units[k] / (t * 1e-3) / 1e9
-            kern_roof[k] = {"bound": "hbm", "achieved": round(a, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                            "frac": round(a / pk["hbm_gbs"], 4)}
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": measured_traffic(dominant),
+                "kernel": dominant, "peak_source": f"{src} HBM copy"}
     value = aggregate_value(wl.flops_step, world, ms)
     e2e_val = aggregate_value(wl.flops_step, world, e2e_ms)
     routes_flat = [r for rr in wl.routes for r in rr]
+    spec = wl.spec
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "nvfp4 (e2m1+e4m3) and int8 codes (int32-exact on the bf16 tensor pipe), bf16 activations",
-        "data": "synthetic (seeded; CogVideoX-2B-shaped activations with outlier channels, N(0,0.02) weights)",
-        "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN, "blocks": NBLOCKS,
-                   "hadamard_block": HBLOCK, "gamma": "U(0,0.2)", "thr": THR,
-                   "int8_layers": routes_flat.count(1), "nvfp4_layers": routes_flat.count(0),
-                   "l2": "inputs larger than L2 (68-273 MB per tensor, two alternating sets)",
+        "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1+e4m3) and int8 codes (int32-exact on the bf16 tensor pipe), bf16 activations",
+        "data": "synthetic (seeded; CogVideoX-shaped activations with outlier channels, N(0,0.02) weights)",
+        "config": {"workload": wl.name, "tokens": spec["tokens"], "hidden": spec["hidden"], "ffn": spec["ffn"],
+                   "blocks": wl.nblocks, "activations": spec["activations"], "hadamard_block": HBLOCK,
+                   "gamma": "U(0,0.2)", "thr": THR, "int8_layers": routes_flat.count(1),
+                   "nvfp4_layers": routes_flat.count(0),
+                   "l2": ("inputs larger than L2 in aggregate: each block reads its own input/output pair and one of "
+                          "two alternating input sets; a step streams tens of GB, so nothing of the previous step "
+                          "is L2-resident when the next starts (no flush)"),
                    "parallelism": f"replicas{world}"},
         "roofline": roof,
-        "kernel_ms_per_step": kern_times,
-        "hbm_gbs_algorithmic": hbm,
+        "kernel_ms_per_step": {k: round(v, 3) for k, v in tot.items()},
         "kernel_roofline": kern_roof,
-        "e2e": {"value": round(e2e_val, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 3), "steps": e_steps,
-                "copies": "pinned host -> device on a copy stream into ping-pong device buffers, one event "
-                          "per block; results read back after each step"},
+        "e2e": {"value": round(e2e_val, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 3),
+                "copies": "pinned host -> device on a copy stream into ping-pong device buffers, one event per "
+                          "block; results read back after each step"},
         "gpu_launches": int(wl.launches_per_step() * args.steps),
         "clocks": clk.summary(),
     }
-    if not args.no_large_shapes:
-        line["large_shapes_1080p"] = run_large_shapes(dev)
-    if not args.no_nvfp4_only:
-        line["nvfp4_only_weights"] = run_nvfp4_only_weights(wl)
-    if not args.no_tdc_loop:
-        line["tdc_loop"] = run_tdc_loop(wl, steps=args.tdc_steps)
+    line.update(extras)
+    wl.free()
+    del wl
+    if not args.no_2b:
+        w2 = Workload(dev, seed=4321, name="cogvideox_2b_block_linears")
+        w2.step()
+        tot2, roof2 = instrumented_kernels(w2, pk)
+        ms2, _ = time_steps(w2, max(3, args.steps // 2), 1, 1, lambda: torch.cuda.synchronize())
+        line["cogvideox_2b_step"] = {"value": round(w2.flops_step / (ms2 * 1e-3) / 1e12, 3), "unit": UNIT,
+                                     "ms_per_step": round(ms2, 3), "blocks": w2.nblocks,
+                                     "int8_layers": sum(r.count(1) for r in w2.routes),
+                                     "nvfp4_layers": sum(r.count(0) for r in w2.routes),
+                                     "kernel_roofline": roof2}
+        if not args.no_tdc_loop:
+            line["tdc_loop"] = run_tdc_loop(w2, steps=args.tdc_steps, replay_blocks=args.tdc_replay_blocks)
+        w2.free()
+        del w2
+    if not args.no_long:
+        line["long_1080p"] = run_long_1080p(dev)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -710,17 +880,18 @@ def run_ours(args, rank, world, local_rank):
 _PREP = {}
 
 
-def _oracle_weights():
+def _oracle_weights(spec):
     """Both routes' weights of one block, prepared once by the oracle (untimed)."""
-    if not _PREP:
+    key = spec["hidden"]
+    if key not in _PREP:
         import synth
         from oracle import dmpq as D
-        for name, k, n in LINEARS:
-            _PREP[name] = D.prepare_weight(synth.weights(n, k, seed=5000 + n + k), HBLOCK)
-    return _PREP
+        _PREP[key] = {name: D.prepare_weight(synth.weights(n, k, seed=5000 + n + k), HBLOCK)
+                      for name, k, n in linears(spec)}
+    return _PREP[key]
 
 
-def oracle_sample(tokens: int, seed: int):
+def oracle_sample(tokens: int, seed: int, workload: str = DEFAULT_WORKLOAD):
     """The oracle on a token sample of one block: the four routed linears (alternating
     routes; the FFN-down input is the bf16 GELU of the FFN-up output) + the delta commit.
     Returns (seconds, flops)."""
@@ -729,14 +900,16 @@ def oracle_sample(tokens: int, seed: int):
     from oracle import dmpq as D
     from oracle import formats as F
     from oracle import tdc as T
-    preps = _oracle_weights()
-    xs = {name: synth.activations(tokens, k, seed=seed + i, dtype="f32")
-          for i, (name, k, _) in enumerate(LINEARS) if name != "ffn_down"}
-    xi = synth.activations(tokens, HIDDEN, seed=seed + 9)
+    spec = WORKLOADS[workload]
+    preps = _oracle_weights(spec)
+    act = lambda k, s, dtype: synth.activations(tokens, k, dist=spec["dist"], outlier_frac=spec["outlier_frac"],
+                                                outlier_mult=spec["outlier_mult"], seed=s, dtype=dtype)
+    xs = {name: act(k, seed + i, "f32") for i, (name, k, _) in enumerate(linears(spec)) if name != "ffn_down"}
+    xi = act(spec["hidden"], seed + 9, "bf16")
     xo = synth.gamma_pair(xi, 0.1, seed + 10)
     flops = 0
     t0 = time.perf_counter()
-    for i, (name, k, n) in enumerate(LINEARS):
+    for i, (name, k, n) in enumerate(linears(spec)):
         route = D.ROUTE_INT8 if i % 2 == 0 else D.ROUTE_NVFP4
         y = D.routed_linear(xs[name], preps[name], HBLOCK, route)
         if name == "ffn_up":
@@ -746,18 +919,18 @@ def oracle_sample(tokens: int, seed: int):
     return time.perf_counter() - t0, flops
 
 
-def cpu_baseline(seconds_budget: float = 15.0):
+def cpu_baseline(seconds_budget: float = 15.0, workload: str = DEFAULT_WORKLOAD):
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    tokens, total_t, total_f, reps = 64, 0.0, 0, 0
+    tokens, total_t, total_f, reps = 32, 0.0, 0, 0
     while total_t < seconds_budget and reps < 50:
-        t, f = oracle_sample(tokens, seed=reps)
+        t, f = oracle_sample(tokens, seed=reps, workload=workload)
         total_t += t
         total_f += f
         reps += 1
         if t < 1.0 and tokens < 2048:
             tokens *= 2
     return {"value": round(total_f / total_t / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{reps} oracle passes over one CogVideoX-2B block (4 routed linears, both routes, GELU "
+            "sample": f"{reps} oracle passes over one {workload} block (4 routed linears, both routes, GELU "
                       f"+ delta commit) on token samples up to {tokens} tokens; weight preparation untimed; "
                       f"{total_t:.1f} s of CPU work (numpy float64 BLAS on all cores)"}
 
@@ -765,23 +938,24 @@ def cpu_baseline(seconds_budget: float = 15.0):
 def run_reference(args, rank, world):
     if rank != 0:
         return
+    workload = getattr(args, "workload", DEFAULT_WORKLOAD)
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    tokens = 128
+    tokens = 64
     for _ in range(max(0, args.warmup)):
-        oracle_sample(32, seed=1)
+        oracle_sample(16, seed=1, workload=workload)
     total_t, total_f = 0.0, 0
     for s in range(args.steps):
-        t, f = oracle_sample(tokens, seed=100 + s)
+        t, f = oracle_sample(tokens, seed=100 + s, workload=workload)
         total_t += t
         total_f += f
     v = total_f / total_t / 1e12
-    sample = (f"each step: the oracle over one CogVideoX-2B block (4 routed linears, both routes, GELU, + delta "
+    sample = (f"each step: the oracle over one {workload} block (4 routed linears, both routes, GELU, + delta "
               f"commit) on a {tokens}-token sample; weight preparation untimed")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_t * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/int64 (CPU oracle)",
-        "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "tokens_sample": tokens},
+        "data": "synthetic (seeded)", "config": {"workload": workload, "tokens_sample": tokens},
         "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -790,15 +964,18 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-2b", action="store_true", help="skip the CogVideoX-2B step (and with it the TDC loop)")
     ap.add_argument("--no-tdc-loop", action="store_true")
-    ap.add_argument("--no-nvfp4-only", action="store_true", help="skip the NVFP4-only-weights variant")
-    ap.add_argument("--no-large-shapes", action="store_true", help="skip the 1080p-shaped GEMM timings")
     ap.add_argument("--tdc-steps", type=int, default=50)
+    ap.add_argument("--tdc-replay-blocks", type=int, default=2)
+    ap.add_argument("--no-nvfp4-only", action="store_true", help="skip the NVFP4-only-weights variant")
+    ap.add_argument("--no-long", action="store_true", help="skip the 1080p-shaped path")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -138,10 +138,16 @@ def e4m3_rounding_margin(v: np.ndarray) -> np.ndarray:
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """float32 -> bf16 bit pattern, round to nearest even (finite inputs)."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    lsb = (u >> np.uint64(16)) & np.uint64(1)
-    r = (u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
+    """float32 -> bf16 bit pattern, round to nearest even (finite inputs).
+
+    Adding 0x7FFF plus the lowest kept bit to the float32 pattern and dropping the low 16
+    bits rounds half to even.  For finite inputs the sum stays below 2^32 (the largest finite
+    pattern is 0xFF7FFFFF), so the arithmetic is exact in uint32."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = (u >> np.uint32(16)) & np.uint32(1)
+    r += u
+    r += np.uint32(0x7FFF)
+    r >>= np.uint32(16)
     return r.astype(np.uint16)
 
 

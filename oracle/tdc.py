@@ -120,40 +120,59 @@ def compute_routes(state: TdcState, alpha, beta, thr) -> list[int]:
     return route_layers(state.gamma_prev, alpha, beta, thr)
 
 
+class BlockLoop:
+    """One block driven through denoising steps one step at a time (synthetic block).
+
+    A computed step's output is x_in + delta_true (no trained block exists, the delta is
+    given).  ``step`` returns the decision, the routes of a compute step (None on a skip), the
+    Gamma it was routed with (None when missing), the decision margin and the step's output
+    (None on a skip unless ``want_skip_output``).
+    """
+
+    def __init__(self, tau, alpha, beta, thr, dtype="bf16"):
+        self.tau, self.alpha, self.beta, self.thr, self.dtype = tau, alpha, beta, thr, dtype
+        self.st = TdcState()
+        self.d1 = None
+
+    def step(self, x_in, delta_true, want_skip_output: bool = True) -> dict:
+        st, dtype = self.st, self.dtype
+        dec = tdc_decide(st, self.tau)
+        margin = decision_margin(st, self.tau)
+        if dec == SKIP:
+            out = tdc_skip(x_in, self.d1, dtype) if want_skip_output else None
+            tdc_apply(st, SKIP)
+            return {"decision": dec, "routes": None, "gamma": None, "margin": margin, "out": out}
+        r = compute_routes(st, self.alpha, self.beta, self.thr)
+        g = st.gamma_prev
+        xo = _store((_as_f32(x_in, dtype) + _as_f32(delta_true, dtype)).astype(np.float32), dtype)
+        c = tdc_commit(x_in, xo, self.d1, dtype)
+        self.d1 = c["delta"]
+        tdc_apply(st, COMPUTE, c)
+        return {"decision": dec, "routes": r, "gamma": g, "margin": margin, "out": xo}
+
+
 def run_block_loop(x_in_seq, delta_true_seq, tau, alpha, beta, thr, dtype="bf16") -> dict:
     """Drive one block through a sequence of denoising steps (synthetic block).
 
     ``x_in_seq[t]`` is the block input at step t; a computed step's output is
-    x_in + delta_true_seq[t] (no trained block exists, the delta is given).  Returns the
-    decision sequence, the routes of every compute step, the Gamma each compute step was
-    routed with (None when missing), per-step outputs and decision margins.
+    x_in + delta_true_seq[t].  Returns the decision sequence, the routes of every compute
+    step, the Gamma each compute step was routed with (None when missing), per-step outputs
+    and decision margins.
     """
-    st = TdcState()
-    d1 = None
+    loop = BlockLoop(tau, alpha, beta, thr, dtype)
     decisions, routes, outs, margins, gammas = [], [], [], [], []
-    for t, (xi, dt) in enumerate(zip(x_in_seq, delta_true_seq)):
-        dec = tdc_decide(st, tau)
-        margins.append(decision_margin(st, tau))
-        decisions.append(dec)
-        if dec == SKIP:
-            routes.append(None)
-            gammas.append(None)
-            outs.append(tdc_skip(xi, d1, dtype))
-            tdc_apply(st, SKIP)
-            continue
-        r = compute_routes(st, alpha, beta, thr)
-        routes.append(r)
-        gammas.append(st.gamma_prev)
-        xo = _store((_as_f32(xi, dtype) + _as_f32(dt, dtype)).astype(np.float32), dtype)
-        c = tdc_commit(xi, xo, d1, dtype)
-        d1 = c["delta"]
-        outs.append(xo)
-        tdc_apply(st, COMPUTE, c)
+    for xi, dt in zip(x_in_seq, delta_true_seq):
+        r = loop.step(xi, dt)
+        decisions.append(r["decision"])
+        routes.append(r["routes"])
+        gammas.append(r["gamma"])
+        margins.append(r["margin"])
+        outs.append(r["out"])
     return {"decisions": decisions, "routes": routes, "outs": outs, "margins": margins,
             "gammas": gammas}
 
 
 __all__ = [
     "COMPUTE", "SKIP", "ROUTE_INT8", "TdcState", "tdc_commit", "tdc_skip", "tdc_decide",
-    "tdc_apply", "compute_routes", "decision_margin", "run_block_loop",
+    "tdc_apply", "compute_routes", "decision_margin", "BlockLoop", "run_block_loop",
 ]

@@ -99,20 +99,26 @@ def gamma_pair(x_in_bits: np.ndarray, gamma_target: float, seed: int) -> np.ndar
     return to_bf16_bits(xi + np.float32(gamma_target) * s * xi)
 
 
-def tdc_deltas(steps: int, rows: int, k: int, *, seed: int, jump_every: float = 8.0,
-               eps_std: float = 0.01, jump_std: float = 0.5) -> tuple[list[np.ndarray], list[bool]]:
-    """Per-step true deltas of one block: Delta_0 ~ N(0, sigma), sigma ~ U(0.02, 0.15);
-    Delta_t = Delta_{t-1} * (1 + eps), eps ~ N(0, 0.01) elementwise, and N(0, 0.5) on jump
-    steps (Bernoulli(1/jump_every)).  Returned as bf16 bits."""
+def tdc_delta_stream(steps: int, rows: int, k: int, *, seed: int, jump_every: float = 8.0,
+                     eps_std: float = 0.01, jump_std: float = 0.5):
+    """Per-step true deltas of one block, one step at a time: Delta_0 ~ N(0, sigma), sigma ~
+    U(0.02, 0.15); Delta_t = Delta_{t-1} * (1 + eps), eps ~ N(0, 0.01) elementwise, and
+    N(0, 0.5) on jump steps (Bernoulli(1/jump_every)).  Yields (bf16 bits, jump) pairs."""
     g = rng(seed)
     sigma = g.uniform(0.02, 0.15)
     d = (g.standard_normal((rows, k), dtype=np.float32) * np.float32(sigma)).astype(np.float32)
-    out, jumps = [to_bf16_bits(d)], [False]
+    yield to_bf16_bits(d), False
     for _ in range(1, steps):
         jump = bool(g.random() < 1.0 / jump_every)
         std = jump_std if jump else eps_std
         eps = g.standard_normal((rows, k), dtype=np.float32) * np.float32(std)
         d = (d * (np.float32(1.0) + eps)).astype(np.float32)
-        out.append(to_bf16_bits(d))
-        jumps.append(jump)
-    return out, jumps
+        yield to_bf16_bits(d), jump
+
+
+def tdc_deltas(steps: int, rows: int, k: int, *, seed: int, jump_every: float = 8.0,
+               eps_std: float = 0.01, jump_std: float = 0.5) -> tuple[list[np.ndarray], list[bool]]:
+    """All steps of tdc_delta_stream at once: (list of bf16 bits, list of jump flags)."""
+    pairs = list(tdc_delta_stream(steps, rows, k, seed=seed, jump_every=jump_every, eps_std=eps_std,
+                                  jump_std=jump_std))
+    return [p[0] for p in pairs], [p[1] for p in pairs]
