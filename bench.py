@@ -696,11 +696,13 @@ def time_steps(wl, steps, warmup, world, barrier, dominant=None, clocks=None):
     wl.timers = {dominant: []} if dominant else None
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
     w0 = time.time()
     e0.record(stream)
     for _ in range(steps):
         wl.step()
     e1.record(stream)
+    torch.cuda.nvtx.range_pop()
     e1.synchronize()
     if clocks is not None:
         clocks.mark(w0, time.time())

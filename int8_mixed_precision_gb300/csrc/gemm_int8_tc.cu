@@ -23,6 +23,9 @@ namespace i8tc {
 constexpr int BK = 64;             // BK bf16 elements = 128 bytes per row
 constexpr int KCHUNK_BLOCKS = 16;  // 16 x 64 = 1024 elements per exact chunk
 constexpr int A_BYTES = 128 * BK * 2;
+#ifndef I8_BAND_BYTES
+#define I8_BAND_BYTES (24ll << 20)
+#endif
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   uint64_t d = 0;
@@ -91,12 +94,14 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
 //         summed in fp32 and the output is the same bit for bit without the int32 round trip.
 // ACCM 2: a plain bf16 GEMM (the BF16 route of PDR): fp32 accumulation over the whole K in one
 //         tensor-memory chunk, no scales.
-template <bool GELU, int ACCM>
+// BANDED: the tile order in bands of N tiles (see tile_mn); a separate instantiation, so that the
+// shapes that keep the plain order run exactly the code they always ran.
+template <bool GELU, int ACCM, bool BANDED>
 __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     k_gemm_int8_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N, int K,
                      const float* __restrict__ bias, void* __restrict__ y, int epi, int32_t* __restrict__ acc_out,
-                     void* ws, int stall) {
+                     void* ws, int stall, int band) {
   using P = PairCfg;
   constexpr int S = P::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -115,10 +120,25 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();  // 0: the leader, which issues the pair's MMAs
   const int n_tiles_n = (N + 255) / 256;
-  const int n_items = ((M + 255) / 256) * n_tiles_n;
+  const int m_tiles = (M + 255) / 256;
+  const int n_items = m_tiles * n_tiles_n;
   const int first_item = blockIdx.x >> 1, item_step = gridDim.x >> 1;
-  auto tile_m0 = [&](int item) { return (item / n_tiles_n) * 256; };
-  auto tile_n0 = [&](int item) { return (item % n_tiles_n) * 256; };
+  // Tile order: N fastest.  BANDED: bands of `band` N tiles, each band walked over all M tiles
+  // (N fastest inside the band), so the band's slice of B stays in L2 while A streams through
+  // once per band.
+  auto tile_mn = [&](int item, int& m0, int& n0) {
+    if constexpr (BANDED) {
+      const int per_band = band * m_tiles;
+      const int b = item / per_band;
+      const int r = item - b * per_band;
+      const int w = min(band, n_tiles_n - b * band);
+      m0 = (r / w) * 256;
+      n0 = (b * band + r % w) * 256;
+    } else {
+      m0 = (item / n_tiles_n) * 256;
+      n0 = (item % n_tiles_n) * 256;
+    }
+  };
   const int nkb = (K + BK - 1) / BK;
   // exactness chunks of the INT8 modes; the bf16 mode accumulates all of K in one chunk
   const int kchunk = ACCM == 2 ? nkb : KCHUNK_BLOCKS;
@@ -157,7 +177,10 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
       uint32_t kc = 0;
       bool ok = true;
       for (int item = first_item; item < n_items && ok; item += item_step) {
-        const int m0 = tile_m0(item) + (int)rank * 128, n0 = tile_n0(item) + (int)rank * 128;
+        int m0, n0;
+        tile_mn(item, m0, n0);
+        m0 += (int)rank * 128;
+        n0 += (int)rank * 128;
         for (int kb = 0; kb < nkb; ++kb, ++kc) {
           const int s = kc % S;
           if (!mbar_wait_cl(empty(s), ((kc / S) & 1) ^ 1, ws, abort_flag)) {
@@ -222,7 +245,9 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     uint32_t cc = 0;
     bool ok = true;
     for (int item = first_item; item < n_items && ok; item += item_step) {
-      const int m0 = tile_m0(item) + (int)rank * 128, n0 = tile_n0(item);
+      int m0, n0;
+      tile_mn(item, m0, n0);
+      m0 += (int)rank * 128;
       constexpr int CW = P::CW;
       int acc[CW];
 #pragma unroll
@@ -352,18 +377,44 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
   }
 }
 
+template <bool GELU, int ACCM, bool BANDED>
+dit_status launch_pair_k(const CUtensorMap& ta, const CUtensorMap& tb, const float* a_scale, const float* b_scale,
+                         int64_t m, int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
+                         void* ws, cudaStream_t st, int band);
+
 template <bool GELU, int ACCM>
 dit_status launch_pair(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
                        int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out, void* ws,
                        cudaStream_t st) {
-  using P = PairCfg;
   CUtensorMap ta, tb;
   if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(a), (uint64_t)k, (uint64_t)m,
                       (uint64_t)k * 2, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(b), (uint64_t)k, (uint64_t)n,
                       (uint64_t)k * 2, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return DIT_ERR_CUDA;
-  auto kern = k_gemm_int8_pair<GELU, ACCM>;
+  // N tiles per band: as many as keep the band's slice of B (256 rows x K bf16 each) within
+  // I8_BAND_BYTES, a share of one die's half of the L2 that leaves room for the A rows and the
+  // output streaming through.  Measured on GB300 (CogVideoX-5B shapes, K = 3072): FFN-up
+  // 784 -> 741 us with DRAM reads of 1.87 -> 0.42 GB per launch, QKV 530 -> 519 us with 0.74 ->
+  // 0.40 GB; for K >= 7680 the plain order was ~1 % faster, so bands are used up to K = 4096.
+  const int64_t n_tiles = (n + 255) / 256;
+  int64_t band = I8_BAND_BYTES / (256 * 2 * k);
+  if (band < 1) band = 1;
+  if constexpr (ACCM != 2) {
+    if (k <= 4096 && band < n_tiles)
+      return launch_pair_k<GELU, ACCM, true>(ta, tb, a_scale, b_scale, m, n, k, bias, y, epi, acc_out, ws, st,
+                                             (int)band);
+  }
+  return launch_pair_k<GELU, ACCM, false>(ta, tb, a_scale, b_scale, m, n, k, bias, y, epi, acc_out, ws, st,
+                                          (int)n_tiles);
+}
+
+template <bool GELU, int ACCM, bool BANDED>
+dit_status launch_pair_k(const CUtensorMap& ta, const CUtensorMap& tb, const float* a_scale, const float* b_scale,
+                         int64_t m, int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
+                         void* ws, cudaStream_t st, int band) {
+  using P = PairCfg;
+  auto kern = k_gemm_int8_pair<GELU, ACCM, BANDED>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES) != cudaSuccess)
@@ -389,7 +440,7 @@ dit_status launch_pair(const void* a, const float* a_scale, const void* b, const
   if (pairs > items) pairs = items;
   cfg.gridDim = dim3((unsigned)(2 * pairs));
   if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, epi, acc_out, ws,
-                         test_stall()) != cudaSuccess)
+                         test_stall(), band) != cudaSuccess)
     return DIT_ERR_CUDA;
   return DIT_OK;
 }

@@ -20,10 +20,6 @@
 //               pipe), then arrive on the stage's sf_ready barrier;
 //   the rest  : epilogue -- tcgen05.ld of the accumulator, global scale (+bias, GELU),
 //               bf16/fp32 conversion, 256-bit stores; optionally the output's Hadamard amax.
-// On 128 x 256 tiles the accumulator is handed over in two 128-column halves: the last K stage
-// of a tile and the first of the next run as two N = 128 MMAs per K step, half 0 first, so the
-// epilogue drains half 0 while half 1 finishes, and the next tile starts in half 0 while half
-// 1 is drained.  The tensor pipe no longer idles for a whole accumulator drain per tile.
 // Every mbarrier wait is bounded (%globaltimer); on expiry the CTA records
 // DIT_ERR_TIMEOUT in the workspace, lets in-flight copies and MMAs land, frees its tensor
 // memory and exits.
@@ -109,7 +105,6 @@ __device__ __forceinline__ void tc_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]
 template <int BN, int STAGES, int CTAS, int EPW = 0>
 struct SCfg {
   static constexpr int NB = BN / 128;
-  static constexpr int NH = BN / 128;                 // accumulator halves handed over separately
   static constexpr int B_BYTES = BN * BK / 2;
   static constexpr int SFA_BYTES = 4 * SF_ATOM;
   static constexpr int SFB_BYTES = NB * 4 * SF_ATOM;
@@ -124,7 +119,6 @@ struct SCfg {
   static constexpr int THREADS = (2 + EPI_WARPS + 4) * 32;
   static_assert(TMEM_USED <= 512 / CTAS, "tensor memory");
   static_assert(SMEM_BYTES * CTAS <= 232448, "shared memory");
-  static_assert(NH == 1 || EPI_WARPS % 8 == 0, "each accumulator half has its own epilogue warps");
 };
 
 // Epilogue of 32 accumulator columns of one output row: Y = acc * (s_gA s_gB) (+ bias), then
@@ -231,20 +225,19 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
   static_assert(AHB == 0 || EPW != 0, "the output's Hadamard amax needs the 64-column epilogue warps");
   using C = SCfg<BN, STAGES, CTAS, EPW>;
   constexpr int S = STAGES;
-  constexpr int NH = C::NH;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::STAGE_BYTES);
-  // bars: full[S], empty[S], sf_ready[S], acc_full[NH], acc_empty[NH], mma_done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 2 * NH + 1);
+  // bars: full[S], empty[S], sf_ready[S], acc_full, acc_empty, mma_done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t sbase = smem_u32(smem);
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto empty = [&](int s) { return smem_u32(bars + S + s); };
   auto sf_ready = [&](int s) { return smem_u32(bars + 2 * S + s); };
-  auto afull = [&](int h) { return smem_u32(bars + 3 * S + h); };
-  auto aempty = [&](int h) { return smem_u32(bars + 3 * S + NH + h); };
-  const uint32_t mma_done = smem_u32(bars + 3 * S + 2 * NH);
+  const uint32_t afull = smem_u32(bars + 3 * S);
+  const uint32_t aempty = smem_u32(bars + 3 * S + 1);
+  const uint32_t mma_done = smem_u32(bars + 3 * S + 2);
   auto a_tile = [&](int s) { return sbase + s * C::STAGE_BYTES; };
   auto b_tile = [&](int s) { return a_tile(s) + A_BYTES; };
   auto sfa_tile = [&](int s) { return smem + s * C::STAGE_BYTES + A_BYTES + C::B_BYTES; };
@@ -263,10 +256,8 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
       mbar_init(empty(s), 1);
       mbar_init(sf_ready(s), 4);
     }
-    for (int h = 0; h < NH; ++h) {
-      mbar_init(afull(h), 1);
-      mbar_init(aempty(h), C::EPI_WARPS / NH);
-    }
+    mbar_init(afull, 1);
+    mbar_init(aempty, C::EPI_WARPS);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -318,19 +309,12 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
   } else if (warp == 1) {  // ------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_nvf4(BM, BN);
-      constexpr uint32_t idesc_half = idesc_nvf4(BM, 128);
       uint32_t kc = 0, tc = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
-        const uint32_t aphase = (tc & 1) ^ 1;  // the epilogue released the previous tile's accumulator
-        // a tile whose columns all fall in half 0 (the last N tile when N % 256 <= 128) runs only
-        // half 0's MMAs; half 1's barriers still turn over once per tile
-        const bool narrow = NH == 2 && N - (tile % n_tiles_n) * BN <= 128;
-        if (NH == 1) {
-          if (!mbar_wait(aempty(0), aphase, ws, abort_flag)) break;
-          tc_fence_after();
-        }
-        for (int kb = 0; kb < num_kb && ok; ++kb, ++kc) {
+        if (!mbar_wait(aempty, (tc & 1) ^ 1, ws, abort_flag)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb, ++kc) {
           const int s = kc % S;
           if (!mbar_wait(full(s), (kc / S) & 1, ws, abort_flag) ||
               !mbar_wait(sf_ready(s), (kc / S) & 1, ws, abort_flag)) {
@@ -339,36 +323,14 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
           }
           tc_fence_after();
           const int nsub = min(4, ksteps - kb * 4);
-          const bool first = kb == 0, last = kb == num_kb - 1;
-          const uint32_t sf0 = tmem + C::SF_BASE + s * 4 * C::SF_COLS;
-          if (NH == 2 && (first || last || narrow)) {
-            // accumulator hand-off: half 0 (columns 0-127, B rows 0-127) then half 1
-            for (int h = 0; h < 2 && ok; ++h) {
-              if (first) {
-                if (!mbar_wait(aempty(h), aphase, ws, abort_flag)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-              }
-              for (int j = 0; j < nsub && (h == 0 || !narrow); ++j) {
-                const uint32_t sfa_col = sf0 + j * C::SF_COLS;
-                tc_mma(tmem + h * 128, desc_sw128(a_tile(s) + j * 32), desc_sw128(b_tile(s) + h * 16384 + j * 32),
-                       idesc_half, sfa_col, sfa_col + 4 + 4 * h, (kb | j) != 0 ? 1u : 0u);
-              }
-              if (last) tc_commit(afull(h));
-            }
-            if (!ok) break;
-          } else {
-            for (int j = 0; j < nsub; ++j) {
-              const uint32_t sfa_col = sf0 + j * C::SF_COLS;
-              tc_mma(tmem, desc_sw128(a_tile(s) + j * 32), desc_sw128(b_tile(s) + j * 32), idesc, sfa_col,
-                     sfa_col + 4, (kb | j) != 0 ? 1u : 0u);
-            }
-            if (NH == 1 && last) tc_commit(afull(0));
+          for (int j = 0; j < nsub; ++j) {
+            const uint32_t sfa_col = C::SF_BASE + (s * 4 + j) * C::SF_COLS;
+            tc_mma(tmem, desc_sw128(a_tile(s) + j * 32), desc_sw128(b_tile(s) + j * 32), idesc, tmem + sfa_col,
+                   tmem + sfa_col + 4, (kb | j) != 0 ? 1u : 0u);
           }
           tc_commit(empty(s));
         }
+        if (ok) tc_commit(afull);
       }
       tc_commit(mma_done);
       volatile int no_abort = 0;
@@ -417,20 +379,19 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
   } else {  // ----------------------------------------------------- epilogue warps
     const int e = warp - 2;
     const int q = warp & 3;
-    const int half = e >> 2;                        // 128-column half (EPW = 0, BN = 256)
-    const int hh = NH == 2 ? e / (C::EPI_WARPS / 2) : 0;  // the accumulator half this warp drains
+    const int half = e >> 2;  // 128-column half of the tile (EPW = 0, BN = 256)
     const float alpha = __fmul_rn(*a_gs, *b_gs);
     float q_amax = 0.f;
     uint32_t tc = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tc) {
       const int m0 = (tile / n_tiles_n) * BM, n0 = (tile % n_tiles_n) * BN;
-      if (!mbar_wait(afull(hh), tc & 1, ws, abort_flag)) break;
+      if (!mbar_wait(afull, tc & 1, ws, abort_flag)) break;
       tc_fence_after();
       const int row = m0 + q * 32 + lane;
       const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
       if constexpr (EPW != 0) {
         // sixteen epilogue warps, 64 columns each: load the raw accumulator words, release the
-        // accumulator half, then scale, add the bias, apply the activation and store -- all of
+        // accumulator, then scale, add the bias, apply the activation and store -- all of
         // the epilogue's arithmetic overlaps the next tile's MMAs
         const int part = e >> 2;  // 64-column quarter of the 256-column tile
         uint32_t r0[32], r1[32];
@@ -439,7 +400,7 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(aempty(hh));
+        if (lane == 0) mbar_arrive(aempty);
         const int col0 = n0 + part * 64;
         if constexpr (AHB > 0) {
           if (row < M && col0 < N) {  // N % 64 == 0: the 64 columns are one transform unit
@@ -464,12 +425,12 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
           epi_store32(r0, alpha, row, col0, M, N, bias, y, epi);
           epi_store32(r1, alpha, row, col0 + 32, M, N, bias, y, epi);
         }
-        continue;  // the accumulator half is already released
+        continue;  // the accumulator is already released
       }
       if constexpr (CTAS == 1) {
       if (epi & EPI_BF16) {
         // one CTA per SM: convert the thread's 128 columns to packed bf16 in registers, release
-        // the accumulator half, then store -- the next tile's MMAs overlap the stores
+        // the accumulator, then store -- the next tile's MMAs overlap the stores
         uint32_t pk[4][16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -495,7 +456,7 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(aempty(hh));
+        if (lane == 0) mbar_arrive(aempty);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int col0 = n0 + half * 128 + c * 32;
@@ -517,7 +478,7 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
               if (col0 + i < N) yp[i] = (uint16_t)(pk[c][i >> 1] >> (16 * (i & 1)));
           }
         }
-        continue;  // the accumulator half is already released
+        continue;  // the accumulator is already released
       }
       }
 #pragma unroll 1
@@ -528,7 +489,7 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(aempty(hh));
+      if (lane == 0) mbar_arrive(aempty);
     }
     tc_fence_before();
     if constexpr (AHB > 0) {
