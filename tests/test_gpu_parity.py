@@ -332,6 +332,26 @@ def test_int8_gemm_many_tiles_per_pair_bit_exact(m, n, k, ws):
     assert (err <= 2.5e-6 * np.abs(x) + 1e-37).all()
 
 
+@pytest.mark.parametrize("m,n,k", [(600, 3584, 4096), (300, 9216, 3072)])
+def test_int8_gemm_banded_tile_order_exact(m, n, k, ws):
+    """K <= 4096 with more N tiles than one band holds (bands of 24 MB of B: 12 tiles at K = 4096,
+    16 at K = 3072): the banded walk over the tiles, with a ragged last band and ragged M, gives
+    the int64 oracle's accumulators on sampled rows and every column."""
+    g = synth.rng(m * 7 + n + k)
+    a = g.integers(-127, 128, (m, k)).astype(np.int8)
+    b = g.integers(-127, 128, (n, k)).astype(np.int8)
+    sa = (g.random(m) * 0.01).astype(np.float32)
+    sb = (g.random(n) * 0.01).astype(np.float32)
+    acc = torch.empty(m, n, dtype=torch.int32, device="cuda")
+    y = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    dit.qgemm_int8(_int8_dev(a, torch.bfloat16), dev_f32(sa), _int8_dev(b, torch.bfloat16), dev_f32(sb), y, ws,
+                   acc_debug=acc, act=dit.ACT_GELU_ERF)
+    _status_clean(ws)
+    rows = np.unique(np.concatenate([synth.rng(m + 1).choice(m, 12, replace=False), [0, 255, 256, m - 1]]))
+    ref = D.gemm_int8_acc(a[rows], b)
+    assert np.array_equal(host(acc[torch.from_numpy(rows).cuda()]).astype(np.int64), ref)
+
+
 def _adversarial_int8(m, n, k, seed):
     """Operands that push every exact-chunk partial sum towards its 2^24 bound, mix huge and
     unit products after a large running sum, and cancel."""
