@@ -66,9 +66,8 @@ const char* dit_status_str(dit_status s);
 /* Library version, "major.minor.patch" (static storage). */
 const char* dit_version(void);
 
-/* Bytes of workspace every call below needs (a constant, about 24 MiB: a status word, a
- * completion counter, per-CTA partial sums, and the int32 partial accumulators with their
- * arrival tickets of the INT8 GEMM's split-K tail). */
+/* Bytes of workspace every call below needs (a constant, 64 KiB: a status word, a completion
+ * counter, a running amax, a tensor scale and the per-CTA partial sums of the reductions). */
 size_t dit_workspace_bytes(void);
 
 /* Byte offset, inside the workspace, of the uint32 device status word (bit i set means

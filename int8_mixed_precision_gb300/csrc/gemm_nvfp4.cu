@@ -550,22 +550,25 @@ static dit_status launch_s(const uint8_t* a, const uint8_t* b, const uint8_t* a_
 
 using namespace dit6;
 
-// Tile configuration per call (PFLOP/s measured on GB300 before the accumulator hand-off).
+// Tile configuration per call (PFLOP/s or microseconds measured on GB300).
 //  * 128 x 256 tiles, one CTA per SM, four stages, sixteen 64-column epilogue warps that
-//    release their accumulator half right after loading it (bias, activation and stores overlap
+//    release their accumulator right after loading it (bias, activation and stores overlap
 //    the next tile's MMAs): with the GELU epilogue it leads everywhere (CogVideoX-2B FFN-up 3.27
-//    vs 2.69 on 128 x 128 tiles, 5B FFN-up 4.11 vs 3.46, 1080p FFN-up 4.26 vs 3.55).
+//    vs 2.69 on 128 x 128 tiles, 5B FFN-up 4.11 vs 3.46, 1080p FFN-up 4.26 vs 3.55); bf16
+//    output without GELU when K >= 3072 (17776 tokens, 5B: QKV 224 vs 229 us, out-proj 80.5 vs
+//    82.6, FFN-down 243 vs 248; 1080p FFN-up without GELU 1697 vs 1739).
 //  * 128 x 256 tiles with eight 128-column epilogue warps that convert to packed bf16 before
-//    the release: bf16 output without GELU (2B QKV 3.50, 5B QKV 4.39, 1080p FFN-up 4.54); fp32
-//    output when K >= 3072 and N is a multiple of 256.
+//    the release: bf16 output without GELU when K < 3072 (2B QKV 111 vs 113 us with sixteen
+//    warps); fp32 output when K >= 3072 and N is a multiple of 256.
 //  * 128 x 128 tiles, two CTAs per SM (three stages each, 108 KB of shared memory): the two
 //    independent MMA streams hide each other's epilogue; fp32 output otherwise, and bf16 output
 //    with N off the 256 grid and K >= 4096 (2B FFN-down, N = 1920: 4.39 vs 4.32).
 static dit_status nvfp4_gemm_dispatch(const uint8_t* a, const uint8_t* a_sf, const float* a_gs, const uint8_t* b,
                                       const uint8_t* b_sf, const float* b_gs, int M, int N, int K, const float* bias,
                                       void* y, int epi, void* ws, cudaStream_t st) {
-  if (epi & EPI_GELU) return f4::launch_s<256, 4, 1, 16>(a, b, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y, epi, ws, st);
   const bool wide = (epi & EPI_BF16) ? !(N % 256 != 0 && K >= 4096) : (K >= 3072 && N % 256 == 0);
+  if ((epi & EPI_GELU) || (wide && (epi & EPI_BF16) && K >= 3072))
+    return f4::launch_s<256, 4, 1, 16>(a, b, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y, epi, ws, st);
   if (wide) return f4::launch_s<256, 4, 1>(a, b, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y, epi, ws, st);
   return f4::launch_s<128, 3, 2>(a, b, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y, epi, ws, st);
 }

@@ -352,6 +352,90 @@ def test_int8_gemm_banded_tile_order_exact(m, n, k, ws):
     assert np.array_equal(host(acc[torch.from_numpy(rows).cuda()]).astype(np.int64), ref)
 
 
+# INT8 GEMM shapes whose tile count leaves the last wave of CTA pairs partly empty (one or two
+# full waves plus a few tiles) or gives fewer tiles than pairs.  The shapes follow the SM count,
+# so that they hit those cases on any GB300 part.
+PAIRS = torch.cuda.get_device_properties(0).multi_processor_count // 2
+WAVE_SHAPES = [
+    (((PAIRS + 12 + 7) // 8) * 256 - 77, 8 * 256 - 40, 1040),      # one wave + 12 tiles, ragged M, N, K
+    (((2 * PAIRS + 4 + 3) // 4) * 256, 4 * 256, 3072),             # two waves + 4 tiles
+    (((PAIRS + 12 + 7) // 8) * 256 - 77, 8 * 256 - 40, 12288),     # deep K: several exact chunks per piece
+    (5 * 256 - 1, 6 * 256, 12288),                                 # 30 tiles: fewer than the pairs
+]
+
+
+def _rows_meeting_every_tile(m):
+    """One row per (256-row tile, CTA of the pair, 32-row lane quarter), at varying lanes."""
+    rows = [mt * 256 + r * 128 + q * 32 + (7 * mt + 5 * q + 3 * r) % 32
+            for mt in range((m + 255) // 256) for r in range(2) for q in range(4)]
+    return np.unique(np.array([x for x in rows if x < m] + [m - 1]))
+
+
+@pytest.mark.parametrize("m,n,k", WAVE_SHAPES)
+def test_int8_gemm_partial_last_wave_exact(m, n, k, ws):
+    """The int64 oracle's accumulators on rows that meet every tile, and the exact product
+    everywhere; the output with and without the raw accumulators requested is the same bit for
+    bit and equals the epilogue's arithmetic on the exact integers."""
+    g = synth.rng(m * 3 + n * 5 + k)
+    a = g.integers(-127, 128, (m, k)).astype(np.int8)
+    b = g.integers(-127, 128, (n, k)).astype(np.int8)
+    sa = (g.random(m) * 0.01).astype(np.float32)
+    sb = (g.random(n) * 0.01).astype(np.float32)
+    ta, tb = _int8_dev(a, torch.bfloat16), _int8_dev(b, torch.bfloat16)
+    acc = torch.empty(m, n, dtype=torch.int32, device="cuda")
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    y2 = torch.empty_like(y)
+    dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws, acc_debug=acc)
+    dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y2, ws)
+    _status_clean(ws)
+    rows = _rows_meeting_every_tile(m)
+    ref = D.gemm_int8_acc(a[rows], b)
+    got = host(acc).astype(np.int64)
+    assert np.array_equal(got[rows], ref)
+    # everywhere: the float64 product of the codes is exact here (|acc| <= k * 127^2 < 2^53);
+    # it agrees with the oracle on the rows above
+    full = a.astype(np.float64) @ b.astype(np.float64).T
+    assert np.array_equal(full[rows], ref.astype(np.float64))
+    assert np.array_equal(got.astype(np.float64), full)
+    assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
+    x = (ref.astype(np.float32) * sa[rows, None]).astype(np.float32) * sb[None, :]
+    assert np.array_equal(host(y)[rows], x)
+
+
+def test_int8_gemm_timeout_recovers_on_every_pair(monkeypatch):
+    """A GEMM on every CTA pair whose producer issues no loads: all the pairs' waits run out,
+    DIT_ERR_TIMEOUT is raised, and the same workspace then serves two normal calls with exact
+    results."""
+    import time
+    ws2 = dit.workspace()
+    m, n, k = WAVE_SHAPES[0]
+    g = synth.rng(77)
+    a = g.integers(-127, 128, (m, k)).astype(np.int8)
+    b = g.integers(-127, 128, (n, k)).astype(np.int8)
+    sa, sb = np.ones(m, np.float32), np.ones(n, np.float32)
+    ta, tb = _int8_dev(a, torch.bfloat16), _int8_dev(b, torch.bfloat16)
+    acc = torch.empty(m, n, dtype=torch.int32, device="cuda")
+    y = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    call = lambda: dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws2, acc_debug=acc)
+    monkeypatch.setenv("DIT6_TEST_STALL_PRODUCER", "1")
+    t0 = time.time()
+    call()
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 30.0
+    assert dit.device_status(ws2) & (1 << 5), "DIT_ERR_TIMEOUT not raised"
+    monkeypatch.delenv("DIT6_TEST_STALL_PRODUCER")
+    dit.clear_device_status(ws2)
+    full = a.astype(np.float64) @ b.astype(np.float64).T
+    rows = _rows_meeting_every_tile(m)
+    assert np.array_equal(full[rows], D.gemm_int8_acc(a[rows], b).astype(np.float64))
+    for _ in range(2):
+        acc.zero_()
+        call()
+        torch.cuda.synchronize()
+        assert dit.device_status(ws2) == 0
+        assert np.array_equal(host(acc).astype(np.float64), full)
+
+
 def _adversarial_int8(m, n, k, seed):
     """Operands that push every exact-chunk partial sum towards its 2^24 bound, mix huge and
     unit products after a large running sum, and cancel."""
