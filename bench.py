@@ -11,7 +11,8 @@ block Hadamard + activation quantisation + quantised GEMM; GELU (erf form) fused
 FFN-up epilogue, whose output is the FFN-down input; when both FFN linears route NVFP4 the
 FFN-up epilogue also yields its output's NVFP4 tensor scale, so FFN-down's quantisation is
 one pass) and the delta-cache commit of the block's own input/output pair (residual delta,
-Gamma_t for the next step's routing, similarity of the last two deltas).
+Gamma_t for the next step's routing, similarity of the last two deltas); block b + 1's input
+is block b's output, as in the DiT's residual stream.
 value = algorithmic GEMM FLOPs of the step / step time (TFLOP/s).
 
 Further keys of the JSON line: the CogVideoX-2B step (hidden 1920, 30 blocks), the whole
@@ -233,7 +234,8 @@ class Workload:
         self.inputs = [{name: act(k, 10 * s + i) for i, (name, k, _) in enumerate(self.lin_shapes)
                         if name != "ffn_down"} for s in range(2)]
         # per-block Gamma pairs: X_out = X_in + gamma_b * S * X_in, gamma_b ~ U(0, 0.2); every
-        # block commits its own pair
+        # block commits its own pair.  The blocks form a residual stream: block b + 1's input is
+        # block b's output (the same tensor), as in the DiT, so a step holds nblocks + 1 of them
         g.manual_seed(seed + 7)
         self.gammas_true = (torch.rand(self.nblocks, generator=g, device=dev) * 0.2).tolist()
         # quantised-activation buffers shared by all blocks (one stream orders their uses)
@@ -243,7 +245,7 @@ class Workload:
                 self.act_bufs[k] = (dit.alloc_nvfp4(M, k, dev), dit.alloc_int8(M, k, dev))
         self.x_in, self.x_out, self.blocks = [], [], []
         for b in range(self.nblocks):
-            xi = act(H, 500 + b)
+            xi = act(H, 500) if b == 0 else self.x_out[b - 1]
             g.manual_seed(seed * 31 + b)
             sgn = torch.randint(0, 2, xi.shape, generator=g, device=dev).to(torch.float32) * 2 - 1
             self.x_in.append(xi)
@@ -715,26 +717,28 @@ def time_steps(wl, steps, warmup, world, barrier, dominant=None, clocks=None):
 
 def e2e_leg(wl, steps, world, barrier):
     """The same metric end to end through the public API: every step copies its inputs from
-    pinned host memory (the linear inputs, every block's input/output pair) and reads its result
-    (the last FFN-down output, Gamma and the similarity of every block) back.  The copies run on
-    a second stream into one of two device buffer sets (ping-pong by step), in block order with
-    one event per block: block b waits only for its own inputs, so the copies of later blocks
-    (and of the next step) overlap the kernels of earlier ones."""
+    pinned host memory (the linear inputs, the first block's input and every block's output,
+    the next block's input) and reads its result (the last FFN-down output, Gamma and the
+    similarity of every block) back.  The copies run on a second stream into one of two device
+    buffer sets (ping-pong by step), in block order with one event per block: block b waits only
+    for its own inputs, so the copies of later blocks (and of the next step) overlap the kernels
+    of earlier ones."""
     torch = wl.torch
     dev = wl.dev
     stream = torch.cuda.current_stream()
     nb = wl.nblocks
     host_in = {(s, name): t.cpu().pin_memory() for s in range(2) for name, t in wl.inputs[s].items()}
-    host_xi = [t.cpu().pin_memory() for t in wl.x_in]
+    host_x0 = wl.x_in[0].cpu().pin_memory()
     host_xo = [t.cpu().pin_memory() for t in wl.x_out]
-    h2d = sum(t.numel() * t.element_size() for t in list(host_in.values()) + host_xi + host_xo)
+    h2d = sum(t.numel() * t.element_size() for t in list(host_in.values()) + [host_x0] + host_xo)
     out_host = torch.empty_like(wl.y["ffn_down"], device="cpu").pin_memory()
     g_host = torch.empty(2 * nb, dtype=torch.float32).pin_memory()
     d2h = out_host.numel() * out_host.element_size() + g_host.numel() * 4
     orig = {"inputs": wl.inputs, "x_out": wl.x_out, "x_in": wl.x_in}
+    x_out1 = [torch.empty_like(t) for t in wl.x_out]
     slots = [orig,
              {"inputs": [{k: torch.empty_like(v) for k, v in st.items()} for st in wl.inputs],
-              "x_out": [torch.empty_like(t) for t in wl.x_out], "x_in": [torch.empty_like(t) for t in wl.x_in]}]
+              "x_out": x_out1, "x_in": [torch.empty_like(wl.x_in[0])] + x_out1[:-1]}]
     copy_stream = torch.cuda.Stream(device=dev)
     ready = [[torch.cuda.Event() for _ in range(nb)] for _ in range(2)]
     slot_free = [torch.cuda.Event() for _ in range(2)]
@@ -751,7 +755,8 @@ def e2e_leg(wl, steps, world, barrier):
                 if b < 2:
                     for name, t in sl["inputs"][b].items():
                         t.copy_(host_in[(b, name)], non_blocking=True)
-                sl["x_in"][b].copy_(host_xi[b], non_blocking=True)
+                if b == 0:
+                    sl["x_in"][0].copy_(host_x0, non_blocking=True)
                 sl["x_out"][b].copy_(host_xo[b], non_blocking=True)
                 ready[k][b].record(copy_stream)
         wl.inputs, wl.x_out, wl.x_in = sl["inputs"], sl["x_out"], sl["x_in"]
@@ -771,7 +776,7 @@ def e2e_leg(wl, steps, world, barrier):
     barrier()
     ms = (time.perf_counter() - t0) * 1e3 / steps
     wl.inputs, wl.x_out, wl.x_in = orig["inputs"], orig["x_out"], orig["x_in"]
-    del slots, host_in, host_xi, host_xo
+    del slots, x_out1, host_in, host_x0, host_xo
     torch.cuda.empty_cache()
     return max_over_ranks(ms, world, dev), int(h2d), int(d2h)
 
@@ -836,9 +841,9 @@ def run_ours(args, rank, world, local_rank):
                    "blocks": wl.nblocks, "activations": spec["activations"], "hadamard_block": HBLOCK,
                    "gamma": "U(0,0.2)", "thr": THR, "int8_layers": routes_flat.count(1),
                    "nvfp4_layers": routes_flat.count(0),
-                   "l2": ("inputs larger than L2 in aggregate: each block reads its own input/output pair and one of "
-                          "two alternating input sets; a step streams tens of GB, so nothing of the previous step "
-                          "is L2-resident when the next starts (no flush)"),
+                   "l2": ("inputs larger than L2 in aggregate: each block reads its input (the previous block's "
+                          "output), its own output and one of two alternating input sets; a step streams tens of GB, "
+                          "so nothing of the previous step is L2-resident when the next starts (no flush)"),
                    "parallelism": f"replicas{world}"},
         "roofline": roof,
         "kernel_ms_per_step": {k: round(v, 3) for k, v in tot.items()},
