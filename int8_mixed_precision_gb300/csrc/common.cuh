@@ -428,6 +428,43 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 // ---------------------------------------------------------------------------------------
 namespace dit6 {
 int num_sms();  // SM count of the current device (cached per device)
+// ---------------------------------------------------------------------------------------
+// Programmatic dependent launch (sm_90+).  Every kernel of the library is launched with the
+// programmatic stream serialisation attribute (launch_pdl).  Its first instruction lets the
+// next kernel on the stream launch once all of its own CTAs are resident
+// (pdl_launch_dependents), and it waits for the previous kernel to complete, with that
+// kernel's memory operations visible, before its own first global memory access (pdl_wait).
+// The next kernel's CTAs thus launch and run their prologue (barrier initialisation, tensor
+// memory allocation) while this one drains.  After a launch without the attribute, or after a
+// stream operation other than a kernel, both are no-ops.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launches `kern` on `st` with the programmatic stream serialisation attribute, plus a
+// cluster dimension when cluster_x > 1.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       unsigned cluster_x, Args... args) {
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = cluster_x > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Failure-path test hook: DIT6_TEST_STALL_PRODUCER=1 makes the GEMMs' producer warp issue no
 // loads, so the consumers' bounded waits run out and the kernels report DIT_ERR_TIMEOUT.
 int test_stall();

@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M,
                 int N, int K, const float* __restrict__ bias, void* __restrict__ y, int epi,
                 int32_t* __restrict__ acc_out, void* ws) {
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -63,6 +64,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_wait();
 
   if (warp == CONSUMERS) {  // ------------------------------------------ TMA producer
     if (lane == 0) {
@@ -203,9 +205,8 @@ extern "C" dit_status dit_qgemm_int8(const void* a, const float* a_scale, const 
   }
   dim3 grid((unsigned)((n + i8::BN - 1) / i8::BN), (unsigned)((m + i8::BM - 1) / i8::BM));
   if (grid.y > 65535) return DIT_ERR_UNSUPPORTED;
-  i8::k_gemm_int8<<<grid, i8::THREADS, i8::SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(
-      ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, epi,
-      acc_debug, ws);
-  DIT_CHECK_LAUNCH();
+  if (launch_pdl(i8::k_gemm_int8, grid, dim3(i8::THREADS), i8::SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream), 1,
+                 ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, epi, acc_debug, ws) != cudaSuccess)
+    return DIT_ERR_CUDA;
   return DIT_OK;
 }

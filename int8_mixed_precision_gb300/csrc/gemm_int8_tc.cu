@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                      const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N, int K,
                      const float* __restrict__ bias, void* __restrict__ y, int epi, int32_t* __restrict__ acc_out,
                      void* ws, int stall, int band) {
+  pdl_launch_dependents();
   using P = PairCfg;
   constexpr int S = P::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();
 
   if (warp == 0) {  // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0 && !stall) {
@@ -438,9 +440,8 @@ dit_status launch_pair_k(const CUtensorMap& ta, const CUtensorMap& tb, const flo
   if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) return DIT_ERR_CUDA;
   int64_t pairs = clusters;
   if (pairs > items) pairs = items;
-  cfg.gridDim = dim3((unsigned)(2 * pairs));
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, epi, acc_out, ws,
-                         test_stall(), band) != cudaSuccess)
+  if (launch_pdl(kern, dim3((unsigned)(2 * pairs)), dim3(P::THREADS), P::SMEM_BYTES, st, 2, ta, tb, a_scale,
+                 b_scale, (int)m, (int)n, (int)k, bias, y, epi, acc_out, ws, test_stall(), band) != cudaSuccess)
     return DIT_ERR_CUDA;
   return DIT_OK;
 }

@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
                    const float* __restrict__ a_gs, const float* __restrict__ b_gs, int M, int N,
                    int K, const float* __restrict__ bias, void* __restrict__ y, int epi,
                    void* ws, int stall, float q_isb, float* __restrict__ q_sg_next) {
+  pdl_launch_dependents();
   static_assert(EPW == 0 || (CTAS == 1 && EPW == BN / 16), "sixteen epilogue warps: BN = 256 only");
   static_assert(AHB == 0 || EPW != 0, "the output's Hadamard amax needs the 64-column epilogue warps");
   using C = SCfg<BN, STAGES, CTAS, EPW>;
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(SCfg<BN, STAGES, CTAS, EPW>::THREADS, CTAS)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();
 
   if (warp == 0) {  // -------------------------------------------------- TMA producer
     if (lane == 0 && !stall) {  // stall: a test hook that issues no loads at all
@@ -539,9 +541,9 @@ static dit_status launch_s(const uint8_t* a, const uint8_t* b, const uint8_t* a_
   const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   int64_t grid = (int64_t)num_sms() * CTAS;
   if (grid > tiles) grid = tiles;
-  kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(ta, tb, a_sf, b_sf, a_gs, b_gs, M, N, K, bias, y,
-                                                         epi, ws, test_stall(), q_isb, q_sg_next);
-  DIT_CHECK_LAUNCH();
+  if (launch_pdl(kern, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, st, 1, ta, tb, a_sf, b_sf, a_gs, b_gs,
+                 M, N, K, bias, y, epi, ws, test_stall(), q_isb, q_sg_next) != cudaSuccess)
+    return DIT_ERR_CUDA;
   return DIT_OK;
 }
 

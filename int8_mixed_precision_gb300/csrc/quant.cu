@@ -103,6 +103,8 @@ __global__ void __launch_bounds__(256) k_quant_int8(const void* __restrict__ x, 
                                                     int upr, int tr, float inv_sqrt_b,
                                                     void* __restrict__ q,
                                                     float* __restrict__ row_scale) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ unsigned row_amax[256];
   const int t = threadIdx.x;
   if (t < tr) row_amax[t] = 0u;
@@ -170,6 +172,8 @@ __global__ void __launch_bounds__(256) k_nvfp4_to_int8(const uint8_t* __restrict
                                                        const float* __restrict__ gs, int64_t rows, int upr,
                                                        int tr, void* __restrict__ q,
                                                        float* __restrict__ row_scale) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ unsigned row_amax[256];
   const int t = threadIdx.x;
   if (t < tr) row_amax[t] = 0u;
@@ -239,6 +243,8 @@ template <typename T, int HB>
 __global__ void __launch_bounds__(256) k_nvfp4_amax(const void* __restrict__ x, int64_t units,
                                                     float inv_sqrt_b, void* ws,
                                                     float* __restrict__ tensor_scale_out, int raw_amax) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ float wmax[8];
   __shared__ bool last;
   float m = 0.f;
@@ -291,6 +297,8 @@ __global__ void __launch_bounds__(256) k_nvfp4_quant(const void* __restrict__ x,
                                                      uint8_t* __restrict__ sf,
                                                      float* __restrict__ tensor_scale_out,
                                                      int copy_scale) {
+  pdl_launch_dependents();
+  pdl_wait();
   const float s_g = *sg_ptr;
   if (copy_scale && blockIdx.x == 0 && threadIdx.x == 0) *tensor_scale_out = s_g;
   const float six_sg = __fmul_rn(6.0f, s_g);
@@ -335,9 +343,9 @@ static dit_status launch_int8(const void* x, int64_t rows, int64_t k, int hb, vo
   if (grid > 0x7fffffff) return DIT_ERR_UNSUPPORTED;
   const float isb = (float)(1.0 / sqrt((double)hb));
   switch (hb) {
-    case 16: k_quant_int8<T, 16, OB><<<(unsigned)grid, threads, 0, st>>>(x, rows, upr, tr, isb, q, rs); break;
-    case 32: k_quant_int8<T, 32, OB><<<(unsigned)grid, threads, 0, st>>>(x, rows, upr, tr, isb, q, rs); break;
-    default: k_quant_int8<T, 64, OB><<<(unsigned)grid, threads, 0, st>>>(x, rows, upr, tr, isb, q, rs); break;
+    case 16: launch_pdl(k_quant_int8<T, 16, OB>, dim3((unsigned)grid), dim3(threads), 0, st, 1, x, rows, upr, tr, isb, q, rs); break;
+    case 32: launch_pdl(k_quant_int8<T, 32, OB>, dim3((unsigned)grid), dim3(threads), 0, st, 1, x, rows, upr, tr, isb, q, rs); break;
+    default: launch_pdl(k_quant_int8<T, 64, OB>, dim3((unsigned)grid), dim3(threads), 0, st, 1, x, rows, upr, tr, isb, q, rs); break;
   }
   DIT_CHECK_LAUNCH();
   return DIT_OK;
@@ -355,14 +363,13 @@ static void launch_nvfp4_t(const void* x, int64_t rows, int upr, float isb, uint
     int64_t g1 = (units + 255) / 256;
     if (g1 > 6 * sms) g1 = 6 * sms;
     if (g1 < 1) g1 = 1;
-    k_nvfp4_amax<T, HB><<<(unsigned)g1, 256, 0, st>>>(x, units, isb, ws, ts_out, 0);
+    launch_pdl(k_nvfp4_amax<T, HB>, dim3((unsigned)g1), dim3(256), 0, st, 1, x, units, isb, ws, ts_out, 0);
     sgp = reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws) + WS_SG);
   }
   int64_t g2 = (pad_units + 255) / 256;
   if (g2 > 6 * sms) g2 = 6 * sms;
   if (g2 < 1) g2 = 1;
-  k_nvfp4_quant<T, HB><<<(unsigned)g2, 256, 0, st>>>(x, rows, upr, pad_units, isb, sgp, codes,
-                                                      sf, ts_out, ts_in ? 1 : 0);
+  launch_pdl(k_nvfp4_quant<T, HB>, dim3((unsigned)g2), dim3(256), 0, st, 1, x, rows, upr, pad_units, isb, sgp, codes, sf, ts_out, ts_in ? 1 : 0);
 }
 
 }  // namespace dit6
@@ -436,9 +443,9 @@ extern "C" dit_status dit_nvfp4_to_int8(const uint8_t* codes, const uint8_t* sf,
   if (grid > 0x7fffffff) return DIT_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (q_dt == DIT_BF16)
-    k_nvfp4_to_int8<true><<<(unsigned)grid, tr * upr, 0, st>>>(codes, sf, tensor_scale, rows, upr, tr, q, row_scale);
+    launch_pdl(k_nvfp4_to_int8<true>, dim3((unsigned)grid), dim3(tr * upr), 0, st, 1, codes, sf, tensor_scale, rows, upr, tr, q, row_scale);
   else
-    k_nvfp4_to_int8<false><<<(unsigned)grid, tr * upr, 0, st>>>(codes, sf, tensor_scale, rows, upr, tr, q, row_scale);
+    launch_pdl(k_nvfp4_to_int8<false>, dim3((unsigned)grid), dim3(tr * upr), 0, st, 1, codes, sf, tensor_scale, rows, upr, tr, q, row_scale);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -453,7 +460,7 @@ static void launch_amax_shard(const void* x, int64_t rows, int upr, float isb, f
   int64_t g1 = (units + 255) / 256;
   if (g1 > 6 * num_sms()) g1 = 6 * num_sms();
   if (g1 < 1) g1 = 1;
-  k_nvfp4_amax<T, HB><<<(unsigned)g1, 256, 0, st>>>(x, units, isb, ws, amax_out, 1);
+  launch_pdl(k_nvfp4_amax<T, HB>, dim3((unsigned)g1), dim3(256), 0, st, 1, x, units, isb, ws, amax_out, 1);
 }
 
 extern "C" dit_status dit_nvfp4_amax(const void* x, dit_dtype dt, int64_t rows, int64_t k, int hblock,

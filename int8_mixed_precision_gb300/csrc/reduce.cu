@@ -142,6 +142,8 @@ __global__ void __launch_bounds__(RED_THREADS) k_gamma_route(const void* __restr
                                                              float* gamma_out,
                                                              int32_t* routes, void* ws,
                                                              double* partials_out) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int N = Vec<T>::N;
   constexpr int U = 4;  // vectors in flight per thread
   const int64_t nv = n / N;
@@ -204,6 +206,8 @@ __global__ void __launch_bounds__(RED_THREADS) k_gamma_route(const void* __restr
 template <typename T>
 __global__ void __launch_bounds__(RED_THREADS) k_sumsq(const void* __restrict__ x, int64_t n, float k_sigma,
                                                        void* ws) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int N = Vec<T>::N;
   const int64_t nv = n / N;
   float s[1] = {0.f};
@@ -226,6 +230,8 @@ __global__ void __launch_bounds__(RED_THREADS) k_sumsq(const void* __restrict__ 
 template <typename T>
 __global__ void __launch_bounds__(RED_THREADS) k_count_over(const void* __restrict__ x, int64_t n, void* ws,
                                                             float* ratio_out, int64_t* count_out) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int N = Vec<T>::N;
   const double thr = *reinterpret_cast<const double*>(reinterpret_cast<const char*>(ws) + WS_THR);
   const int64_t nv = n / N;
@@ -255,6 +261,8 @@ __global__ void __launch_bounds__(RED_THREADS) k_tdc_commit(const void* __restri
                                                             void* __restrict__ dnew, int64_t n,
                                                             float* gamma_out, float* sim_out,
                                                             void* ws, double* partials_out) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int N = Vec<T>::N;
   const int64_t nv = n / N;
   float s[4] = {0.f, 0.f, 0.f, 0.f};
@@ -306,6 +314,8 @@ template <typename T>
 __global__ void __launch_bounds__(RED_THREADS) k_tdc_skip(const void* __restrict__ xi,
                                                           const void* __restrict__ d1,
                                                           void* __restrict__ out, int64_t n) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int N = Vec<T>::N;
   const int64_t nv = n / N;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -373,11 +383,9 @@ extern "C" dit_status dit_gamma_route(const void* x_in, const void* x_out, dit_d
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (dt == DIT_BF16)
-    k_gamma_route<__nv_bfloat16><<<red_grid(n, 16), RED_THREADS, 0, st>>>(x_in, x_out, n, rp,
-                                                                         gamma_dev, routes_dev, ws, nullptr);
+    launch_pdl(k_gamma_route<__nv_bfloat16>, dim3(red_grid(n, 16)), dim3(RED_THREADS), 0, st, 1, x_in, x_out, n, rp, gamma_dev, routes_dev, ws, nullptr);
   else
-    k_gamma_route<float><<<red_grid(n, 8), RED_THREADS, 0, st>>>(x_in, x_out, n, rp, gamma_dev,
-                                                               routes_dev, ws, nullptr);
+    launch_pdl(k_gamma_route<float>, dim3(red_grid(n, 8)), dim3(RED_THREADS), 0, st, 1, x_in, x_out, n, rp, gamma_dev, routes_dev, ws, nullptr);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -398,9 +406,9 @@ extern "C" dit_status dit_tdc_step(int mode, const void* x_in, const void* x_out
     if (g > cap) g = cap;
     if (g < 1) g = 1;
     if (dt == DIT_BF16)
-      k_tdc_skip<__nv_bfloat16><<<(unsigned)g, RED_THREADS, 0, st>>>(x_in, d1, x_out_skip, n);
+      launch_pdl(k_tdc_skip<__nv_bfloat16>, dim3((unsigned)g), dim3(RED_THREADS), 0, st, 1, x_in, d1, x_out_skip, n);
     else
-      k_tdc_skip<float><<<(unsigned)g, RED_THREADS, 0, st>>>(x_in, d1, x_out_skip, n);
+      launch_pdl(k_tdc_skip<float>, dim3((unsigned)g), dim3(RED_THREADS), 0, st, 1, x_in, d1, x_out_skip, n);
     DIT_CHECK_LAUNCH();
     return DIT_OK;
   }
@@ -412,11 +420,9 @@ extern "C" dit_status dit_tdc_step(int mode, const void* x_in, const void* x_out
       !aligned32(ws))
     return DIT_ERR_ALIGNMENT;
   if (dt == DIT_BF16)
-    k_tdc_commit<__nv_bfloat16><<<red_grid(n, 16), RED_THREADS, 0, st>>>(
-        x_in, x_out, d1, d_new, n, gamma_dev, sim_dev, ws, nullptr);
+    launch_pdl(k_tdc_commit<__nv_bfloat16>, dim3(red_grid(n, 16)), dim3(RED_THREADS), 0, st, 1,  x_in, x_out, d1, d_new, n, gamma_dev, sim_dev, ws, nullptr);
   else
-    k_tdc_commit<float><<<red_grid(n, 8), RED_THREADS, 0, st>>>(x_in, x_out, d1, d_new, n,
-                                                              gamma_dev, sim_dev, ws, nullptr);
+    launch_pdl(k_tdc_commit<float>, dim3(red_grid(n, 8)), dim3(RED_THREADS), 0, st, 1, x_in, x_out, d1, d_new, n, gamma_dev, sim_dev, ws, nullptr);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -490,11 +496,9 @@ extern "C" dit_status dit_gamma_route_noalloc(const void* x_in, const void* x_ou
   // the status word and completion counter must start at zero for every call
   if (cudaMemsetAsync(scratch, 0, 8, st) != cudaSuccess) return DIT_ERR_CUDA;
   if (dt == DIT_BF16)
-    k_gamma_route<__nv_bfloat16><<<grid, RED_THREADS, 0, st>>>(x_in, x_out, n, rp, gamma_dev,
-                                                               routes_dev, scratch, nullptr);
+    launch_pdl(k_gamma_route<__nv_bfloat16>, dim3(grid), dim3(RED_THREADS), 0, st, 1, x_in, x_out, n, rp, gamma_dev, routes_dev, scratch, nullptr);
   else
-    k_gamma_route<float><<<grid, RED_THREADS, 0, st>>>(x_in, x_out, n, rp, gamma_dev,
-                                                       routes_dev, scratch, nullptr);
+    launch_pdl(k_gamma_route<float>, dim3(grid), dim3(RED_THREADS), 0, st, 1, x_in, x_out, n, rp, gamma_dev, routes_dev, scratch, nullptr);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
@@ -507,12 +511,12 @@ extern "C" dit_status dit_outlier_ratio(const void* x, dit_dtype dt, int64_t n, 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (dt == DIT_BF16) {
     const unsigned g = red_grid(n, 16);
-    k_sumsq<__nv_bfloat16><<<g, RED_THREADS, 0, st>>>(x, n, k_sigma, ws);
-    k_count_over<__nv_bfloat16><<<g, RED_THREADS, 0, st>>>(x, n, ws, ratio_dev, count_dev);
+    launch_pdl(k_sumsq<__nv_bfloat16>, dim3(g), dim3(RED_THREADS), 0, st, 1, x, n, k_sigma, ws);
+    launch_pdl(k_count_over<__nv_bfloat16>, dim3(g), dim3(RED_THREADS), 0, st, 1, x, n, ws, ratio_dev, count_dev);
   } else {
     const unsigned g = red_grid(n, 8);
-    k_sumsq<float><<<g, RED_THREADS, 0, st>>>(x, n, k_sigma, ws);
-    k_count_over<float><<<g, RED_THREADS, 0, st>>>(x, n, ws, ratio_dev, count_dev);
+    launch_pdl(k_sumsq<float>, dim3(g), dim3(RED_THREADS), 0, st, 1, x, n, k_sigma, ws);
+    launch_pdl(k_count_over<float>, dim3(g), dim3(RED_THREADS), 0, st, 1, x, n, ws, ratio_dev, count_dev);
   }
   DIT_CHECK_LAUNCH();
   return DIT_OK;
@@ -530,6 +534,8 @@ namespace dit6 {
 __global__ void k_shard_finish(const double* __restrict__ p, int n_partials, const float* __restrict__ amax,
                                RouteParams rp, float* gamma_out, float* sim_out, int32_t* routes,
                                float* tensor_scale_out) {
+  pdl_launch_dependents();
+  pdl_wait();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
   if (p) {
     const double g = ratio(p[0], p[1]);
@@ -560,20 +566,16 @@ extern "C" dit_status dit_l1_partials(int mode, const void* x_in, const void* x_
   if (commit) {
     if (!d1 && cudaMemsetAsync(partials_dev + 2, 0, 2 * sizeof(double), st) != cudaSuccess) return DIT_ERR_CUDA;
     if (dt == DIT_BF16)
-      k_tdc_commit<__nv_bfloat16><<<red_grid(n, 16), RED_THREADS, 0, st>>>(x_in, x_out, d1, d_new, n, nullptr,
-                                                                          nullptr, ws, partials_dev);
+      launch_pdl(k_tdc_commit<__nv_bfloat16>, dim3(red_grid(n, 16)), dim3(RED_THREADS), 0, st, 1, x_in, x_out, d1, d_new, n, nullptr, nullptr, ws, partials_dev);
     else
-      k_tdc_commit<float><<<red_grid(n, 8), RED_THREADS, 0, st>>>(x_in, x_out, d1, d_new, n, nullptr, nullptr, ws,
-                                                                partials_dev);
+      launch_pdl(k_tdc_commit<float>, dim3(red_grid(n, 8)), dim3(RED_THREADS), 0, st, 1, x_in, x_out, d1, d_new, n, nullptr, nullptr, ws, partials_dev);
   } else {
     RouteParams rp;
     rp.n_layers = 0;
     if (dt == DIT_BF16)
-      k_gamma_route<__nv_bfloat16><<<red_grid(n, 16), RED_THREADS, 0, st>>>(x_in, x_out, n, rp, nullptr, nullptr,
-                                                                           ws, partials_dev);
+      launch_pdl(k_gamma_route<__nv_bfloat16>, dim3(red_grid(n, 16)), dim3(RED_THREADS), 0, st, 1, x_in, x_out, n, rp, nullptr, nullptr, ws, partials_dev);
     else
-      k_gamma_route<float><<<red_grid(n, 8), RED_THREADS, 0, st>>>(x_in, x_out, n, rp, nullptr, nullptr, ws,
-                                                                 partials_dev);
+      launch_pdl(k_gamma_route<float>, dim3(red_grid(n, 8)), dim3(RED_THREADS), 0, st, 1, x_in, x_out, n, rp, nullptr, nullptr, ws, partials_dev);
   }
   DIT_CHECK_LAUNCH();
   return DIT_OK;
@@ -605,9 +607,7 @@ extern "C" dit_status dit_shard_finish(const double* partials_dev, int n_partial
   RouteParams rp;
   dit_status s = route_params(alpha, beta, thr, routes_dev ? n_layers : 0, &rp);
   if (s != DIT_OK) return s;
-  k_shard_finish<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(partials_dev, n_partials, amax_dev, rp,
-                                                                      gamma_dev, sim_dev, routes_dev,
-                                                                      tensor_scale_dev);
+  launch_pdl(k_shard_finish, dim3(1), dim3(32), 0, reinterpret_cast<cudaStream_t>(stream), 1, partials_dev, n_partials, amax_dev, rp, gamma_dev, sim_dev, routes_dev, tensor_scale_dev);
   DIT_CHECK_LAUNCH();
   return DIT_OK;
 }
