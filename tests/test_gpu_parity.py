@@ -402,13 +402,14 @@ def test_int8_gemm_partial_last_wave_exact(m, n, k, ws):
     assert np.array_equal(host(y)[rows], x)
 
 
-def test_int8_gemm_timeout_recovers_on_every_pair(monkeypatch):
-    """A GEMM on every CTA pair whose producer issues no loads: all the pairs' waits run out,
+@pytest.mark.parametrize("shape", [0, 1])
+def test_int8_gemm_timeout_recovers_on_every_pair(shape, monkeypatch):
+    """A GEMM on every CTA pair whose producers issue no loads: all the pairs' waits run out,
     DIT_ERR_TIMEOUT is raised, and the same workspace then serves two normal calls with exact
     results."""
     import time
     ws2 = dit.workspace()
-    m, n, k = WAVE_SHAPES[0]
+    m, n, k = WAVE_SHAPES[shape]
     g = synth.rng(77)
     a = g.integers(-127, 128, (m, k)).astype(np.int8)
     b = g.integers(-127, 128, (n, k)).astype(np.int8)
