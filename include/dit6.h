@@ -13,7 +13,9 @@
  * - Pointers named *_dev or passed as tensors are DEVICE pointers owned by the caller.
  *   Pointers documented as "host" are read synchronously during the call.
  * - The library never allocates, frees or synchronises.  Every call only enqueues work on
- *   `stream` and returns.  The return code covers argument errors found on the host;
+ *   `stream` and returns.  Its kernels are launched with programmatic dependent launch: one
+ *   may start its prologue while the previous kernel on the stream drains, but waits for that
+ *   kernel to complete before touching memory, so stream order holds as for plain launches.  The return code covers argument errors found on the host;
  *   errors found on the device (a bounded wait that ran out) are OR-ed into the status
  *   word at byte 0 of the workspace (see dit_ws_status_offset), which the caller reads
  *   after synchronising.
