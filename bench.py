@@ -484,6 +484,58 @@ def run_long_1080p(dev, reps: int = 5):
     return out
 
 
+def run_int8_requant(dev, reps: int = 5):
+    """The INT8 leg of fusing the next layer's quantisation, at the CogVideoX-5B FFN-up shape
+    (17776 tokens, 3072 -> 12288, GELU): the GEMM writing bf16 followed by FFN-down's INT8
+    quantiser, against the GEMM whose epilogue quantises with given per-token scales (here the
+    exact ones of the unfused run, so the codes must agree bit for bit; in a denoising loop they
+    would be the previous step's).  Not part of the step: the method's scales are dynamic."""
+    import numpy as np
+    import torch
+    import int8_mixed_precision_gb300 as dit
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    m, k, n = 17776, 3072, 12288
+    ws = dit.workspace(dev)
+    a = torch.randint(-127, 128, (m, k), generator=g, device=dev).to(torch.bfloat16)
+    w = torch.randint(-127, 128, (n, k), generator=g, device=dev).to(torch.bfloat16)
+    sa = torch.rand(m, generator=g, device=dev) * 2e-4 + 1e-5
+    sw = torch.rand(n, generator=g, device=dev) * 2e-4 + 1e-5
+    y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+    q_ref = torch.empty_like(y)
+    s_ref = torch.empty(m, dtype=torch.float32, device=dev)
+    q = torch.empty_like(y)
+    amax = torch.zeros(m, dtype=torch.float32, device=dev)
+    flush = torch.empty(640 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def unfused():
+        dit.qgemm_int8(a, sa, w, sw, y, ws, act=dit.ACT_GELU_ERF)
+        dit.hadamard_quant_int8(y, 64, q_ref, s_ref)
+
+    def fused():
+        dit.qgemm_int8_requant(a, sa, w, sw, s_ref, q, amax, ws, act=dit.ACT_GELU_ERF)
+
+    t_gemm = _median_us(torch, lambda: dit.qgemm_int8(a, sa, w, sw, y, ws, act=dit.ACT_GELU_ERF), reps, flush)
+    t_unfused = _median_us(torch, unfused, reps, flush)
+    t_fused = _median_us(torch, fused, reps, flush)
+    amax.zero_()
+    fused()
+    torch.cuda.synchronize()
+    same = bool(torch.equal(q.view(torch.int16), q_ref.view(torch.int16)))
+    s_from_amax = (amax.cpu().numpy() / np.float32(127.0)).astype(np.float32)   # IEEE division, as the quantiser
+    same_scale = bool(np.array_equal(s_from_amax.view(np.uint32), s_ref.cpu().numpy().view(np.uint32)))
+    status = dit.device_status(ws)
+    del a, w, y, q_ref, q, flush
+    torch.cuda.empty_cache()
+    flops = 2 * m * n * k
+    return {"shape": "17776 x 3072 -> 12288, GELU", "gemm_us": round(t_gemm, 1),
+            "gemm_then_quantiser_us": round(t_unfused, 1), "fused_requant_us": round(t_fused, 1),
+            "saved_us": round(t_unfused - t_fused, 1), "fused_tflops": round(flops / (t_fused * 1e-6) / 1e12, 1),
+            "codes_equal_unfused": same, "row_maxima_give_the_same_scales": same_scale, "status": status,
+            "note": "per-token scales given (exact ones here); the method's scales are dynamic, so the step "
+                    "keeps the unfused pair"}
+
+
 def run_nvfp4_only_weights(wl, steps: int = 3):
     """The same step with every weight resident in NVFP4 only ([ZH] 2.A weight handling): each
     INT8-routed layer derives its INT8 weights per call into one scratch buffer per K."""
@@ -874,6 +926,7 @@ def run_ours(args, rank, world, local_rank):
         del w2
     if not args.no_long:
         line["long_1080p"] = run_long_1080p(dev)
+        line["int8_requant_ffn_up"] = run_int8_requant(dev)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)

@@ -226,6 +226,32 @@ dit_status dit_qgemm_nvfp4_amax(const uint8_t* a, const uint8_t* a_sf, const flo
                                 size_t ws_bytes, dit_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
+ * INT8 GEMM whose epilogue quantises its own output for the next INT8 layer (FFN up -> down)
+ * with caller-supplied per-token scales: the INT8 form of fusing the next layer's
+ * quantisation.  [EN] 2.A Mechanism 3 (per-token INT8) and 2.A Outlier Smoothing (online block
+ * Hadamard before quantisation).  The method's per-token scale of the next layer's input is
+ * max|H z| / 127 over the whole output row, which 30-48 output tiles hold; this call takes
+ * the scales as an input (from an earlier denoising step: delayed per-token scales, a
+ * variant the pages do not describe) and reports the exact row maxima of this output, so the
+ * bf16 round trip of the output and the next layer's quantiser pass are skipped.
+ *
+ * a, b: bf16-held INT8 codes (K-major), scales as dit_qgemm_int8.  For each row m and each
+ * 64-element block of n: z = act(acc * a_scale[m] * b_scale[n] (+ bias[n])) rounded to bf16
+ * exactly as dit_qgemm_int8 stores it; y = H_64 z / 8 (the quantiser's butterfly order);
+ * q = clamp(RN(y * RN(1 / next_scale[m])), -127, 127) (next_scale[m] = 0 gives 0), written
+ * to q_next (device, bf16-held codes [m x n], 32-byte aligned); row_amax (device float [m],
+ * zero-filled by the caller) receives max(row_amax[m], max over the row of |y|).  With
+ * next_scale[m] = row_amax[m] / 127 of this very output, q_next equals
+ * dit_hadamard_quant_int8(z, hblock = 64) bit for bit; a smaller scale saturates the entries
+ * beyond 127 * next_scale[m].  n % 64 == 0, k % 16 == 0, act NONE or GELU_ERF.
+ * ------------------------------------------------------------------------------------ */
+dit_status dit_qgemm_int8_requant(const void* a, const float* a_scale, const void* b,
+                                  const float* b_scale, int64_t m, int64_t n, int64_t k,
+                                  const float* bias, dit_act act, const float* next_scale,
+                                  void* q_next, float* row_amax, void* ws, size_t ws_bytes,
+                                  dit_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
  * PDR outlier ratio and the BF16 route.  [EN] 2.C first bullet, [ZH] 2.C: a layer whose
  * input has a high outlier ratio runs in full precision.  The pages do not define the
  * ratio; reading: the fraction of elements with |x| > k_sigma * RMS(x) over the whole block

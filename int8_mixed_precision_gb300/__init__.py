@@ -238,6 +238,29 @@ def qgemm_int8(a, a_scale, b, b_scale, y, ws, bias=None, acc_debug=None, act=ACT
     _check(st, "dit_qgemm_int8")
 
 
+def qgemm_int8_requant(a, a_scale, b, b_scale, next_scale, q_next, row_amax, ws, bias=None, act=ACT_NONE,
+                       stream=None):
+    """INT8 GEMM (bf16-held codes) whose epilogue quantises its output for the next INT8 layer
+    with the caller's per-token scales next_scale [m]: q_next [m, n] receives the bf16-held codes
+    dit_hadamard_quant_int8(output, 64) would write with those scales, row_amax [m] (zero-filled
+    by the caller) the output's exact per-row max|H z| / 8."""
+    if a.dtype != _torch().bfloat16 or b.dtype != _torch().bfloat16:
+        raise DitError("qgemm_int8_requant: a and b must be bf16-held codes")
+    if a.dim() != 2 or b.dim() != 2 or b.shape[1] != a.shape[1]:
+        raise DitError("qgemm_int8_requant: a [m, k] and b [n, k] codes with the same k")
+    m, n, k = a.shape[0], b.shape[0], a.shape[1]
+    _need(a_scale, 4 * m, "a_scale")
+    _need(b_scale, 4 * n, "b_scale")
+    _need(next_scale, 4 * m, "next_scale")
+    _need(row_amax, 4 * m, "row_amax")
+    _need(q_next, 2 * m * n, "q_next")
+    _bias_ok(bias, n)
+    _same_device(a, a_scale, b, b_scale, bias, next_scale, q_next, row_amax, ws)
+    st = lib().dit_qgemm_int8_requant(_p(a), _p(a_scale), _p(b), _p(b_scale), m, n, k, _p(bias), act,
+                                      _p(next_scale), _p(q_next), _p(row_amax), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "dit_qgemm_int8_requant")
+
+
 def tdc_step(mode, x_in, ws, x_out=None, x_out_skip=None, d1=None, d_new=None, gamma=None,
              sim=None, stream=None):
     for name, t in (("x_out", x_out), ("x_out_skip", x_out_skip), ("d1", d1), ("d_new", d_new)):

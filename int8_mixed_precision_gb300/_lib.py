@@ -36,6 +36,8 @@ SIGNATURES = {
     "dit_nvfp4_to_int8": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp, _i32, _vp, _vp]),
     "dit_qgemm_int8": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp, _sz,
                                _vp]),
+    "dit_qgemm_int8_requant": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _vp, _vp, _vp, _sz,
+                                       _vp]),
     "dit_tdc_step": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _sz, _vp]),
     "dit_tdc_state_init": (None, [_vp]),
     "dit_tdc_decide": (_i32, [_vp, ctypes.c_double]),

@@ -168,6 +168,9 @@ namespace dit6 {
 dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
                         int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
                         void* ws, size_t ws_bytes, cudaStream_t st);
+dit_status gemm_int8_tc_requant(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
+                                int64_t n, int64_t k, const float* bias, bool gelu, const float* next_scale,
+                                void* q_next, float* amax_out, void* ws, cudaStream_t st);
 }
 
 extern "C" dit_status dit_qgemm_int8(const void* a, const float* a_scale, const void* b,
@@ -209,4 +212,25 @@ extern "C" dit_status dit_qgemm_int8(const void* a, const float* a_scale, const 
                  ta, tb, a_scale, b_scale, (int)m, (int)n, (int)k, bias, y, epi, acc_debug, ws) != cudaSuccess)
     return DIT_ERR_CUDA;
   return DIT_OK;
+}
+
+// INT8 GEMM with the requantising epilogue ([EN] 2.A Mechanism 3, 2.A Outlier Smoothing): the
+// output quantised for the next INT8 layer with caller-supplied per-token scales, on the
+// CTA-pair kernel (bf16-held codes).
+extern "C" dit_status dit_qgemm_int8_requant(const void* a, const float* a_scale, const void* b,
+                                             const float* b_scale, int64_t m, int64_t n, int64_t k,
+                                             const float* bias, dit_act act, const float* next_scale,
+                                             void* q_next, float* row_amax, void* ws, size_t ws_bytes,
+                                             dit_stream_t stream) {
+  if (!a || !b || !a_scale || !b_scale || !next_scale || !q_next || !row_amax || !ws || ws_bytes < WS_BYTES)
+    return DIT_ERR_INVALID_ARG;
+  if (m <= 0 || n <= 0 || k <= 0 || m > 0x7fffffff || n > 0x7fffffff || k > 0x7fffffff)
+    return DIT_ERR_INVALID_ARG;
+  if (act != DIT_ACT_NONE && act != DIT_ACT_GELU_ERF) return DIT_ERR_INVALID_ARG;
+  if (k % 16 || n % 64) return DIT_ERR_UNSUPPORTED;
+  if (!aligned32(a) || !aligned32(b) || !aligned32(q_next) || !aligned32(ws) ||
+      (reinterpret_cast<uintptr_t>(b_scale) & 15) || (bias && (reinterpret_cast<uintptr_t>(bias) & 15)))
+    return DIT_ERR_ALIGNMENT;
+  return gemm_int8_tc_requant(a, a_scale, b, b_scale, m, n, k, bias, act == DIT_ACT_GELU_ERF, next_scale, q_next,
+                              row_amax, ws, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -68,16 +68,22 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // chunk buffer by arriving on the leader's chunk-empty barrier.  Tensor memory is allocated and
 // freed by one warp in each CTA together (cta_group::2).
 // ------------------------------------------------------------------------------------------
-struct PairCfg {
+// EPW: epilogue warps, 4 per tensor-memory lane quarter x (EPW / 4) column groups of CW.
+template <int EPW>
+struct PairCfgT {
   static constexpr int STAGES = 6;
   static constexpr int B_BYTES = 128 * BK * 2;                 // this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;        // 32 KB
-  static constexpr int EPI_WARPS = 8;
-  static constexpr int CW = 128;
+  static constexpr int EPI_WARPS = EPW;
+  static constexpr int CW = 256 / (EPW / 4);                    // accumulator columns per thread
   static constexpr int THREADS = (2 + EPI_WARPS) * 32;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
   static constexpr int TMEM_COLS = 512;                         // two 256-column chunk buffers
 };
+using PairCfg = PairCfgT<8>;
+// the requantising epilogue runs sixteen warps of 64 columns (its per-thread work is heavier)
+template <bool REQ>
+using PairCfgFor = PairCfgT<REQ ? 16 : 8>;
 
 __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
@@ -85,6 +91,72 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
+}
+
+// Arguments of the requantising epilogue (REQ): the next INT8 linear's per-token scales, the
+// per-row maxima it reports, and the Hadamard normalisation 1/sqrt(64).
+struct ReqArgs {
+  const float* scale;  // [M] s of the next layer's per-token quantisation (caller-supplied)
+  float* amax;         // [M] max |H z| / 8 over the row, atomically maxed (caller zero-fills)
+  float inv_sqrt_b;
+};
+
+// The requantising epilogue of one thread's CW accumulator columns of output row `row` (CW / 64
+// units of 64 columns of the next layer's K): z = act((acc * s_a) * s_w (+ bias)) rounded to bf16 as
+// the unfused path stores it; y = FWHT64(z) * 1/8 in the INT8 quantiser's stage order;
+// q = clamp(RN(y * RN(1/s)), -127, 127) stored as bf16-held codes; the unit maxima of |y| go to
+// req.amax[row].  With s = max_row |y| / 127 these are the quantiser's codes bit for bit.
+template <bool GELU, int CW>
+__device__ __forceinline__ void requant_row(const int (&acc)[CW], int row, int col0, int M, int N,
+                                            const float* __restrict__ a_scale, const float* __restrict__ b_scale,
+                                            const float* __restrict__ bias, void* __restrict__ q_out,
+                                            const ReqArgs& req) {
+  if (row >= M || col0 >= N) return;
+  const float sa = a_scale[row];
+  const float2 sa2 = make_float2(sa, sa);
+  const float s = req.scale[row];
+  const float inv = s == 0.f ? 0.f : __frcp_rn(s);
+  const float2 iv = make_float2(inv, inv), isb = make_float2(req.inv_sqrt_b, req.inv_sqrt_b);
+  float tmax = 0.f;
+#pragma unroll
+  for (int u = 0; u < CW / 64; ++u) {
+    const int cu = col0 + 64 * u;
+    if (cu >= N) break;  // N % 64 == 0: a unit is whole or absent
+    float2 z[32];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {  // four columns per step, as the plain epilogue rounds them
+      const int c = 64 * u + 4 * j;
+      const float4 sb = reinterpret_cast<const float4*>(b_scale + col0 + c)[0];
+      float2 lo = mul2(mul2(make_float2((float)acc[c], (float)acc[c + 1]), sa2), make_float2(sb.x, sb.y));
+      float2 hi = mul2(mul2(make_float2((float)acc[c + 2], (float)acc[c + 3]), sa2), make_float2(sb.z, sb.w));
+      if (bias) {
+        const float4 bb = reinterpret_cast<const float4*>(bias + col0 + c)[0];
+        lo = add2(lo, make_float2(bb.x, bb.y));
+        hi = add2(hi, make_float2(bb.z, bb.w));
+      }
+      if (GELU) {
+        lo = gelu_erf2(lo);
+        hi = gelu_erf2(hi);
+      }
+      z[2 * j] = bf16x2_to_f2(f2_to_bf16x2(lo.x, lo.y));
+      z[2 * j + 1] = bf16x2_to_f2(f2_to_bf16x2(hi.x, hi.y));
+    }
+    fwht64<64>(z);
+#pragma unroll
+    for (int p = 0; p < 32; ++p) z[p] = mul2(z[p], isb);
+    tmax = fmaxf(tmax, amax_range(z, 0, 32));
+    U8x32 o[4];
+#pragma unroll
+    for (int p = 0; p < 32; ++p) {
+      const float2 a = mul2(z[p], iv);
+      const float q0 = fminf(fmaxf(rintf(a.x), -127.f), 127.f), q1 = fminf(fmaxf(rintf(a.y), -127.f), 127.f);
+      o[p / 8].w[p % 8] = f2_to_bf16x2(q0, q1);
+    }
+    uint16_t* dst = reinterpret_cast<uint16_t*>(q_out) + (int64_t)row * N + cu;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) st256(dst + 16 * c, o[c]);
+  }
+  atomicMax(reinterpret_cast<unsigned*>(req.amax) + row, __float_as_uint(tmax));
 }
 
 // ACCM 0: INT8 codes, exact chunks summed in int32.
@@ -96,14 +168,16 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
 //         tensor-memory chunk, no scales.
 // BANDED: the tile order in bands of N tiles (see tile_mn); a separate instantiation, so that the
 // shapes that keep the plain order run exactly the code they always ran.
-template <bool GELU, int ACCM, bool BANDED>
-__global__ void __launch_bounds__(PairCfg::THREADS, 1)
+// REQ (ACCM 0 only): the epilogue quantises the output for the next INT8 linear (requant_row)
+// instead of storing it; y then receives the bf16-held codes.
+template <bool GELU, int ACCM, bool BANDED, bool REQ = false>
+__global__ void __launch_bounds__(PairCfgFor<REQ>::THREADS, 1)
     k_gemm_int8_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const float* __restrict__ a_scale, const float* __restrict__ b_scale, int M, int N, int K,
                      const float* __restrict__ bias, void* __restrict__ y, int epi, int32_t* __restrict__ acc_out,
-                     void* ws, int stall, int band) {
+                     void* ws, int stall, int band, ReqArgs req) {
   pdl_launch_dependents();
-  using P = PairCfg;
+  using P = PairCfgFor<REQ>;
   constexpr int S = P::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -242,7 +316,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
   } else {  // ------------------------------------------------------ epilogue warps (both CTAs)
     const int e = warp - 2;
     const int q = warp & 3;   // tensor-memory lane quarter of this warp
-    const int half = e >> 2;  // which 128-column half of the 256-column tile
+    const int half = e >> 2;  // which CW-column group of the 256-column tile
     const uint32_t cempty_leader[2] = {mapa_rank(cempty(0), 0), mapa_rank(cempty(1), 0)};
     uint32_t cc = 0;
     bool ok = true;
@@ -281,6 +355,10 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
       if (!ok) break;
       const int row = m0 + q * 32 + lane;
       const int col0 = n0 + half * CW;
+      if constexpr (REQ) {
+        requant_row<GELU, CW>(acc, row, col0, M, N, a_scale, b_scale, bias, y, req);
+        continue;
+      }
       if (row < M && col0 < N) {
         const float sa = ACCM == 2 ? 1.0f : a_scale[row];
         const int64_t off = (int64_t)row * N + col0;
@@ -379,15 +457,15 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
   }
 }
 
-template <bool GELU, int ACCM, bool BANDED>
+template <bool GELU, int ACCM, bool BANDED, bool REQ>
 dit_status launch_pair_k(const CUtensorMap& ta, const CUtensorMap& tb, const float* a_scale, const float* b_scale,
                          int64_t m, int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
-                         void* ws, cudaStream_t st, int band);
+                         void* ws, cudaStream_t st, int band, const ReqArgs& req);
 
-template <bool GELU, int ACCM>
+template <bool GELU, int ACCM, bool REQ = false>
 dit_status launch_pair(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
                        int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out, void* ws,
-                       cudaStream_t st) {
+                       cudaStream_t st, const ReqArgs& req = ReqArgs{}) {
   CUtensorMap ta, tb;
   if (!encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(a), (uint64_t)k, (uint64_t)m,
                       (uint64_t)k * 2, BK, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -404,19 +482,19 @@ dit_status launch_pair(const void* a, const float* a_scale, const void* b, const
   if (band < 1) band = 1;
   if constexpr (ACCM != 2) {
     if (k <= 4096 && band < n_tiles)
-      return launch_pair_k<GELU, ACCM, true>(ta, tb, a_scale, b_scale, m, n, k, bias, y, epi, acc_out, ws, st,
-                                             (int)band);
+      return launch_pair_k<GELU, ACCM, true, REQ>(ta, tb, a_scale, b_scale, m, n, k, bias, y, epi, acc_out, ws, st,
+                                                  (int)band, req);
   }
-  return launch_pair_k<GELU, ACCM, false>(ta, tb, a_scale, b_scale, m, n, k, bias, y, epi, acc_out, ws, st,
-                                          (int)n_tiles);
+  return launch_pair_k<GELU, ACCM, false, REQ>(ta, tb, a_scale, b_scale, m, n, k, bias, y, epi, acc_out, ws, st,
+                                               (int)n_tiles, req);
 }
 
-template <bool GELU, int ACCM, bool BANDED>
+template <bool GELU, int ACCM, bool BANDED, bool REQ>
 dit_status launch_pair_k(const CUtensorMap& ta, const CUtensorMap& tb, const float* a_scale, const float* b_scale,
                          int64_t m, int64_t n, int64_t k, const float* bias, void* y, int epi, int32_t* acc_out,
-                         void* ws, cudaStream_t st, int band) {
-  using P = PairCfg;
-  auto kern = k_gemm_int8_pair<GELU, ACCM, BANDED>;
+                         void* ws, cudaStream_t st, int band, const ReqArgs& req) {
+  using P = PairCfgFor<REQ>;
+  auto kern = k_gemm_int8_pair<GELU, ACCM, BANDED, REQ>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES) != cudaSuccess)
@@ -441,7 +519,7 @@ dit_status launch_pair_k(const CUtensorMap& ta, const CUtensorMap& tb, const flo
   int64_t pairs = clusters;
   if (pairs > items) pairs = items;
   if (launch_pdl(kern, dim3((unsigned)(2 * pairs)), dim3(P::THREADS), P::SMEM_BYTES, st, 2, ta, tb, a_scale,
-                 b_scale, (int)m, (int)n, (int)k, bias, y, epi, acc_out, ws, test_stall(), band) != cudaSuccess)
+                 b_scale, (int)m, (int)n, (int)k, bias, y, epi, acc_out, ws, test_stall(), band, req) != cudaSuccess)
     return DIT_ERR_CUDA;
   return DIT_OK;
 }
@@ -461,6 +539,17 @@ dit_status gemm_int8_tc(const void* a, const float* a_scale, const void* b, cons
              : i8tc::launch_pair<false, 1>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
   return g ? i8tc::launch_pair<true, 0>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st)
            : i8tc::launch_pair<false, 0>(a, a_scale, b, b_scale, m, n, k, bias, y, epi, acc_out, ws, st);
+}
+
+// The INT8 GEMM with the requantising epilogue (exact int32 chunk sums, ACCM 0).
+dit_status gemm_int8_tc_requant(const void* a, const float* a_scale, const void* b, const float* b_scale, int64_t m,
+                                int64_t n, int64_t k, const float* bias, bool gelu, const float* next_scale,
+                                void* q_next, float* amax_out, void* ws, cudaStream_t st) {
+  const i8tc::ReqArgs req{next_scale, amax_out, 0.125f};
+  return gelu ? i8tc::launch_pair<true, 0, true>(a, a_scale, b, b_scale, m, n, k, bias, q_next, EPI_BF16 | EPI_GELU,
+                                                 nullptr, ws, st, req)
+              : i8tc::launch_pair<false, 0, true>(a, a_scale, b, b_scale, m, n, k, bias, q_next, EPI_BF16, nullptr,
+                                                  ws, st, req);
 }
 
 }  // namespace dit6

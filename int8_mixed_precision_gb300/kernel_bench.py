@@ -3,7 +3,7 @@
   python -m int8_mixed_precision_gb300.kernel_bench --case gemm_nvfp4 --m 17776 --n 5760 --k 1920
 
 Cases: quant_int8, quant_nvfp4 (two passes), quant_nvfp4_given (one pass, tensor scale
-given), gamma, tdc_commit, tdc_skip, gemm_int8, gemm_nvfp4, gemm_nvfp4_amax (the GEMM that
+given), gamma, tdc_commit, tdc_skip, gemm_int8, gemm_int8_requant, gemm_nvfp4, gemm_nvfp4_amax (the GEMM that
 also returns its output's NVFP4 tensor scale), outlier_ratio and gemm_bf16 (the PDR
 full-precision route).  Inputs are synthetic bf16 activations (N(0,1), 1% outlier channels
 x50) and N(0,0.02) weights.  Prints one JSON line with the median time and the algorithmic
@@ -94,6 +94,22 @@ def main(argv=None):
         A, W = lin.a4, lin.w.nvfp4
         fn = lambda: dit.qgemm_nvfp4_amax(A["codes"], A["sf"], A["gs"], W["codes"], W["sf"], W["gs"], y, ws,
                                           a.hblock, nxt, act=dit.ACT_GELU_ERF)
+        units, unit = 2 * m * n * k, "TFLOP/s"
+    elif case == "gemm_int8_requant":
+        # FFN up with GELU whose output feeds an INT8 layer: the epilogue quantises the output
+        # with per-token scales supplied (here: the exact ones of an unfused run)
+        x = act(m, k)
+        w = torch.randn(n, k, device=dev, generator=g) * 0.02
+        lin = dit.RoutedLinear(dit.QuantizedWeight(w, a.hblock, ws), m, ws, dev)
+        y = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        lin(x, dit.ROUTE_INT8, y, act=dit.ACT_GELU_ERF)
+        s_next = torch.empty(m, dtype=torch.float32, device=dev)
+        q_next = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        dit.hadamard_quant_int8(y, 64, q_next, s_next)
+        amax = torch.zeros(m, dtype=torch.float32, device=dev)
+        W8 = lin.w.int8
+        fn = lambda: dit.qgemm_int8_requant(lin.a8["q"], lin.a8["scale"], W8["q"], W8["scale"], s_next, q_next, amax,
+                                            ws, act=dit.ACT_GELU_ERF)
         units, unit = 2 * m * n * k, "TFLOP/s"
     elif case == "outlier_ratio":
         x = act(m, k)

@@ -278,6 +278,28 @@ def quant_int8_rows(y: np.ndarray) -> dict:
     return {"q": q, "scale": s, "v": v}
 
 
+def quant_int8_rows_given(y: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """Per-row symmetric INT8 of a transformed float32 tensor y [rows x K] with given per-row
+    scales s: the per-token rule of gist.science (EN) 2.A Mechanism 3 with the scale supplied
+    instead of derived (the fused INT8 epilogue's input; delayed scales are not on the pages):
+
+      v = y * (1 / s)                  (float32: reciprocal rounded, then a product)
+      q = clamp(round-half-even(v), -127, 127)
+
+    s == 0 gives q = 0.  With s = amax_row|y| / 127 this is ``quant_int8_rows``; a smaller s
+    saturates the entries beyond 127 s.
+    """
+    y = np.asarray(y, dtype=np.float32)
+    s = np.asarray(s, dtype=np.float32)
+    zero = s == 0
+    with np.errstate(divide="ignore"):
+        inv = np.where(zero, np.float32(0), np.float32(1.0) / np.where(zero, 1, s)).astype(np.float32)
+    v = (y * inv[:, None]).astype(np.float32)
+    q = np.clip(np.rint(v), -127, 127).astype(np.int8)
+    q[zero] = 0
+    return q
+
+
 def int8_rounding_margin(v: np.ndarray) -> np.ndarray:
     """Relative distance of v to the nearest half-integer (a round-half-even boundary)."""
     v = np.asarray(v, dtype=np.float32).astype(np.float64)

@@ -437,6 +437,49 @@ def test_int8_gemm_timeout_recovers_on_every_pair(shape, monkeypatch):
         assert np.array_equal(host(acc).astype(np.float64), full)
 
 
+@pytest.mark.parametrize("m,n,k,act,with_bias", [(300, 9216, 3072, 1, False), (777, 2048, 1920, 0, True),
+                                                  (1030, 4096, 4096, 1, True)])
+def test_int8_requant_epilogue(m, n, k, act, with_bias, ws):
+    """The INT8 GEMM whose epilogue quantises its output for the next INT8 layer: given the
+    exact per-token scales of that output (from the unfused path: GEMM to bf16, then the INT8
+    quantiser) its codes are the quantiser's bit for bit and its row maxima give the same
+    scales; given half those scales (delayed scales that are too small) the codes are the
+    oracle's given-scale quantisation of the oracle's transform of the stored output."""
+    g = synth.rng(m + 3 * n + k)
+    a = g.integers(-127, 128, (m, k)).astype(np.int8)
+    b = g.integers(-127, 128, (n, k)).astype(np.int8)
+    sa = (g.random(m) * 0.002 + 1e-4).astype(np.float32)
+    sb = (g.random(n) * 0.002 + 1e-4).astype(np.float32)
+    bias = dev_f32(g.standard_normal(n).astype(np.float32)) if with_bias else None
+    ta, tb = _int8_dev(a, torch.bfloat16), _int8_dev(b, torch.bfloat16)
+    act_code = dit.ACT_GELU_ERF if act else dit.ACT_NONE
+    y = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    dit.qgemm_int8(ta, dev_f32(sa), tb, dev_f32(sb), y, ws, bias=bias, act=act_code)
+    q_ref = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    s_ref = torch.empty(m, dtype=torch.float32, device="cuda")
+    dit.hadamard_quant_int8(y, 64, q_ref, s_ref)
+    q = torch.empty_like(q_ref)
+    amax = torch.zeros(m, dtype=torch.float32, device="cuda")
+    dit.qgemm_int8_requant(ta, dev_f32(sa), tb, dev_f32(sb), s_ref, q, amax, ws, bias=bias, act=act_code)
+    _status_clean(ws)
+    assert torch.equal(q.view(torch.int16), q_ref.view(torch.int16))
+    s_from_amax = (host(amax).astype(np.float32) / np.float32(127.0)).astype(np.float32)
+    assert np.array_equal(s_from_amax.view(np.uint32), host(s_ref).view(np.uint32))
+    # delayed scales that are too small: saturation, against the oracle on sampled rows
+    half = (s_ref * 0.5).contiguous()
+    q2 = torch.empty_like(q_ref)
+    amax2 = torch.zeros_like(amax)
+    dit.qgemm_int8_requant(ta, dev_f32(sa), tb, dev_f32(sb), half, q2, amax2, ws, bias=bias, act=act_code)
+    _status_clean(ws)
+    assert torch.equal(amax2, amax)
+    rows = np.unique(np.concatenate([synth.rng(m + 5).choice(m, 16, replace=False), [0, m - 1]]))
+    z = F.bf16_bits_to_f32(host(y)[rows])                   # the output as the unfused path stores it
+    yt = D.block_fwht_f32(z, 64)
+    want = D.quant_int8_rows_given(yt, host(half)[rows])
+    assert np.array_equal(F.bf16_bits_to_f32(host(q2)[rows]).astype(np.int64), want.astype(np.int64))
+    assert (np.abs(want) == 127).any()                      # the half scales do saturate
+
+
 def _adversarial_int8(m, n, k, seed):
     """Operands that push every exact-chunk partial sum towards its 2^24 bound, mix huge and
     unit products after a large running sum, and cancel."""

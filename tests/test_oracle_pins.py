@@ -278,6 +278,33 @@ def test_int8_zero_row():
     assert r["scale"][0] == 0 and not r["q"][0].any() and r["q"][1, 3] == -127
 
 
+def test_int8_given_scales_hand_values_and_saturation():
+    """Quantisation with caller-supplied scales: hand-worked values at s = 0.5 (y/s = 0.48,
+    0.52, 1.5, 2.5, -3.5 -> 0, 1, 2, 2, -4 under round-half-even), saturation at +-127 when y
+    exceeds 127 s, and s = 0 giving zeros."""
+    y = np.array([[0.24, 0.26, 0.75, 1.25, -1.75, 100.0, -100.0],
+                  [1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0]], np.float32)
+    q = D.quant_int8_rows_given(y, np.array([0.5, 0.0], np.float32))
+    assert q[0].tolist() == [0, 1, 2, 2, -4, 127, -127]
+    assert not q[1].any()
+
+
+def test_int8_given_scales_reduce_to_the_dynamic_rule():
+    """With s = amax_row / 127 the given-scale rule is the per-token rule, code for code; with
+    half that scale every |v| beyond 63.5 saturates and the rest double (brute force)."""
+    y = D.block_fwht_f32(synth.activations(16, 128, seed=9, dtype="f32"), 64)
+    r = D.quant_int8_rows(y)
+    assert np.array_equal(D.quant_int8_rows_given(y, r["scale"]), r["q"])
+    half = (r["scale"] * np.float32(0.5)).astype(np.float32)
+    q = D.quant_int8_rows_given(y, half).astype(np.int64)
+    cand = np.arange(-127, 128)
+    for i in range(0, y.size, 37):
+        x = float(np.float32(y.flat[i] * (np.float32(1.0) / half[i // y.shape[1]])))
+        d = np.abs(cand - x)
+        best = cand[d == d.min()]
+        assert q.flat[i] == (best[0] if len(best) == 1 else best[best % 2 == 0][0])
+
+
 # ------------------------------------------------------------------------------- GEMMs
 
 
