@@ -834,6 +834,39 @@ def test_gemm_bounded_wait_reports_timeout_and_recovers(route, monkeypatch):
     assert rel_fro(host(y), ref) <= GEMM_TOL
 
 
+def test_int8_requant_bounded_wait_reports_timeout_and_recovers(monkeypatch):
+    """The requantising INT8 GEMM (sixteen epilogue warps) with a producer that issues no loads:
+    the waits run out, DIT_ERR_TIMEOUT is raised, and the next normal call on the same workspace
+    gives the quantiser's codes bit for bit."""
+    import time
+    ws2 = dit.workspace()
+    m, n, k = 256, 512, 1024
+    g = synth.rng(57)
+    ta = _int8_dev(g.integers(-127, 128, (m, k)).astype(np.int8), torch.bfloat16)
+    tb = _int8_dev(g.integers(-127, 128, (n, k)).astype(np.int8), torch.bfloat16)
+    sa, sb = dev_f32(np.full(m, 1e-3, np.float32)), dev_f32(np.full(n, 1e-3, np.float32))
+    y = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    dit.qgemm_int8(ta, sa, tb, sb, y, ws2)
+    q_ref = torch.empty_like(y)
+    s_ref = torch.empty(m, dtype=torch.float32, device="cuda")
+    dit.hadamard_quant_int8(y, 64, q_ref, s_ref)
+    q = torch.zeros_like(y)
+    amax = torch.zeros(m, dtype=torch.float32, device="cuda")
+    monkeypatch.setenv("DIT6_TEST_STALL_PRODUCER", "1")
+    t0 = time.time()
+    dit.qgemm_int8_requant(ta, sa, tb, sb, s_ref, q, amax, ws2)
+    torch.cuda.synchronize()
+    assert dit.device_status(ws2) & (1 << 5), "DIT_ERR_TIMEOUT not raised"
+    assert time.time() - t0 < 30.0
+    monkeypatch.delenv("DIT6_TEST_STALL_PRODUCER")
+    dit.clear_device_status(ws2)
+    amax.zero_()
+    dit.qgemm_int8_requant(ta, sa, tb, sb, s_ref, q, amax, ws2)
+    torch.cuda.synchronize()
+    assert dit.device_status(ws2) == 0
+    assert torch.equal(q.view(torch.int16), q_ref.view(torch.int16))
+
+
 def test_delta_cache_checkpoint_resume(ws):
     """A block's delta cache saved mid-run (decision state + cached delta) and loaded into a
     fresh block continues exactly like the original: same decisions, same outputs bit for bit."""
